@@ -1,0 +1,94 @@
+"""Decode attention over the dequantized paged cache.
+
+Sources:
+* "SAW-INT4 ...", section 3 (fused engine): attention reads the compact
+  cache; rotation and quantization are undone on the fly.  This oracle does
+  the plain thing instead: it dequantizes every cached vector, undoes the
+  rotation by explicit matrix multiply, and runs ordinary softmax attention.
+* "LogQuant ...", Methodology section 4 (position-agnostic optimisation):
+  attention output does not depend on the order of the (key, value) pairs,
+  A V = A_P V_P, so full-precision window tokens and quantized tokens may be
+  combined in any order.
+* CriticalKV technical summary, Methodology (perturbation definition): the L1
+  distance between two attention outputs, used here to report quantization
+  error.
+
+Readings: scores are (q . k) * softmax_scale with softmax_scale = 1/sqrt(d)
+by default; one decode query attends to every cached token of its sequence
+(no causal mask); query head h reads KV head h // (Hq / Hkv); the output is
+float64 here and float32 on the GPU; a sequence of length 0 yields zeros.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import layout
+from .cache import CacheState
+from .hadamard import unrotate
+from .quantizer import dequantize
+
+
+def softmax_attention(q: np.ndarray, keys: np.ndarray, values: np.ndarray,
+                      scale: float) -> np.ndarray:
+    """o = softmax(keys q * scale) values for q[G, d], keys/values[T, d] (float64)."""
+    q = np.asarray(q, dtype=np.float64)
+    if keys.shape[0] == 0:
+        return np.zeros((q.shape[0], values.shape[-1]))
+    s = (q @ np.asarray(keys, dtype=np.float64).T) * scale        # [G, T]
+    s = s - s.max(axis=1, keepdims=True)
+    p = np.exp(s)
+    p /= p.sum(axis=1, keepdims=True)
+    return p @ np.asarray(values, dtype=np.float64)
+
+
+def cached_kv(state: CacheState, layer: int, b: int, h: int, length: int,
+              page_table: np.ndarray):
+    """Reconstructed (keys, values) float64 [length, d] of (sequence b, KV head h)."""
+    r = state.window
+    lq = max(0, length - r) if r else length
+    d = state.head_dim
+    view = state.view(layer)
+    pos = np.arange(lq)
+    pages = np.asarray(page_table[b, pos // layout.PAGE_SIZE], dtype=np.int64)
+    slots = pos % layout.PAGE_SIZE
+    out = []
+    for kv in (0, 1):
+        if lq:
+            codes, s, z = view.read(pages, slots, h, kv)
+            rec = unrotate(dequantize(codes, s, z), state.had_block)
+        else:
+            rec = np.zeros((0, d))
+        if length > lq:
+            wpos = np.arange(lq, length) % r
+            win = state.windows[layer][b, h, kv, wpos].astype(np.float64)
+            rec = np.concatenate([rec, win], axis=0)
+        out.append(rec)
+    return out[0], out[1]
+
+
+def decode(state: CacheState, layer: int, q: np.ndarray, page_table: np.ndarray,
+           seq_lens: np.ndarray, scale: float | None = None,
+           pairs: list | None = None) -> np.ndarray:
+    """o[B, Hq, d] float64 for queries q[B, Hq, d].
+
+    ``pairs`` optionally restricts the work to a list of (b, kv_head); the
+    other rows are left as NaN (used to sample full-size workloads).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    bsz, hq, d = q.shape
+    hkv = state.num_kv_heads
+    g = hq // hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    o = np.full((bsz, hq, d), np.nan)
+    todo = pairs if pairs is not None else [(b, h) for b in range(bsz) for h in range(hkv)]
+    for b, h in todo:
+        keys, values = cached_kv(state, layer, b, h, int(seq_lens[b]), page_table)
+        o[b, h * g:(h + 1) * g] = softmax_attention(q[b, h * g:(h + 1) * g], keys, values,
+                                                    scale)
+    return o
+
+
+def l1_perturbation(o: np.ndarray, o_hat: np.ndarray) -> float:
+    """CriticalKV's output perturbation || o - o_hat ||_1 (summed over all rows)."""
+    return float(np.abs(np.asarray(o, np.float64) - np.asarray(o_hat, np.float64)).sum())

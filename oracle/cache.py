@@ -1,0 +1,104 @@
+"""Quantize-on-append into the paged cache, plus the bf16 recent-token window.
+
+Sources:
+* "SAW-INT4 ...", summary and section 2: each new K/V head vector is rotated
+  by a block-diagonal Hadamard transform and quantized token-wise; section 1:
+  the cache lives in uniform fixed-size pages.
+* RateQuant technical summary, Methodology section 3: K and V of every
+  (layer, head) are separate components with their own bit-widths
+  (the per-layer table ``bits[h] = (bK, bV)``).
+* "LogQuant: Log-Distributed 2-Bit Quantization of KV Cache ...",
+  Methodology section 2 (window configuration / full-precision reserve): the
+  most recent tokens are kept at full precision.
+
+Semantics (readings where the pages are silent):
+* Position p of sequence b lives in logical page p // 16 at slot p % 16;
+  ``page_table[b, p // 16]`` names the physical page.
+* With a window of R > 0 tokens, after an append the last min(L, R)
+  positions of a sequence of length L are held as bf16 in a ring indexed by
+  p mod R; positions p < L - R are quantized.  A token is quantized when it
+  leaves the window (its bf16 value is read from the ring) or directly from
+  the appended input if it never enters the window.
+* With R = 0 every appended token is quantized.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import List, Optional
+
+import numpy as np
+
+from . import layout
+from .quantizer import rotate_and_quantize
+
+
+@dataclasses.dataclass
+class CacheState:
+    head_dim: int
+    had_block: int
+    window: int
+    bits: np.ndarray                 # int [L, Hkv, 2]
+    pools: List[np.ndarray]          # per layer uint8 [num_pages, page_bytes]
+    windows: Optional[List[np.ndarray]]  # per layer float32 [Bmax, Hkv, 2, R, d] or None
+
+    @property
+    def num_kv_heads(self) -> int:
+        return int(self.bits.shape[1])
+
+    def view(self, layer: int) -> layout.PageView:
+        return layout.PageView(self.pools[layer], self.head_dim, self.bits[layer])
+
+
+def new_state(num_layers: int, num_pages: int, head_dim: int, had_block: int,
+              bits: np.ndarray, window: int = 0, max_batch: int = 0) -> CacheState:
+    bits = np.asarray(bits, dtype=np.int64).reshape(num_layers, -1, 2)
+    hkv = bits.shape[1]
+    pools = [np.zeros((num_pages, layout.page_bytes(head_dim, bits[l])), dtype=np.uint8)
+             for l in range(num_layers)]
+    wins = None
+    if window:
+        wins = [np.zeros((max_batch, hkv, 2, window, head_dim), dtype=np.float32)
+                for _ in range(num_layers)]
+    return CacheState(head_dim, had_block, window, bits, pools, wins)
+
+
+def append(state: CacheState, layer: int, k: np.ndarray, v: np.ndarray,
+           page_table: np.ndarray, seq_lens: np.ndarray) -> dict:
+    """Append k, v [B, T_new, Hkv, d] (bf16-exact float32) after seq_lens[b] tokens.
+
+    Mutates ``state`` and returns, for tests, a dict keyed by (b, h, kv) of
+    (positions, codes, s, z, u32): the positions quantized by this call, what
+    was written for them, and the float32-rounded rotated vectors.
+    """
+    k = np.asarray(k, dtype=np.float32)
+    v = np.asarray(v, dtype=np.float32)
+    bsz, t_new, hkv, d = k.shape
+    r = state.window
+    view = state.view(layer)
+    written = {}
+    for b in range(bsz):
+        l0 = int(seq_lens[b])
+        l_end = l0 + t_new
+        q_old = max(0, l0 - r) if r else l0
+        q_new = max(0, l_end - r) if r else l_end
+        pos = np.arange(q_old, q_new)
+        from_ring = pos < l0                  # leaving the window: bf16 value in the ring
+        for kv, src in ((0, k), (1, v)):
+            for h in range(hkv):
+                if not len(pos):
+                    continue
+                bits = int(state.bits[layer, h, kv])
+                vecs = np.empty((len(pos), d), dtype=np.float32)
+                if from_ring.any():
+                    vecs[from_ring] = state.windows[layer][b, h, kv, pos[from_ring] % r]
+                if (~from_ring).any():
+                    vecs[~from_ring] = src[b, pos[~from_ring] - l0, h]
+                codes, s, z, u32 = rotate_and_quantize(vecs, state.had_block, bits)
+                pages = np.asarray(page_table[b, pos // layout.PAGE_SIZE], dtype=np.int64)
+                view.write_many(pages, pos % layout.PAGE_SIZE, h, kv, codes, s, z)
+                written[(b, h, kv)] = (pos, codes, s, z, u32)
+        if r:
+            for p in range(max(l0, q_new), l_end):
+                state.windows[layer][b, :, 0, p % r] = k[b, p - l0]
+                state.windows[layer][b, :, 1, p % r] = v[b, p - l0]
+    return written
