@@ -1,0 +1,426 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized KV-cache hot path on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {kvq,reference}]
+
+One JSON line on stdout (rank 0).
+
+Workload (the decode configuration the headline metric is quoted on): a
+Llama-3-8B-shaped decode layer -- batch 16, 32 query / 8 KV heads, head_dim
+128, context 4096, K and V INT4 token-wise with Hadamard block 128, page 16 --
+replicated over 32 distinct layer caches (2.3 GB of packed KV, far above the
+126 MB L2), so every step streams its cache from HBM.
+
+A step is one serving decode step through all 32 layers: per layer, kvq_append
+quantizes the new token of each of the 16 sequences into the paged cache
+(rotation, scale/zero, codes, paged store) and kvq_decode_attn runs split-K
+attention over the 4096 cached tokens (query rotation, page streaming,
+dequantization in registers, online softmax, combine).  The bit-widths come
+from kvq_alloc_bits at set-up (this workload's widths are uniform: 4 and 4).
+The step is captured once in a CUDA graph and replayed.
+
+value = algorithmic decode bytes of a step (packed codes + fp16 scale/zero per
+(token, KV head): 136 B for K4V4) / step time, summed over ranks.  The
+"roofline" object is the decode kernel alone, timed by CUDA-event nodes around
+each decode launch inside the replayed step.  "append" adds the quantize-on-
+append sweep (8 sequences x 8192 new tokens, every Hadamard block and bit
+width) in tokens/s.  "cpu_baseline" times the CPU oracle on a bounded sample.
+
+--impl reference times the CPU oracle itself as the reference arm (this
+library has no third-party reference implementation to install).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import (APPEND_BITS, APPEND_BLOCKS, APPEND_SWEEP, LLAMA3_8B_LAYER,  # noqa: E402
+                       kv_tokens, page_table, queries)
+
+METRIC = "quantized-KV decode attention GB/s (% of HBM peak); append tokens/s"
+N_LAYERS = 32
+W = LLAMA3_8B_LAYER
+
+
+def unit_bytes(d: int, bk: int, bv: int) -> int:
+    """Algorithmic bytes per (token, KV head): packed K and V codes + fp16 (s, z) x 2."""
+    return d * (bk + bv) // 8 + 8
+
+
+def decode_bytes_per_layer() -> int:
+    return W.batch * W.ctx * W.hkv * unit_bytes(W.head_dim, 4, 4)
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self) -> dict:
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------- oracle legs
+
+def oracle_sample(n_seqs: int, repeats: int):
+    """Time the CPU oracle on a bounded sample of the workload.
+
+    The sample is n_seqs of the 16 sequences of one layer: the oracle fills its
+    own cache for them (untimed), then each timed repeat is one decode step for
+    them -- append of the new token and attention over 4096 tokens for all 8
+    KV heads / 32 query heads.  Returns (GB/s over the same algorithmic bytes,
+    seconds per repeat, BLAS threads, description)."""
+    from oracle import attention, cache as ocache
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:  # noqa: BLE001
+        threads = 1
+    d, hkv = W.head_dim, W.hkv
+    ctx = W.ctx
+    k = kv_tokens(W.seed, 0, n_seqs, ctx, hkv, d, W.k_outliers, W.outlier_lo, W.outlier_hi)
+    v = kv_tokens(W.seed, 1, n_seqs, ctx, hkv, d, W.v_outliers, W.outlier_lo, W.outlier_hi)
+    mp = ctx // 16
+    pt = page_table(W.seed, n_seqs, mp)
+    st = ocache.new_state(1, n_seqs * mp, d, W.had_block, np.full((1, hkv, 2), 4))
+    ocache.append(st, 0, k[:, :ctx - 1], v[:, :ctx - 1], pt, np.zeros(n_seqs, np.int32))
+    q = queries(W.seed, 0, n_seqs, W.hq, d, False).astype(np.float64)
+    before = np.full(n_seqs, ctx - 1, np.int32)
+    after = before + 1
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        ocache.append(st, 0, k[:, ctx - 1:], v[:, ctx - 1:], pt, before)
+        attention.decode(st, 0, q, pt, after)
+        times.append(time.perf_counter() - t0)
+    sec = statistics.median(times)
+    nbytes = n_seqs * ctx * hkv * unit_bytes(d, 4, 4)
+    desc = (f"{n_seqs} of {W.batch} sequences x 8 KV heads x {ctx} tokens of one layer "
+            f"(one decode step: append 1 token + attention), median of {repeats}")
+    return nbytes / sec / 1e9, sec, threads, desc
+
+
+def run_reference(args) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    sec_total = 0.0
+    n_seqs = 2
+    for _ in range(args.warmup):
+        oracle_sample(n_seqs, 1)
+    gbs, sec, threads, desc = oracle_sample(n_seqs, max(1, args.steps))
+    sec_total = sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec_total * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict() -> dict:
+    return {"workload": "llama3-8b-decode-layer x 32 layer caches",
+            "batch": W.batch, "q_heads": W.hq, "kv_heads": W.hkv, "head_dim": W.head_dim,
+            "context": W.ctx, "bits": "K4V4", "had_block": W.had_block, "page": 16,
+            "layers": N_LAYERS, "step": "per layer: append 1 token/seq + split-K decode",
+            "l2": "inputs larger than L2: 32 distinct layer caches, 2.28 GB of packed KV per step",
+            "parallelism": "replicas (weak scaling), no collective on the data path"}
+
+
+# ------------------------------------------------------------------------- GPU leg
+
+def run_kvq(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    import quantized_decode_attention_diag_b300 as kvq
+    from quantized_decode_attention_diag_b300 import build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+
+    # CPU baseline first (rank 0 only), before the first kernel runs
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, sec, threads, desc = oracle_sample(2, 3)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": desc}
+
+    d, hkv, hq, bsz, ctx = W.head_dim, W.hkv, W.hq, W.batch, W.ctx
+    # bit-widths from the allocator (uniform sensitivities, only width 4 allowed)
+    bits, _ = kvq.kvq_alloc_bits([1.0] * (N_LAYERS * hkv * 2), [4.0] * (N_LAYERS * hkv * 2),
+                                 4 * N_LAYERS * hkv * 2, [kvq.mask_of([4])] * (N_LAYERS * hkv * 2))
+    bits = np.array(bits).reshape(N_LAYERS, hkv, 2)
+    mp = ctx // 16
+    cache = kvq.Cache(N_LAYERS, hkv, d, W.had_block, bits, bsz * mp, device=dev)
+    pt = torch.from_numpy(page_table(W.seed, bsz, mp)).to(dev)
+
+    # prefill every layer cache with the first ctx-1 tokens (one layer's data, 32 caches)
+    k = kv_tokens(W.seed, 0, bsz, ctx, hkv, d, W.k_outliers, W.outlier_lo, W.outlier_hi)
+    v = kv_tokens(W.seed, 1, bsz, ctx, hkv, d, W.v_outliers, W.outlier_lo, W.outlier_hi)
+    kd = torch.from_numpy(k).to(dev).to(torch.bfloat16)
+    vd = torch.from_numpy(v).to(dev).to(torch.bfloat16)
+    zero = torch.zeros(bsz, dtype=torch.int32, device=dev)
+    for l in range(N_LAYERS):
+        cache.append(l, kd[:, :ctx - 1].contiguous(), vd[:, :ctx - 1].contiguous(), pt, zero)
+    knew = kd[:, ctx - 1:].contiguous().unsqueeze(0).repeat(N_LAYERS, 1, 1, 1, 1).contiguous()
+    vnew = vd[:, ctx - 1:].contiguous().unsqueeze(0).repeat(N_LAYERS, 1, 1, 1, 1).contiguous()
+    del kd, vd
+    q_host = np.stack([queries(W.seed, l, bsz, hq, d, False) for l in range(N_LAYERS)])
+    q_all = torch.from_numpy(q_host).to(dev).to(torch.bfloat16)
+    o_all = torch.empty((N_LAYERS, bsz, hq, d), dtype=torch.float32, device=dev)
+    before = torch.full((bsz,), ctx - 1, dtype=torch.int32, device=dev)
+    after = before + 1
+    ws = cache.workspace(bsz, hq, mp)
+    torch.cuda.synchronize(dev)
+    assert cache.get_status() == 0
+
+    stream = torch.cuda.Stream(device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True, external=True),
+           torch.cuda.Event(enable_timing=True, external=True)) for _ in range(N_LAYERS)]
+
+    def step():
+        for l in range(N_LAYERS):
+            cache.append(l, knew[l], vnew[l], pt, before)
+            ev[l][0].record()
+            cache.decode(l, q_all[l], pt, after, o=o_all[l], workspace=ws)
+            ev[l][1].record()
+
+    with torch.cuda.stream(stream):
+        step()                                   # eager warm-up outside capture
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    torch.cuda.synchronize(dev)
+
+    def timed(fn, k_steps):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            t0.record()
+            for _ in range(k_steps):
+                fn()
+            t1.record()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        ms = t0.elapsed_time(t1) / k_steps
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            graph.replay()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        ms = timed(graph.replay, args.steps)
+    dec_ms = [ev[l][0].elapsed_time(ev[l][1]) for l in range(N_LAYERS)]   # last replay
+    assert cache.get_status() == 0, f"device status {cache.get_status():#x}"
+
+    # end to end: pinned host inputs -> device, step, o -> pinned host
+    knew_h = knew.cpu().pin_memory()
+    vnew_h = vnew.cpu().pin_memory()
+    q_h = q_all.cpu().pin_memory()
+    o_h = torch.empty(o_all.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        q_all.copy_(q_h, non_blocking=True)
+        knew.copy_(knew_h, non_blocking=True)
+        vnew.copy_(vnew_h, non_blocking=True)
+        graph.replay()
+        o_h.copy_(o_all, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        with torch.cuda.stream(stream):
+            e2e_step()
+    ms_e2e = timed(e2e_step, args.steps)
+    h2d = q_h.numel() * 2 + knew_h.numel() * 2 + vnew_h.numel() * 2
+    d2h = o_h.numel() * 4
+
+    # append sweep: 8 sequences x 8192 new tokens into empty caches
+    append = append_sweep(kvq, torch, dev) if not args.skip_append else None
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    pk = peaks()
+    step_bytes = N_LAYERS * decode_bytes_per_layer()
+    gbs = world * step_bytes / (ms * 1e-3) / 1e9
+    dec_avg = statistics.mean(dec_ms)
+    achieved = decode_bytes_per_layer() / (dec_avg * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u4 codes, fp16 MMA, fp32 accumulate", "data": "synthetic",
+        "config": config_dict(),
+        "frac_of_hbm": round(gbs / world / pk["hbm_gbs"], 4),
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel<128> (split-K decode + combine)",
+                     "achieved": round(achieved, 2), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / pk["hbm_gbs"], 4),
+                     "peak_source": pk["source"], "traffic": None,
+                     "algorithmic_bytes_per_launch": decode_bytes_per_layer(),
+                     "avg_launch_us": round(dec_avg * 1e3, 3)},
+        "e2e": {"value": round(world * step_bytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(ms_e2e, 4)},
+        "gpu_launches": 2 * N_LAYERS * args.steps,
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+        "append": append,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def append_sweep(kvq, torch, dev) -> dict:
+    w = APPEND_SWEEP
+    bsz, t, hkv, d = w.batch, w.new_tokens, w.hkv, w.head_dim
+    k = kv_tokens(w.seed, 0, bsz, t, hkv, d, w.k_outliers, w.outlier_lo, w.outlier_hi)
+    v = kv_tokens(w.seed, 1, bsz, t, hkv, d, w.v_outliers, w.outlier_lo, w.outlier_hi)
+    kd = torch.from_numpy(k).to(dev).to(torch.bfloat16)
+    vd = torch.from_numpy(v).to(dev).to(torch.bfloat16)
+    del k, v
+    mp = t // 16
+    pt = torch.from_numpy(page_table(w.seed, bsz, mp)).to(dev)
+    zero = torch.zeros(bsz, dtype=torch.int32, device=dev)
+    pk = peaks()
+    points = []
+    tokens = bsz * t
+    for block in APPEND_BLOCKS:
+        for bits in APPEND_BITS:
+            c = kvq.Cache(1, hkv, d, block, np.full((1, hkv, 2), bits), bsz * mp, device=dev)
+            for _ in range(3):
+                c.append(0, kd, vd, pt, zero)
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            reps = 10
+            e0.record()
+            for _ in range(reps):
+                c.append(0, kd, vd, pt, zero)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            assert c.get_status() == 0
+            sec = e0.elapsed_time(e1) / reps * 1e-3
+            nbytes = tokens * hkv * 2 * (d * 2 + d * bits // 8 + 4)
+            points.append({"block": block, "bits": bits, "us": round(sec * 1e6, 2),
+                           "tokens_per_s": round(tokens / sec, 1),
+                           "GB_s": round(nbytes / sec / 1e9, 1),
+                           "frac": round(nbytes / sec / 1e9 / pk["hbm_gbs"], 4)})
+            del c
+    return {"workload": "append-sweep 8 seqs x 8192 new tokens, 8 KV heads, head_dim 128",
+            "bytes": "bf16 K/V read + packed codes + fp16 (s, z) written",
+            "unit": "tokens/s", "points": points}
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-append", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_kvq(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,194 @@
+/*
+ * kvq.h -- C ABI of the quantized KV-cache library for NVIDIA B300 (sm_103a).
+ *
+ * Two hot-path calls and one host utility:
+ *
+ *   kvq_append       quantize-on-append: block-diagonal Walsh-Hadamard rotation
+ *                    of each new K/V head vector, token-wise asymmetric INT-b
+ *                    quantization with one fp16 scale and zero per (token, head),
+ *                    packed into a paged cache; optional bf16 recent-token window.
+ *   kvq_decode_attn  split-K decode attention that reads the packed codes,
+ *                    dequantizes in registers and scores them against the
+ *                    once-rotated query; merges the bf16 window; writes fp32 o.
+ *   kvq_alloc_bits   RateQuant greedy marginal-gain allocation of per-component
+ *                    bit-widths (host only).
+ *
+ * Conventions shared by every call
+ *   - Every pointer marked "device" is caller-owned device memory (e.g. from
+ *     PyTorch).  The library allocates no memory and never synchronises a
+ *     stream; kernels are launched on the stream passed in (NULL = legacy
+ *     default stream).
+ *   - Arguments that can be checked on the host are checked before any launch;
+ *     a failed check returns KVQ_EINVAL / KVQ_EUNSUPPORTED and launches nothing.
+ *     kvq_last_error() then holds a message (thread-local).
+ *   - Errors that only the device can see (a page id outside [0, num_pages), a
+ *     sequence longer than its page-table row, a vector whose scale or zero is
+ *     not finite in fp16, an asynchronous copy that did not complete in time)
+ *     are OR-ed into the cache's device status word; the affected work is
+ *     skipped, nothing traps.  Read it with kvq_get_status() after
+ *     synchronising the stream.
+ *   - Position p of sequence b lives in logical page p / 16, slot p % 16;
+ *     page_table[b * max_pages + p / 16] names the physical page.
+ *
+ * Page layout (layer l; a convention of this library -- the pages only say that
+ * a paged-attention server stores the cache in uniform blocks):
+ *   for each KV head h = 0 .. Hkv-1, a contiguous 16-byte-aligned segment
+ *     K codes  [16][head_dim * bK / 8]   token-major
+ *     V codes  [16][head_dim * bV / 8]
+ *     K (s, z) [16] x {fp16 s, fp16 z}
+ *     V (s, z) [16] x {fp16 s, fp16 z}
+ *   codes packed little-endian: element j at bit (j * b) % 8 of byte (j * b) / 8.
+ *   page_bytes(l) = sum_h 16 * (head_dim * (bK_h + bV_h) / 8 + 8).
+ *
+ * Rotation and quantizer (what a stored vector means)
+ *   u = H_blk x, H_blk = diag(H_n, ..., H_n), H_n the Sylvester Hadamard matrix
+ *   (entries (-1)^popcount(i & j), unnormalised).  Per (token, head, K|V):
+ *     z = fp16_round_down(min u),  s = fp16_round_up((max u - z) / (2^b - 1)),
+ *     c_j = round_half_even((u_j - z) * (1 / s)),   deq_j = c_j * s + z,
+ *   with u, u - z and 1 / s rounded to fp32.  Since H_n H_n = n I,
+ *   q . k = (H q) . (H k) / n and x = H u / n.
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_EINVAL = 1,        /* bad argument (null pointer, bad size, misalignment) */
+  KVQ_EUNSUPPORTED = 2,  /* valid but not built: head_dim, block, bits, GQA group */
+  KVQ_ECUDA = 3,         /* a CUDA runtime call failed (message in kvq_last_error) */
+  KVQ_EBUDGET = 4,       /* kvq_alloc_bits: budget below the minimum allocation */
+  KVQ_EDEVICE = 5,       /* kvq_get_status: the device status word is non-zero */
+  KVQ_EWORKSPACE = 6     /* kvq_decode_attn: workspace smaller than required */
+} kvq_status;
+
+/* Bits of the device status word (OR-ed together by kernels). */
+#define KVQ_DEV_BAD_PAGE      0x1  /* page id outside [0, num_pages) */
+#define KVQ_DEV_BAD_LENGTH    0x2  /* seq_len < 0 or beyond max_pages * 16 */
+#define KVQ_DEV_NONFINITE     0x4  /* scale or zero not finite in fp16 (input out of range) */
+#define KVQ_DEV_COPY_TIMEOUT  0x8  /* an asynchronous page copy did not complete in time */
+
+/* Descriptor of a paged quantized cache.  Plain data; the library keeps no
+ * reference to it after a call returns. */
+typedef struct kvq_cache {
+  int num_layers;
+  int num_kv_heads;          /* Hkv, 1 .. 64 */
+  int head_dim;              /* d: 64 or 128 */
+  int page_size;             /* must be 16 */
+  int had_block;             /* Hadamard block n: 32, 64 or 128, dividing head_dim */
+  int window;                /* R: bf16 recent-token window (0 = none), 0 .. 4096 */
+  int max_batch;             /* sequences addressable in each window buffer */
+  int num_pages;             /* physical pages in each layer pool */
+  const int8_t* bits_host;   /* host [num_layers][num_kv_heads][2] (bK, bV), each 2, 4 or 8 */
+  void* const* layer_pools;  /* host array [num_layers] of device pointers, each
+                                num_pages * kvq_page_bytes(layer) bytes, 16-byte aligned */
+  void* const* window_bufs;  /* host array [num_layers] of device pointers to bf16
+                                [max_batch][Hkv][2][R][head_dim], or NULL when R == 0 */
+  int* status_dev;           /* device int, the sticky status word (may be NULL) */
+} kvq_cache;
+
+/* Bytes of one page of `layer` (layout above); 0 on a bad descriptor. */
+size_t kvq_page_bytes(const kvq_cache* cache, int layer);
+
+/*
+ * kvq_append -- quantize-on-append.
+ * Follows "SAW-INT4: System-Aware 4-Bit KV-Cache Quantization for Real-World LLM
+ * Serving" (summary; section 2, block-diagonal Hadamard rotation before
+ * quantization; section 3, the fused engine doing rotation and quantization in
+ * the same memory pass) and the RateQuant technical summary, Methodology
+ * section 3 (K and V as separate components with their own bit-widths, taken
+ * here from cache->bits_host).  The recent-token window follows "LogQuant:
+ * Log-Distributed 2-Bit Quantization of KV Cache ...", Methodology section 2
+ * (most recent tokens kept at full precision).
+ *
+ *   K, V        device bf16 [B][T_new][Hkv][head_dim], contiguous, 16-byte aligned.
+ *   page_table  device int32 [B][max_pages]; must cover every position written.
+ *   seq_lens    device int32 [B]: tokens already in each sequence BEFORE this call
+ *               (window included); they are not modified.
+ * Appended token i of sequence b takes position p = seq_lens[b] + i.  With R = 0
+ * it is quantized into its page slot.  With R > 0, positions p < L - R (L the new
+ * length) are quantized -- tokens leaving the window are read from the ring slot
+ * p % R of window_bufs[layer] before it is overwritten -- and the last min(L, R)
+ * positions are copied to the ring.  Two appends to one sequence must be
+ * stream-ordered.  Returns KVQ_OK once the kernel is enqueued.
+ */
+kvq_status kvq_append(const kvq_cache* cache, int layer, const void* K, const void* V,
+                      const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                      int B, int T_new, void* stream);
+
+/* Workspace bytes kvq_decode_attn needs for this (B, Hq, max_pages) on the
+ * current device; 0 on a bad argument.  The workspace must be zero-filled once
+ * before its first use (e.g. torch.zeros); every call leaves it ready for the
+ * next.  Two calls that run concurrently must not share a workspace. */
+size_t kvq_decode_workspace_bytes(const kvq_cache* cache, int B, int Hq, int max_pages);
+
+/*
+ * kvq_decode_attn -- one decode step of attention over the quantized cache.
+ * Follows "SAW-INT4 ..." section 3 (attention consumes the compact cache, the
+ * rotation undone on the fly: the query is rotated once, q . k = (H q).(H k)/n),
+ * "LogQuant ..." Methodology section 4 (attention is independent of the order of
+ * the (key, value) pairs, A V = A_P V_P, so split-K partials, quantized pages
+ * and the bf16 window may be combined in any order) and Methodology section 2
+ * (full-precision recent window).
+ *
+ *   q            device [B][Hq][head_dim], bf16 (q_is_fp32 = 0) or fp32 (1).
+ *                Query head h reads KV head h / (Hq / Hkv); Hq / Hkv in {1, 2, 4}.
+ *   seq_lens     device int32 [B]: tokens per sequence INCLUDING the window.
+ *   softmax_scale  multiplies q . k; pass 0 for 1 / sqrt(head_dim).
+ *   o            device fp32 [B][Hq][head_dim], written.  A sequence of length 0
+ *                gets o = 0.
+ *   workspace    device, ws_bytes >= kvq_decode_workspace_bytes(cache, B, Hq,
+ *                max_pages), 16-byte aligned, zero-filled before its first use.
+ * One kernel launch.  Returns KVQ_OK once enqueued.
+ */
+kvq_status kvq_decode_attn(const kvq_cache* cache, int layer, const void* q, int q_is_fp32,
+                           const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                           int B, int Hq, float softmax_scale, float* o, void* workspace,
+                           size_t ws_bytes, void* stream);
+
+/*
+ * kvq_alloc_bits -- RateQuant greedy marginal-gain bit allocation (host only).
+ * Follows the RateQuant technical summary, Methodology section 1 (distortion
+ * model D(b) = alpha * beta^-b, objective min sum_i w_i D_i(b_i) subject to
+ * sum_i b_i = B) and section 3 (integer refinement by a greedy marginal-gain
+ * loop; K and V as 2N independent components with their own beta).
+ *
+ *   w[n]          sensitivities with alpha folded in, > 0.
+ *   beta[n]       distortion decay rates, > 1.
+ *   budget        total bits sum_i b_i may not exceed.
+ *   allowed_mask  [n] (or NULL = {2, 4, 8} for all): bit b set means width b
+ *                 (1 .. 15) is allowed for component i.
+ *   bits_out[n]   written; leftover (may be NULL) receives budget - sum(bits).
+ * Every component starts at its smallest allowed width; while a step fits the
+ * remaining budget, the step to the next allowed width with the largest gain per
+ * bit w_i (beta_i^-b - beta_i^-b') / (b' - b) is taken (ties: lowest index).
+ * Returns KVQ_EBUDGET (bits_out untouched) if the budget is below the minimum.
+ * Component order for a cache: (layer * Hkv + head) * 2 + kv, kv = 0 for K.
+ */
+kvq_status kvq_alloc_bits(const double* w, const double* beta, int n, long long budget,
+                          const uint16_t* allowed_mask, int* bits_out, long long* leftover);
+
+/* Copy the device status word into *device_status (synchronous copy; the caller
+ * synchronises the streams that ran kernels first).  Returns KVQ_EDEVICE when it
+ * is non-zero, KVQ_OK when it is zero. */
+kvq_status kvq_get_status(const kvq_cache* cache, int* device_status);
+
+/* Zero the device status word on `stream`. */
+kvq_status kvq_reset_status(const kvq_cache* cache, void* stream);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* kvq_last_error(void);
+
+/* Library version string, e.g. "kvq 0.1 sm_103a". */
+const char* kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H_ */

@@ -1,0 +1,339 @@
+// C ABI of the quantized KV-cache library: argument checks, page geometry,
+// split planning, kernel dispatch, and the RateQuant greedy allocator.
+#include <cuda_runtime_api.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "kvq.h"
+#include "kvq_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kvq_status fail(kvq_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks the geometry fields of the descriptor and the bits of `layer`; fills
+// the page geometry.  Does not look at the device pointers.
+kvq_status check_geometry(const kvq_cache* c, int layer, kvq::LayerGeom* geom) {
+  if (!c) return fail(KVQ_EINVAL, "cache descriptor is NULL");
+  if (c->num_layers < 1) return fail(KVQ_EINVAL, "num_layers must be >= 1");
+  if (layer < 0 || layer >= c->num_layers)
+    return fail(KVQ_EINVAL, "layer %d outside [0, %d)", layer, c->num_layers);
+  if (c->num_kv_heads < 1 || c->num_kv_heads > kvq::kMaxHeads)
+    return fail(KVQ_EUNSUPPORTED, "num_kv_heads %d outside [1, %d]", c->num_kv_heads,
+                kvq::kMaxHeads);
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(KVQ_EUNSUPPORTED, "head_dim %d not built (64 or 128)", c->head_dim);
+  if (c->page_size != kvq::kPage)
+    return fail(KVQ_EUNSUPPORTED, "page_size %d not built (16)", c->page_size);
+  if ((c->had_block != 32 && c->had_block != 64 && c->had_block != 128) ||
+      c->had_block > c->head_dim)
+    return fail(KVQ_EUNSUPPORTED, "Hadamard block %d not built for head_dim %d (32/64/128)",
+                c->had_block, c->head_dim);
+  if (c->window < 0 || c->window > kvq::kMaxWindow)
+    return fail(KVQ_EUNSUPPORTED, "window %d outside [0, %d]", c->window, kvq::kMaxWindow);
+  if (c->num_pages < 1) return fail(KVQ_EINVAL, "num_pages must be >= 1");
+  if (!c->bits_host) return fail(KVQ_EINVAL, "bits_host is NULL");
+  kvq::LayerGeom local;
+  kvq::LayerGeom* g = geom ? geom : &local;
+  std::memset(g, 0, sizeof *g);
+  long long off = 0;
+  int maxh = 0;
+  for (int h = 0; h < c->num_kv_heads; ++h) {
+    const int bk = c->bits_host[(layer * c->num_kv_heads + h) * 2 + 0];
+    const int bv = c->bits_host[(layer * c->num_kv_heads + h) * 2 + 1];
+    for (int b : {bk, bv})
+      if (b != 2 && b != 4 && b != 8)
+        return fail(KVQ_EUNSUPPORTED, "bits %d of layer %d head %d not built (2, 4, 8)", b,
+                    layer, h);
+    const int hb = kvq::kPage * (c->head_dim * (bk + bv) / 8 + 8);
+    g->head_off[h] = static_cast<int>(off);
+    g->bits[h][0] = static_cast<int8_t>(bk);
+    g->bits[h][1] = static_cast<int8_t>(bv);
+    off += hb;
+    if (hb > maxh) maxh = hb;
+  }
+  g->page_bytes = off;
+  g->max_head_bytes = maxh;
+  return KVQ_OK;
+}
+
+// check_geometry plus the device pointers of `layer`.
+kvq_status check_cache(const kvq_cache* c, int layer, kvq::LayerGeom* geom) {
+  const kvq_status st = check_geometry(c, layer, geom);
+  if (st != KVQ_OK) return st;
+  if (!c->layer_pools || !c->layer_pools[layer])
+    return fail(KVQ_EINVAL, "layer_pools[%d] is NULL", layer);
+  if (!aligned(c->layer_pools[layer], 16))
+    return fail(KVQ_EINVAL, "layer_pools[%d] is not 16-byte aligned", layer);
+  if (c->window > 0) {
+    if (c->max_batch < 1) return fail(KVQ_EINVAL, "max_batch must be >= 1 with a window");
+    if (!c->window_bufs || !c->window_bufs[layer])
+      return fail(KVQ_EINVAL, "window_bufs[%d] is NULL but window = %d", layer, c->window);
+    if (!aligned(c->window_bufs[layer], 16))
+      return fail(KVQ_EINVAL, "window_bufs[%d] is not 16-byte aligned", layer);
+  }
+  return KVQ_OK;
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+struct Plan {
+  int S, NS, pages_per_split;
+  size_t counter_bytes, bytes;
+};
+
+// Split count: enough CTAs to fill every SM about four deep in one wave, at
+// least 4 pages (one per warp) per split, at most kMaxSplits.
+kvq_status plan_decode(const kvq_cache* c, int B, int max_pages, Plan* pl) {
+  const int sms = sm_count();
+  if (sms <= 0) return fail(KVQ_ECUDA, "no CUDA device visible");
+  const long long units = static_cast<long long>(B) * c->num_kv_heads;
+  long long s = (4ll * sms + units - 1) / units;
+  const long long cap = (max_pages + 3) / 4;
+  if (s > cap) s = cap;
+  if (s > 256) s = 256;
+  if (s < 1) s = 1;
+  const int pps = static_cast<int>((max_pages + s - 1) / s);
+  pl->S = (max_pages + pps - 1) / pps;
+  pl->pages_per_split = pps;
+  pl->NS = pl->S + (c->window > 0 ? 1 : 0);
+  pl->counter_bytes = (static_cast<size_t>(units) * 4 + 255) / 256 * 256;
+  pl->bytes = pl->counter_bytes + static_cast<size_t>(units) * pl->NS * kvq::kMaxGroup *
+                                      (c->head_dim + 2) * sizeof(float);
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kvq_page_bytes(const kvq_cache* cache, int layer) {
+  kvq::LayerGeom g;
+  if (check_geometry(cache, layer, &g) != KVQ_OK) return 0;
+  return static_cast<size_t>(g.page_bytes);
+}
+
+kvq_status kvq_append(const kvq_cache* cache, int layer, const void* K, const void* V,
+                      const int32_t* page_table, int max_pages, const int32_t* seq_lens, int B,
+                      int T_new, void* stream) {
+  kvq::AppendParams p;
+  std::memset(&p, 0, sizeof p);
+  kvq_status st = check_cache(cache, layer, &p.geom);
+  if (st != KVQ_OK) return st;
+  if (B < 1) return fail(KVQ_EINVAL, "B must be >= 1");
+  if (T_new < 0) return fail(KVQ_EINVAL, "T_new must be >= 0");
+  if (T_new == 0) return KVQ_OK;
+  if (!K || !V || !page_table || !seq_lens)
+    return fail(KVQ_EINVAL, "K, V, page_table and seq_lens must be non-NULL");
+  if (!aligned(K, 16) || !aligned(V, 16))
+    return fail(KVQ_EINVAL, "K and V must be 16-byte aligned");
+  if (!aligned(page_table, 4) || !aligned(seq_lens, 4))
+    return fail(KVQ_EINVAL, "page_table and seq_lens must be 4-byte aligned");
+  if (max_pages < 1) return fail(KVQ_EINVAL, "max_pages must be >= 1");
+  if (static_cast<long long>(B) * T_new > (1ll << 28))
+    return fail(KVQ_EINVAL, "B * T_new too large");
+  if (cache->window > 0 && B > cache->max_batch)
+    return fail(KVQ_EINVAL, "B %d exceeds the window buffers' max_batch %d", B, cache->max_batch);
+  p.K = static_cast<const uint16_t*>(K);
+  p.V = static_cast<const uint16_t*>(V);
+  p.pool = static_cast<uint8_t*>(cache->layer_pools[layer]);
+  p.window = cache->window > 0 ? static_cast<uint16_t*>(cache->window_bufs[layer]) : nullptr;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.status = cache->status_dev;
+  p.max_pages = max_pages;
+  p.B = B;
+  p.T = T_new;
+  p.Hkv = cache->num_kv_heads;
+  p.R = cache->window;
+  p.num_pages = cache->num_pages;
+  p.warps_per_group = static_cast<int>((static_cast<long long>(B) * T_new + 15) / 16);
+  const cudaError_t e = kvq::launch_append(p, cache->head_dim, cache->had_block,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "append launch: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
+
+size_t kvq_decode_workspace_bytes(const kvq_cache* cache, int B, int Hq, int max_pages) {
+  if (check_geometry(cache, 0, nullptr) != KVQ_OK) return 0;
+  if (B < 1 || max_pages < 1 || Hq < 1) {
+    fail(KVQ_EINVAL, "B, Hq and max_pages must be >= 1");
+    return 0;
+  }
+  Plan pl;
+  if (plan_decode(cache, B, max_pages, &pl) != KVQ_OK) return 0;
+  return pl.bytes;
+}
+
+kvq_status kvq_decode_attn(const kvq_cache* cache, int layer, const void* q, int q_is_fp32,
+                           const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                           int B, int Hq, float softmax_scale, float* o, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  kvq::DecodeParams p;
+  std::memset(&p, 0, sizeof p);
+  kvq_status st = check_cache(cache, layer, &p.geom);
+  if (st != KVQ_OK) return st;
+  if (B < 1 || max_pages < 1) return fail(KVQ_EINVAL, "B and max_pages must be >= 1");
+  if (B > 65535) return fail(KVQ_EUNSUPPORTED, "B %d above the grid limit 65535", B);
+  if (!q || !o || !page_table || !seq_lens || !workspace)
+    return fail(KVQ_EINVAL, "q, o, page_table, seq_lens and workspace must be non-NULL");
+  if (!aligned(q, 4) || !aligned(o, 4) || !aligned(page_table, 4) || !aligned(seq_lens, 4))
+    return fail(KVQ_EINVAL, "q, o, page_table and seq_lens must be 4-byte aligned");
+  if (!aligned(workspace, 16)) return fail(KVQ_EINVAL, "workspace must be 16-byte aligned");
+  const int hkv = cache->num_kv_heads;
+  if (Hq < hkv || Hq % hkv) return fail(KVQ_EINVAL, "Hq %d is not a multiple of Hkv %d", Hq, hkv);
+  const int G = Hq / hkv;
+  if (G != 1 && G != 2 && G != 4)
+    return fail(KVQ_EUNSUPPORTED, "GQA group %d not built (1, 2, 4)", G);
+  if (cache->window > 0 && B > cache->max_batch)
+    return fail(KVQ_EINVAL, "B %d exceeds the window buffers' max_batch %d", B, cache->max_batch);
+  if (!std::isfinite(softmax_scale) || softmax_scale < 0.f)
+    return fail(KVQ_EINVAL, "softmax_scale must be finite and >= 0");
+  Plan pl;
+  st = plan_decode(cache, B, max_pages, &pl);
+  if (st != KVQ_OK) return st;
+  if (ws_bytes < pl.bytes)
+    return fail(KVQ_EWORKSPACE, "workspace of %zu bytes < %zu required", ws_bytes, pl.bytes);
+  const float scale =
+      softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cache->head_dim));
+  p.pool = static_cast<const uint8_t*>(cache->layer_pools[layer]);
+  p.window = cache->window > 0 ? static_cast<const uint16_t*>(cache->window_bufs[layer]) : nullptr;
+  p.q = q;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.o = o;
+  p.counters = static_cast<unsigned int*>(workspace);
+  p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.counter_bytes);
+  p.status = cache->status_dev;
+  p.q_fp32 = q_is_fp32 ? 1 : 0;
+  p.max_pages = max_pages;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = hkv;
+  p.G = G;
+  p.R = cache->window;
+  p.num_pages = cache->num_pages;
+  p.had_block = cache->had_block;
+  p.S = pl.S;
+  p.NS = pl.NS;
+  p.pages_per_split = pl.pages_per_split;
+  p.stage_bytes = (p.geom.max_head_bytes + 127) / 128 * 128;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const cudaError_t e = kvq::launch_decode(p, cache->head_dim, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "decode launch: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
+
+kvq_status kvq_alloc_bits(const double* w, const double* beta, int n, long long budget,
+                          const uint16_t* allowed_mask, int* bits_out, long long* leftover) {
+  if (n < 1 || !w || !beta || !bits_out)
+    return fail(KVQ_EINVAL, "n >= 1 and non-NULL w, beta, bits_out required");
+  for (int i = 0; i < n; ++i) {
+    if (!(std::isfinite(w[i]) && w[i] > 0.0))
+      return fail(KVQ_EINVAL, "w[%d] must be finite and > 0", i);
+    if (!(std::isfinite(beta[i]) && beta[i] > 1.0))
+      return fail(KVQ_EINVAL, "beta[%d] must be finite and > 1", i);
+    const unsigned m = allowed_mask ? allowed_mask[i] : 0x114u;  // {2, 4, 8}
+    if ((m & 0xfffeu) == 0) return fail(KVQ_EINVAL, "allowed_mask[%d] has no width in 1..15", i);
+  }
+  auto mask_of = [&](int i) -> unsigned {
+    return (allowed_mask ? allowed_mask[i] : 0x114u) & 0xfffeu;
+  };
+  auto next_allowed = [&](int i, int b) -> int {
+    const unsigned m = mask_of(i);
+    for (int x = b + 1; x <= 15; ++x)
+      if (m & (1u << x)) return x;
+    return -1;
+  };
+  // smallest allowed width of every component
+  long long used = 0;
+  int* bits = bits_out;
+  // work on a local copy so that bits_out stays untouched on KVQ_EBUDGET
+  std::string scratch(static_cast<size_t>(n) * sizeof(int), '\0');
+  int* cur = reinterpret_cast<int*>(&scratch[0]);
+  for (int i = 0; i < n; ++i) {
+    const unsigned m = mask_of(i);
+    int b = 1;
+    while (!(m & (1u << b))) ++b;
+    cur[i] = b;
+    used += b;
+  }
+  if (used > budget)
+    return fail(KVQ_EBUDGET, "budget %lld below the minimum allocation %lld", budget, used);
+  for (;;) {
+    int best = -1;
+    double best_gain = 0.0;
+    for (int i = 0; i < n; ++i) {
+      const int nxt = next_allowed(i, cur[i]);
+      if (nxt < 0) continue;
+      const int cost = nxt - cur[i];
+      if (cost > budget - used) continue;
+      const double gain = w[i] * (std::pow(beta[i], static_cast<double>(-cur[i])) -
+                                  std::pow(beta[i], static_cast<double>(-nxt))) /
+                          static_cast<double>(cost);
+      if (best < 0 || gain > best_gain) {
+        best = i;
+        best_gain = gain;
+      }
+    }
+    if (best < 0) break;
+    const int nxt = next_allowed(best, cur[best]);
+    used += nxt - cur[best];
+    cur[best] = nxt;
+  }
+  std::memcpy(bits, cur, static_cast<size_t>(n) * sizeof(int));
+  if (leftover) *leftover = budget - used;
+  return KVQ_OK;
+}
+
+kvq_status kvq_get_status(const kvq_cache* cache, int* device_status) {
+  if (!cache || !cache->status_dev || !device_status)
+    return fail(KVQ_EINVAL, "cache, cache->status_dev and device_status must be non-NULL");
+  int v = 0;
+  const cudaError_t e = cudaMemcpy(&v, cache->status_dev, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "status copy: %s", cudaGetErrorString(e));
+  *device_status = v;
+  return v ? KVQ_EDEVICE : KVQ_OK;
+}
+
+kvq_status kvq_reset_status(const kvq_cache* cache, void* stream) {
+  if (!cache || !cache->status_dev)
+    return fail(KVQ_EINVAL, "cache and cache->status_dev must be non-NULL");
+  const cudaError_t e =
+      cudaMemsetAsync(cache->status_dev, 0, sizeof(int), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "status reset: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
+
+const char* kvq_last_error(void) { return g_last_error.c_str(); }
+
+const char* kvq_version(void) { return "kvq 0.1 sm_103a"; }
+
+}  // extern "C"

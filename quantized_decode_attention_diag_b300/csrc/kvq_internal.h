@@ -1,0 +1,65 @@
+// Internal interface between the C ABI (kvq_api.cpp) and the kernels.
+// Plain structs passed by value as kernel parameters (well under 4 KB).
+#pragma once
+
+#include <cuda_runtime_api.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kvq {
+
+constexpr int kPage = 16;        // tokens per page (= MMA M dimension)
+constexpr int kMaxHeads = 64;    // KV heads per layer
+constexpr int kMaxWindow = 1024; // bf16 recent-token window
+constexpr int kMaxGroup = 4;     // query heads per KV head handled per CTA
+
+// Per-layer page geometry, computed on the host from the bits table.
+struct LayerGeom {
+  int head_off[kMaxHeads];       // byte offset of head h's segment in a page
+  int8_t bits[kMaxHeads][2];     // (bK, bV)
+  long long page_bytes;
+  int max_head_bytes;            // largest head segment (one async copy)
+};
+
+struct AppendParams {
+  const uint16_t* K;             // bf16 [B][T][Hkv][D]
+  const uint16_t* V;
+  uint8_t* pool;                 // [num_pages][page_bytes]
+  uint16_t* window;              // bf16 [max_batch][Hkv][2][R][D] or null
+  const int32_t* page_table;     // [B][max_pages]
+  const int32_t* seq_lens;       // [B], before the append
+  int* status;
+  int max_pages, B, T, Hkv, R, num_pages;
+  int warps_per_group;           // ceil(B * T / 16)
+  LayerGeom geom;
+};
+
+struct DecodeParams {
+  const uint8_t* pool;
+  const uint16_t* window;        // bf16 ring or null
+  const void* q;                 // [B][Hq][D] bf16 or fp32
+  const int32_t* page_table;
+  const int32_t* seq_lens;       // [B], including the window
+  float* o;                      // fp32 [B][Hq][D]
+  float* partials;               // fp32 [B][Hkv][NS][kMaxGroup][D + 2]
+  unsigned int* counters;        // [B][Hkv]
+  int* status;
+  int q_fp32, max_pages, B, Hq, Hkv, G, R, num_pages, had_block;
+  int S;                         // quantized-token splits
+  int NS;                        // S + (R > 0): the window gets its own split
+  int pages_per_split;
+  int stage_bytes;               // bytes of one pipeline stage buffer
+  float scale_log2;              // softmax_scale * log2(e)
+  LayerGeom geom;
+};
+
+constexpr int kDecodeWarps = 4;
+constexpr int kDecodeStages = 4;
+constexpr int kAppendWarps = 8;
+
+// Launchers (defined in the .cu files).  Return cudaSuccess or the launch error.
+cudaError_t launch_append(const AppendParams& p, int head_dim, int had_block, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, int head_dim, cudaStream_t s);
+size_t decode_smem_bytes(const DecodeParams& p, int head_dim);
+
+}  // namespace kvq

@@ -1,0 +1,138 @@
+"""C-ABI library on the host: it loads, exports every declared symbol, its
+host-only logic (allocator, page geometry, argument checks) matches the oracle.
+No call here reaches a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import quantized_decode_attention_diag_b300 as kvq
+from oracle import allocator, layout
+from tests.conftest import ROOT
+from workloads import sensitivities
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built_library():
+    from quantized_decode_attention_diag_b300 import build
+    build.build()
+    return kvq.lib()
+
+
+def test_exports_every_declared_symbol():
+    header = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    names = sorted(set(re.findall(r"^\s*(?:[\w\*]+\s+)+\**(kvq_\w+)\s*\(", header, re.M)))
+    assert {"kvq_append", "kvq_decode_attn", "kvq_alloc_bits", "kvq_page_bytes",
+            "kvq_decode_workspace_bytes", "kvq_get_status", "kvq_reset_status",
+            "kvq_last_error", "kvq_version"} <= set(names)
+    handle = ctypes.CDLL(kvq.LIB_PATH)
+    for n in names:
+        assert hasattr(handle, n), n
+    assert kvq.kvq_version().startswith("kvq")
+
+
+def _desc(hkv=8, d=128, block=128, bits=(4, 4), layers=1, window=0, pages=64):
+    b = np.zeros((layers, hkv, 2), np.int8)
+    b[..., 0], b[..., 1] = bits
+    desc = kvq.kvq_cache()
+    desc.num_layers, desc.num_kv_heads, desc.head_dim, desc.page_size = layers, hkv, d, 16
+    desc.had_block, desc.window, desc.max_batch, desc.num_pages = block, window, 4, pages
+    desc.bits_host = b.ctypes.data_as(ctypes.POINTER(ctypes.c_int8))
+    desc._keep = b
+    return desc
+
+
+@pytest.mark.parametrize("hkv,d,bits", [(8, 128, (4, 4)), (8, 128, (4, 2)), (4, 64, (4, 2)),
+                                         (2, 64, (8, 2)), (3, 128, (2, 8))])
+def test_page_bytes_matches_layout(hkv, d, bits):
+    desc = _desc(hkv=hkv, d=d, block=min(d, 64), bits=bits)
+    assert kvq.kvq_page_bytes(desc, 0) == layout.page_bytes(d, np.array([bits] * hkv))
+
+
+def test_page_bytes_mixed_heads():
+    b = np.array([[[4, 2], [8, 4], [4, 4], [2, 2]]], np.int8)
+    desc = _desc(hkv=4)
+    desc.bits_host = b.ctypes.data_as(ctypes.POINTER(ctypes.c_int8))
+    desc._keep = b
+    assert kvq.kvq_page_bytes(desc, 0) == layout.page_bytes(128, b[0])
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_alloc_bits_matches_oracle(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 40))
+    w = rng.lognormal(0, 1.2, n)
+    beta = rng.uniform(3.0, 6.0, n)
+    sets = [[2, 4, 8], [4, 8], [2, 4], list(range(1, 9)), [3, 5, 6]]
+    allowed = [sets[int(rng.integers(0, len(sets)))] for _ in range(n)]
+    lo = sum(min(a) for a in allowed)
+    hi = sum(max(a) for a in allowed)
+    budget = int(rng.integers(lo, hi + 3))
+    want, left = allocator.greedy(w, beta, budget, allowed)
+    got, gleft = kvq.kvq_alloc_bits(w, beta, budget, [kvq.mask_of(a) for a in allowed])
+    assert got == want and gleft == left
+
+
+def test_alloc_bits_mixed_layer_config():
+    w = sensitivities(1003, 32, 8).reshape(-1)
+    allowed = [[4, 8], [2, 4]] * 256
+    masks = [kvq.mask_of(a) for a in allowed]
+    for budget in (3 * 512, int(3.5 * 512)):
+        want, left = allocator.greedy(w, [4.0] * 512, budget, allowed)
+        got, gleft = kvq.kvq_alloc_bits(w, [4.0] * 512, budget, masks)
+        assert got == want and gleft == left
+
+
+def test_alloc_bits_errors():
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kvq_alloc_bits([1.0, 1.0], [4.0, 4.0], 5, [kvq.mask_of([4, 8]), kvq.mask_of([2, 4])])
+    assert e.value.status == kvq.KVQ_EBUDGET
+    for w, beta in (([0.0], [4.0]), ([1.0], [1.0]), ([float("nan")], [4.0])):
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.kvq_alloc_bits(w, beta, 8)
+        assert e.value.status == kvq.KVQ_EINVAL
+    bits, left = kvq.kvq_alloc_bits([1.0, 2.0], [4.0, 4.0], 10)   # default {2, 4, 8}
+    # (2,2) -> V-like step of the heavier component 2->4, then the other 2->4;
+    # no 4->8 step fits the last 2 bits
+    assert (bits, left) == ([4, 4], 2)
+    assert (bits, left) == tuple(allocator.greedy([1.0, 2.0], [4.0, 4.0], 10, [[2, 4, 8]] * 2))
+
+
+def _checked(fn, *args):
+    with pytest.raises(kvq.KvqError) as e:
+        fn(*args)
+    return e.value.status
+
+
+def test_host_argument_checks_run_before_any_device_call():
+    fake = 1 << 20                            # never dereferenced: checks fail first
+    desc = _desc()
+    pools = (ctypes.c_void_p * 1)(fake)
+    desc.layer_pools = pools
+    ap = lambda d, K=fake, layer=0, B=2, T=3: kvq.kvq_append(d, layer, K, fake, fake, 4, fake,
+                                                              B, T, 0)
+    assert _checked(ap, desc, 0) == kvq.KVQ_EINVAL              # NULL K
+    assert _checked(ap, desc, fake + 8) == kvq.KVQ_EINVAL       # misaligned K
+    assert _checked(ap, desc, fake, 1) == kvq.KVQ_EINVAL        # layer out of range
+    assert _checked(ap, desc, fake, 0, 0) == kvq.KVQ_EINVAL     # B = 0
+    bad = _desc(d=96)
+    bad.layer_pools = pools
+    assert _checked(ap, bad) == kvq.KVQ_EUNSUPPORTED
+    bad = _desc(bits=(3, 4))
+    bad.layer_pools = pools
+    assert _checked(ap, bad) == kvq.KVQ_EUNSUPPORTED
+    bad = _desc(block=16)
+    bad.layer_pools = pools
+    assert _checked(ap, bad) == kvq.KVQ_EUNSUPPORTED
+    nopool = _desc()
+    assert _checked(ap, nopool) == kvq.KVQ_EINVAL
+    win = _desc(window=16)
+    win.layer_pools = pools
+    assert _checked(ap, win) == kvq.KVQ_EINVAL                  # window buffer missing
+    dec = lambda d, Hq: kvq.kvq_decode_attn(d, 0, fake, 0, fake, 4, fake, 2, Hq, 0.0, fake, fake,
+                                             1 << 20, 0)
+    assert _checked(dec, desc, 12) == kvq.KVQ_EINVAL            # Hq not a multiple of Hkv
+    assert _checked(dec, desc, 64) == kvq.KVQ_EUNSUPPORTED      # GQA group of 8
+    assert kvq.kvq_append(desc, 0, fake, fake, fake, 4, fake, 2, 0, 0) is None   # T_new = 0: no-op
