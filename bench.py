@@ -73,13 +73,14 @@ def peaks() -> dict:
 # ------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.window = None   # (start, end) of the timed region, local wall clock
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
 
     def __enter__(self):
@@ -90,12 +91,14 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(1.5)          # nvidia-smi needs a moment before its first sample
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.3)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -103,88 +106,108 @@ class ClockSampler:
                 self.proc.kill()
             self.fh.close()
 
+    def mark(self, start, end) -> None:
+        self.window = (start, end)
+
     def summary(self) -> dict:
+        import datetime as _dt
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                ts = _dt.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, cmax = float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            if self.window and not (self.window[0] - 0.25 <= ts <= self.window[1] + 0.25):
+                continue
+            sm.append(clk)
+            smax.append(cmax)
+            for n, v in zip(names, f[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------------------- oracle legs
 
-def oracle_sample(n_seqs: int, repeats: int):
-    """Time the CPU oracle on a bounded sample of the workload.
+class OracleSample:
+    """The CPU oracle on a bounded sample of the workload.
 
     The sample is n_seqs of the 16 sequences of one layer: the oracle fills its
-    own cache for them (untimed), then each timed repeat is one decode step for
+    own cache for them at construction (untimed); step() is one decode step for
     them -- append of the new token and attention over 4096 tokens for all 8
-    KV heads / 32 query heads.  Returns (GB/s over the same algorithmic bytes,
-    seconds per repeat, BLAS threads, description)."""
-    from oracle import attention, cache as ocache
-    try:
-        from threadpoolctl import threadpool_info
-        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
-    except Exception:  # noqa: BLE001
-        threads = 1
-    d, hkv = W.head_dim, W.hkv
-    ctx = W.ctx
-    k = kv_tokens(W.seed, 0, n_seqs, ctx, hkv, d, W.k_outliers, W.outlier_lo, W.outlier_hi)
-    v = kv_tokens(W.seed, 1, n_seqs, ctx, hkv, d, W.v_outliers, W.outlier_lo, W.outlier_hi)
-    mp = ctx // 16
-    pt = page_table(W.seed, n_seqs, mp)
-    st = ocache.new_state(1, n_seqs * mp, d, W.had_block, np.full((1, hkv, 2), 4))
-    ocache.append(st, 0, k[:, :ctx - 1], v[:, :ctx - 1], pt, np.zeros(n_seqs, np.int32))
-    q = queries(W.seed, 0, n_seqs, W.hq, d, False).astype(np.float64)
-    before = np.full(n_seqs, ctx - 1, np.int32)
-    after = before + 1
-    times = []
-    for _ in range(repeats):
+    KV heads / 32 query heads."""
+
+    def __init__(self, n_seqs: int):
+        from oracle import cache as ocache
+        try:
+            from threadpoolctl import threadpool_info
+            self.threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+        except Exception:  # noqa: BLE001
+            self.threads = 1
+        d, hkv, ctx = W.head_dim, W.hkv, W.ctx
+        self.n = n_seqs
+        self.k = kv_tokens(W.seed, 0, n_seqs, ctx, hkv, d, W.k_outliers, W.outlier_lo,
+                           W.outlier_hi)
+        self.v = kv_tokens(W.seed, 1, n_seqs, ctx, hkv, d, W.v_outliers, W.outlier_lo,
+                           W.outlier_hi)
+        mp = ctx // 16
+        self.pt = page_table(W.seed, n_seqs, mp)
+        self.st = ocache.new_state(1, n_seqs * mp, d, W.had_block, np.full((1, hkv, 2), 4))
+        ocache.append(self.st, 0, self.k[:, :ctx - 1], self.v[:, :ctx - 1], self.pt,
+                      np.zeros(n_seqs, np.int32))
+        self.q = queries(W.seed, 0, n_seqs, W.hq, d, False).astype(np.float64)
+        self.before = np.full(n_seqs, ctx - 1, np.int32)
+        self.nbytes = n_seqs * ctx * hkv * unit_bytes(d, 4, 4)
+
+    def step(self) -> float:
+        from oracle import attention, cache as ocache
+        ctx = W.ctx
         t0 = time.perf_counter()
-        ocache.append(st, 0, k[:, ctx - 1:], v[:, ctx - 1:], pt, before)
-        attention.decode(st, 0, q, pt, after)
-        times.append(time.perf_counter() - t0)
-    sec = statistics.median(times)
-    nbytes = n_seqs * ctx * hkv * unit_bytes(d, 4, 4)
-    desc = (f"{n_seqs} of {W.batch} sequences x 8 KV heads x {ctx} tokens of one layer "
-            f"(one decode step: append 1 token + attention), median of {repeats}")
-    return nbytes / sec / 1e9, sec, threads, desc
+        ocache.append(self.st, 0, self.k[:, ctx - 1:], self.v[:, ctx - 1:], self.pt, self.before)
+        attention.decode(self.st, 0, self.q, self.pt, self.before + 1)
+        return time.perf_counter() - t0
+
+    def describe(self, repeats: int) -> str:
+        return (f"{self.n} of {W.batch} sequences x {W.hkv} KV heads x {W.ctx} tokens of one "
+                f"layer (one decode step: append 1 token + attention), median of {repeats}")
+
+
+def oracle_baseline(n_seqs: int = 4, repeats: int = 5) -> dict:
+    o = OracleSample(n_seqs)
+    o.step()
+    sec = statistics.median([o.step() for _ in range(repeats)])
+    return {"value": round(o.nbytes / sec / 1e9, 4), "unit": "GB/s", "cores": o.threads,
+            "kind": "oracle", "sample": o.describe(repeats)}
 
 
 def run_reference(args) -> None:
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    sec_total = 0.0
-    n_seqs = 2
+    o = OracleSample(2)
     for _ in range(args.warmup):
-        oracle_sample(n_seqs, 1)
-    gbs, sec, threads, desc = oracle_sample(n_seqs, max(1, args.steps))
-    sec_total = sec
+        o.step()
+    times = [o.step() for _ in range(max(1, min(args.steps, 50)))]
+    sec = sum(times) / len(times)
+    gbs = o.nbytes / sec / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(sec_total * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(),
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": o.threads,
+                         "kind": "oracle", "sample": o.describe(len(times))},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -196,7 +219,8 @@ def config_dict() -> dict:
             "batch": W.batch, "q_heads": W.hq, "kv_heads": W.hkv, "head_dim": W.head_dim,
             "context": W.ctx, "bits": "K4V4", "had_block": W.had_block, "page": 16,
             "layers": N_LAYERS, "step": "per layer: append 1 token/seq + split-K decode",
-            "l2": "inputs larger than L2: 32 distinct layer caches, 2.28 GB of packed KV per step",
+            "l2": (f"inputs larger than L2: {N_LAYERS} distinct layer caches, "
+                   f"{N_LAYERS * decode_bytes_per_layer() / 1e9:.2f} GB of packed KV per step"),
             "parallelism": "replicas (weak scaling), no collective on the data path"}
 
 
@@ -224,9 +248,7 @@ def run_kvq(args) -> None:
     # CPU baseline first (rank 0 only), before the first kernel runs
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        gbs, sec, threads, desc = oracle_sample(2, 3)
-        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": desc}
+        cpu = oracle_baseline(4, 5)
 
     d, hkv, hq, bsz, ctx = W.head_dim, W.hkv, W.hq, W.batch, W.ctx
     # bit-widths from the allocator (uniform sensitivities, only width 4 allowed)
@@ -302,7 +324,9 @@ def run_kvq(args) -> None:
             graph.replay()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
+        t_start = time.time()
         ms = timed(graph.replay, args.steps)
+        clocks.mark(t_start, time.time())
     dec_ms = [ev[l][0].elapsed_time(ev[l][1]) for l in range(N_LAYERS)]   # last replay
     assert cache.get_status() == 0, f"device status {cache.get_status():#x}"
 
@@ -408,12 +432,16 @@ def append_sweep(kvq, torch, dev) -> dict:
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-append", action="store_true")
+    ap.add_argument("--layers", type=int, default=32,
+                    help="distinct layer caches per step (profiling uses a small case)")
     args = ap.parse_args()
+    global N_LAYERS
+    N_LAYERS = args.layers
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
