@@ -105,24 +105,50 @@ int sm_count() {
 }
 
 struct Plan {
-  int S, NS, pages_per_split;
+  int S, NS, pages_per_split, stage_bytes;
   size_t counter_bytes, bytes;
 };
 
-// Split count: enough CTAs to fill every SM about four deep in one wave, at
-// least 4 pages (one per warp) per split, at most kMaxSplits.
-kvq_status plan_decode(const kvq_cache* c, int B, int max_pages, Plan* pl) {
+// Split count for one layer: as many splits per (sequence, KV head) as keep the
+// whole grid resident in one wave (CTAs per SM from the occupancy calculator
+// for this layer's shared-memory size), at least 8 pages (two per warp) per
+// split, at most the kernel's split limit.
+kvq_status plan_decode(const kvq_cache* c, const kvq::LayerGeom& g, int B, int max_pages,
+                       Plan* pl) {
   const int sms = sm_count();
   if (sms <= 0) return fail(KVQ_ECUDA, "no CUDA device visible");
+  kvq::DecodeParams probe;
+  std::memset(&probe, 0, sizeof probe);
+  probe.stage_bytes = (g.max_head_bytes + 127) / 128 * 128;
+  probe.R = c->window;
+  const size_t smem = kvq::decode_smem_bytes(probe, c->head_dim);
+  static thread_local int cache_key[4] = {0, 0, 0, 0}, cache_val[4] = {0, 0, 0, 0};
+  const int key = static_cast<int>(smem) * 2 + (c->head_dim == 128);
+  int bps = 0;
+  for (int i = 0; i < 4; ++i)
+    if (cache_key[i] == key) bps = cache_val[i];
+  if (!bps) {
+    bps = kvq::decode_blocks_per_sm(c->head_dim, smem);
+    if (bps <= 0)
+      return fail(KVQ_ECUDA, "decode kernel cannot be resident with %zu bytes of shared memory",
+                  smem);
+    for (int i = 3; i > 0; --i) {
+      cache_key[i] = cache_key[i - 1];
+      cache_val[i] = cache_val[i - 1];
+    }
+    cache_key[0] = key;
+    cache_val[0] = bps;
+  }
   const long long units = static_cast<long long>(B) * c->num_kv_heads;
-  long long s = (4ll * sms + units - 1) / units;
-  const long long cap = (max_pages + 3) / 4;
+  long long s = static_cast<long long>(sms) * bps / units;
+  const long long cap = (max_pages + 7) / 8;
   if (s > cap) s = cap;
-  if (s > 256) s = 256;
+  if (s > kvq::decode_max_splits()) s = kvq::decode_max_splits();
   if (s < 1) s = 1;
   const int pps = static_cast<int>((max_pages + s - 1) / s);
   pl->S = (max_pages + pps - 1) / pps;
   pl->pages_per_split = pps;
+  pl->stage_bytes = probe.stage_bytes;
   pl->NS = pl->S + (c->window > 0 ? 1 : 0);
   pl->counter_bytes = (static_cast<size_t>(units) * 4 + 255) / 256 * 256;
   pl->bytes = pl->counter_bytes + static_cast<size_t>(units) * pl->NS * kvq::kMaxGroup *
@@ -187,9 +213,15 @@ size_t kvq_decode_workspace_bytes(const kvq_cache* cache, int B, int Hq, int max
     fail(KVQ_EINVAL, "B, Hq and max_pages must be >= 1");
     return 0;
   }
-  Plan pl;
-  if (plan_decode(cache, B, max_pages, &pl) != KVQ_OK) return 0;
-  return pl.bytes;
+  size_t most = 0;   // enough for every layer
+  for (int layer = 0; layer < cache->num_layers; ++layer) {
+    kvq::LayerGeom g;
+    Plan pl;
+    if (check_geometry(cache, layer, &g) != KVQ_OK) return 0;
+    if (plan_decode(cache, g, B, max_pages, &pl) != KVQ_OK) return 0;
+    if (pl.bytes > most) most = pl.bytes;
+  }
+  return most;
 }
 
 kvq_status kvq_decode_attn(const kvq_cache* cache, int layer, const void* q, int q_is_fp32,
@@ -217,7 +249,7 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, int layer, const void* q, int
   if (!std::isfinite(softmax_scale) || softmax_scale < 0.f)
     return fail(KVQ_EINVAL, "softmax_scale must be finite and >= 0");
   Plan pl;
-  st = plan_decode(cache, B, max_pages, &pl);
+  st = plan_decode(cache, p.geom, B, max_pages, &pl);
   if (st != KVQ_OK) return st;
   if (ws_bytes < pl.bytes)
     return fail(KVQ_EWORKSPACE, "workspace of %zu bytes < %zu required", ws_bytes, pl.bytes);
@@ -244,7 +276,7 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, int layer, const void* q, int
   p.S = pl.S;
   p.NS = pl.NS;
   p.pages_per_split = pl.pages_per_split;
-  p.stage_bytes = (p.geom.max_head_bytes + 127) / 128 * 128;
+  p.stage_bytes = pl.stage_bytes;
   p.scale_log2 = scale * 1.4426950408889634f;
   const cudaError_t e = kvq::launch_decode(p, cache->head_dim, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "decode launch: %s", cudaGetErrorString(e));

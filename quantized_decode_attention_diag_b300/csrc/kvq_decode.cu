@@ -189,6 +189,44 @@ __device__ __forceinline__ float warp_sum_group(float x) {
 
 __device__ __forceinline__ float hi_part(float x) { return __half2float(__float2half_rn(x)); }
 
+// ------------------------------------------------------- query prologue --
+// qtab <- the group's queries scaled by softmax_scale * log2(e) (and, for the
+// quantized splits, rotated: q'' = H q / n); qsum[i] = sum_d qtab[i][d].
+template <int D>
+__device__ void query_prologue(const DecodeParams& p, const Smem& sm, bool rotate) {
+  const int tid = threadIdx.x;
+  if (rotate) {
+    const int nb = p.had_block;
+    for (int hs = 1; hs < nb; hs <<= 1) {
+      for (int idx = tid; idx < kMaxGroup * (D / 2); idx += kThreads) {
+        const int i = idx / (D / 2), r = idx - i * (D / 2);
+        const int lo = (r / hs) * 2 * hs + (r % hs);
+        const float a = sm.qtab[i * D + lo], c = sm.qtab[i * D + lo + hs];
+        sm.qtab[i * D + lo] = a + c;
+        sm.qtab[i * D + lo + hs] = a - c;
+      }
+      __syncthreads();
+    }
+  }
+  const float qscale = rotate ? p.scale_log2 / static_cast<float>(p.had_block) : p.scale_log2;
+  for (int idx = tid; idx < kMaxGroup * D; idx += kThreads) sm.qtab[idx] *= qscale;
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31;
+  float s = 0.f;
+  for (int d = lane; d < D; d += 32) s += sm.qtab[warp * D + d];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFullMask, s, o);
+  if (lane == 0) sm.qsum[warp] = s;
+  __syncthreads();
+}
+
+// 2^x with the hardware approximation (relative error ~2^-22); 2^-inf = 0
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------ quantized split
 template <int D, int BK, int BV>
 __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h, int split,
@@ -205,11 +243,53 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   // more than are used, from the zero upper half of a 2-byte slice)
   constexpr int VPAIRS = (BV == 2 ? 16 : BV == 4 ? 8 : 4) * VWORDS;
   static_assert(VPAIRS >= 2 * NJ, "value slice too small");
+  constexpr int NST = kDecodeStages;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
 
-  // B fragments of the rotated, scaled query (hi / lo split), column n = g
+  // ---- this warp's pages: first + 4 k, k < nk; their ids in registers,
+  //      32 per chunk (lane i holds page k = 32 * chunk + i)
+  const int npages = (lq + kPage - 1) / kPage;
+  const int pg0 = split * p.pages_per_split;
+  const int pg1 = min(npages, pg0 + p.pages_per_split);
+  const int first = pg0 + warp;
+  const int nk = pg1 > first ? (pg1 - first + kDecodeWarps - 1) / kDecodeWarps : 0;
+  const int32_t* ptab = p.page_table + static_cast<size_t>(b) * p.max_pages + first;
+  auto load_chunk = [&](int ch) -> int {
+    const int kk = 32 * ch + lane;
+    return kk < nk ? __ldg(ptab + kDecodeWarps * kk) : -1;
+  };
+  int chunk = 0;
+  int pid_cur = load_chunk(0);
+  int pid_nxt = nk > 32 ? load_chunk(1) : -1;
+  auto pid_of = [&](int kk) -> int {  // warp-uniform kk in [32 chunk, 32 chunk + 64)
+    const int v = (kk >> 5) == chunk ? pid_cur : pid_nxt;
+    return __shfl_sync(kFullMask, v, kk & 31);
+  };
+  uint8_t* stages = sm.area + static_cast<size_t>(warp) * NST * p.stage_bytes;
+  uint64_t* bars = sm.bars + warp * NST;
+  const uint8_t* head_base = p.pool + p.geom.head_off[h];
+  auto issue = [&](int kk, int pid) {  // lane 0 only
+    uint64_t* bar = bars + (kk % NST);
+    if (pid < 0 || pid >= p.num_pages) {
+      flag_status(p.status, 0x1);
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+      return;
+    }
+    mbar_expect_tx(bar, CHUNK);
+    bulk_g2s(stages + (kk % NST) * p.stage_bytes,
+             head_base + static_cast<size_t>(pid) * p.geom.page_bytes, CHUNK, bar);
+  };
+  // start streaming before the query prologue
+  for (int kk = 0; kk < nk && kk < NST; ++kk) {
+    const int pid = pid_of(kk);
+    if (lane == 0) issue(kk, pid);
+  }
+
+  query_prologue<D>(p, sm, true);
+
+  // ---- B fragments of the rotated, scaled query (hi / lo split), column n = g
   uint32_t bq[NJ][2];
   {
     const float* qh = sm.qtab + (g >> 1) * D;
@@ -222,7 +302,8 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
         kpair_dims<D, BK>(c, 2 * j + s2, d0, d1);
         float x0 = qh[d0], x1 = qh[d1];
         if (lo_part) { x0 -= hi_part(x0); x1 -= hi_part(x1); }
-        bq[j][s2] = pack_half2(__float2half_rn(x0), __float2half_rn(x1));
+        const __half2 hv = __floats2half2_rn(x0, x1);
+        bq[j][s2] = *reinterpret_cast<const uint32_t*>(&hv);
       }
     }
   }
@@ -233,138 +314,138 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
 #pragma unroll
   for (int j = 0; j < NJ; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
 
-  const int npages = (lq + kPage - 1) / kPage;
-  const int pg0 = split * p.pages_per_split;
-  const int pg1 = min(npages, pg0 + p.pages_per_split);
-  const int first = pg0 + warp;
-  const int nk = pg1 > first ? (pg1 - first + kDecodeWarps - 1) / kDecodeWarps : 0;
-  uint8_t* stages = sm.area + static_cast<size_t>(warp) * kDecodeStages * p.stage_bytes;
-  uint64_t* bars = sm.bars + warp * kDecodeStages;
-  const int32_t* ptab = p.page_table + static_cast<size_t>(b) * p.max_pages;
-  const uint8_t* head_base = p.pool + p.geom.head_off[h];
-
-  auto issue = [&](int k) {  // lane 0
-    const int pid = __ldg(ptab + first + kDecodeWarps * k);
-    uint64_t* bar = bars + (k % kDecodeStages);
-    if (pid < 0 || pid >= p.num_pages) {
-      flag_status(p.status, 0x1);
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-      return;
+  // scores of tokens (g, g + 8) of one staged page, log2 units, -inf if masked
+  auto scores = [&](const uint8_t* st, int tok0, float& sc0, float& sc1) {
+    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t w0[KWORDS], w1[KWORDS];
+    lds_words<KSLICE>(st + g * KB + c * KSLICE, w0);
+    lds_words<KSLICE>(st + (g + 8) * KB + c * KSLICE, w1);
+    uint32_t p0[2 * NJ], p1[2 * NJ];
+    kconv<BK, KWORDS>(w0, p0);
+    kconv<BK, KWORDS>(w1, p1);
+#pragma unroll
+    for (int j = 0; j < NJ; j += 2) {   // two independent accumulator chains
+      const uint32_t x[4] = {p0[2 * j], p1[2 * j], p0[2 * j + 1], p1[2 * j + 1]};
+      mma_16816(a0, x, bq[j][0], bq[j][1]);
+      const uint32_t y[4] = {p0[2 * j + 2], p1[2 * j + 2], p0[2 * j + 3], p1[2 * j + 3]};
+      mma_16816(a1, y, bq[j + 1][0], bq[j + 1][1]);
     }
-    mbar_expect_tx(bar, CHUNK);
-    bulk_g2s(stages + (k % kDecodeStages) * p.stage_bytes,
-             head_base + static_cast<size_t>(pid) * p.geom.page_bytes, CHUNK, bar);
+    const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + kPage * (KB + VB));
+    const float2 k0 = __half22float2(*reinterpret_cast<const __half2*>(ksz + g));
+    const float2 k1 = __half22float2(*reinterpret_cast<const __half2*>(ksz + g + 8));
+    sc0 = tok0 + g < lq ? __fmaf_rn(k0.x, (a0[0] + a0[1]) + (a1[0] + a1[1]), k0.y * qs)
+                        : -CUDART_INF_F;
+    sc1 = tok0 + g + 8 < lq ? __fmaf_rn(k1.x, (a0[2] + a0[3]) + (a1[2] + a1[3]), k1.y * qs)
+                            : -CUDART_INF_F;
+  };
+  // p (already exp'ed, 0 if masked) -> B fragments of the PV MMA; l, zacc
+  auto pfrag = [&](const uint8_t* st, float p0, float p1, uint32_t& pb0, uint32_t& pb1) {
+    const uint32_t* vsz = reinterpret_cast<const uint32_t*>(st + kPage * (KB + VB)) + kPage;
+    const float2 v0 = __half22float2(*reinterpret_cast<const __half2*>(vsz + g));
+    const float2 v1 = __half22float2(*reinterpret_cast<const __half2*>(vsz + g + 8));
+    const float ps0 = p0 > 0.f ? p0 * v0.x : 0.f;   // masked tokens: garbage s, z ignored
+    const float ps1 = p1 > 0.f ? p1 * v1.x : 0.f;
+    if (p0 > 0.f) zacc = __fmaf_rn(p0, v0.y, zacc);
+    if (p1 > 0.f) zacc = __fmaf_rn(p1, v1.y, zacc);
+    l += p0 + p1;
+    const __half2 hi = __floats2half2_rn(ps0, ps1);
+    const float2 hf = __half22float2(hi);
+    const __half2 lo = __floats2half2_rn(ps0 - hf.x, ps1 - hf.y);
+    const uint32_t hip = *reinterpret_cast<const uint32_t*>(&hi);
+    const uint32_t lop = *reinterpret_cast<const uint32_t*>(&lo);
+    const int src1 = 4 * c + (g >> 1), src2 = src1 + 16;
+    const uint32_t h1 = __shfl_sync(kFullMask, hip, src1);
+    const uint32_t l1 = __shfl_sync(kFullMask, lop, src1);
+    const uint32_t h2 = __shfl_sync(kFullMask, hip, src2);
+    const uint32_t l2 = __shfl_sync(kFullMask, lop, src2);
+    pb0 = (g & 1) ? l1 : h1;
+    pb1 = (g & 1) ? l2 : h2;
+  };
+  // values: tokens (c, c+8) and (c+4, c+12), dims [g D/8, (g+1) D/8)
+  auto pv = [&](const uint8_t* st, uint32_t pb0, uint32_t pb1) {
+    const uint8_t* vc = st + kPage * KB;
+    uint32_t a0[VWORDS], a1[VWORDS], b0[VWORDS], b1[VWORDS];
+    lds_words<VSLICE>(vc + c * VB + g * VSLICE, a0);
+    lds_words<VSLICE>(vc + (c + 8) * VB + g * VSLICE, a1);
+    lds_words<VSLICE>(vc + (c + 4) * VB + g * VSLICE, b0);
+    lds_words<VSLICE>(vc + (c + 12) * VB + g * VSLICE, b1);
+    uint32_t pa[VPAIRS], pb[VPAIRS];
+    vconv<BV, VWORDS>(a0, a1, pa);
+    vconv<BV, VWORDS>(b0, b1, pb);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const uint32_t x[4] = {pa[2 * j], pa[2 * j + 1], pb[2 * j], pb[2 * j + 1]};
+      mma_16816(oacc[j], x, pb0, pb1);
+    }
   };
 
-  if (lane == 0) {
-    for (int k = 0; k < nk && k < kDecodeStages; ++k) issue(k);
-  }
-  __syncwarp();
-
-  int k = 0;
   bool timed_out = false;
-  for (; k < nk; ++k) {
-    const int st = k % kDecodeStages;
-    const unsigned par = (k / kDecodeStages) & 1;
-    const bool ok = mbar_wait_bounded(bars + st, par);
+  int k = 0;
+  for (; k < nk; k += 2) {                    // two pages per iteration
+    if (k >= 32 * (chunk + 1)) {
+      ++chunk;
+      pid_cur = pid_nxt;
+      pid_nxt = load_chunk(chunk + 1);
+    }
+    const bool has_b = k + 1 < nk;            // warp-uniform
+    const int pid_a = pid_of(k);
+    const int pid_b = has_b ? pid_of(k + 1) : -1;
+    bool ok = mbar_wait_bounded(bars + (k % NST), (k / NST) & 1);
+    if (has_b) ok = mbar_wait_bounded(bars + ((k + 1) % NST), ((k + 1) / NST) & 1) && ok;
     if (!__all_sync(kFullMask, ok)) {
       timed_out = true;
       break;
     }
-    const int pg = first + kDecodeWarps * k;
-    const int pid = __ldg(ptab + pg);
-    if (pid >= 0 && pid < p.num_pages) {
-      const uint8_t* kc = stages + st * p.stage_bytes;
-      const uint8_t* vc = kc + kPage * KB;
-      const uint32_t* ksz = reinterpret_cast<const uint32_t*>(vc + kPage * VB);
-      const uint32_t* vsz = ksz + kPage;
-      const int tok0 = pg * kPage;
-      const bool valid0 = tok0 + g < lq, valid1 = tok0 + g + 8 < lq;
+    const bool va = pid_a >= 0 && pid_a < p.num_pages;
+    const bool vb = has_b && pid_b >= 0 && pid_b < p.num_pages;
+    const uint8_t* sta = stages + (k % NST) * p.stage_bytes;
+    const uint8_t* stb = stages + ((k + 1) % NST) * p.stage_bytes;
+    const int tok_a = (first + kDecodeWarps * k) * kPage;
+    const int tok_b = tok_a + kDecodeWarps * kPage;
 
-      // ---- scores
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        uint32_t w0[KWORDS], w1[KWORDS];
-        lds_words<KSLICE>(kc + g * KB + c * KSLICE, w0);
-        lds_words<KSLICE>(kc + (g + 8) * KB + c * KSLICE, w1);
-        uint32_t p0[2 * NJ], p1[2 * NJ];
-        kconv<BK, KWORDS>(w0, p0);
-        kconv<BK, KWORDS>(w1, p1);
+    float sa0 = -CUDART_INF_F, sa1 = -CUDART_INF_F, sb0 = -CUDART_INF_F, sb1 = -CUDART_INF_F;
+    if (va) scores(sta, tok_a, sa0, sa1);
+    if (vb) scores(stb, tok_b, sb0, sb1);
+
+    // online softmax over the 32 tokens, per query head c
+    const float mnew = fmaxf(m, warp_max_group(fmaxf(fmaxf(sa0, sa1), fmaxf(sb0, sb1))));
+    const bool grow = mnew > m;
+    if (__any_sync(kFullMask, grow)) {
+      const float alpha = grow ? ex2(m - mnew) : 1.f;
+      l *= alpha;
+      zacc *= alpha;
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-          const uint32_t a[4] = {p0[2 * j], p1[2 * j], p0[2 * j + 1], p1[2 * j + 1]};
-          mma_16816(sacc, a, bq[j][0], bq[j][1]);
-        }
+      for (int j = 0; j < NJ; ++j) {
+        oacc[j][0] *= alpha; oacc[j][1] *= alpha; oacc[j][2] *= alpha; oacc[j][3] *= alpha;
       }
-      const __half2 kz0 = *reinterpret_cast<const __half2*>(ksz + g);
-      const __half2 kz1 = *reinterpret_cast<const __half2*>(ksz + g + 8);
-      const float sc0 = valid0 ? __fmaf_rn(__low2float(kz0), sacc[0] + sacc[1],
-                                           __high2float(kz0) * qs)
-                               : -CUDART_INF_F;
-      const float sc1 = valid1 ? __fmaf_rn(__low2float(kz1), sacc[2] + sacc[3],
-                                           __high2float(kz1) * qs)
-                               : -CUDART_INF_F;
-
-      // ---- online softmax (per query head c, over the 8 lanes sharing c)
-      const float mnew = fmaxf(m, warp_max_group(fmaxf(sc0, sc1)));
-      const bool grow = mnew > m;
-      if (__any_sync(kFullMask, grow)) {
-        const float alpha = grow ? exp2f(m - mnew) : 1.f;
-        l *= alpha;
-        zacc *= alpha;
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-          oacc[j][0] *= alpha; oacc[j][1] *= alpha; oacc[j][2] *= alpha; oacc[j][3] *= alpha;
-        }
-        m = mnew;
-      }
-      const float pr0 = valid0 ? exp2f(sc0 - m) : 0.f;
-      const float pr1 = valid1 ? exp2f(sc1 - m) : 0.f;
-      l += pr0 + pr1;
-      const __half2 vz0 = *reinterpret_cast<const __half2*>(vsz + g);
-      const __half2 vz1 = *reinterpret_cast<const __half2*>(vsz + g + 8);
-      const float ps0 = valid0 ? pr0 * __low2float(vz0) : 0.f;
-      const float ps1 = valid1 ? pr1 * __low2float(vz1) : 0.f;
-      if (valid0) zacc = __fmaf_rn(pr0, __high2float(vz0), zacc);
-      if (valid1) zacc = __fmaf_rn(pr1, __high2float(vz1), zacc);
-
-      // ---- P (p * s_V, hi / lo) into the B-fragment layout of the PV MMA
-      const __half hi0 = __float2half_rn(ps0), hi1 = __float2half_rn(ps1);
-      const uint32_t hip = pack_half2(hi0, hi1);
-      const uint32_t lop = pack_half2(__float2half_rn(ps0 - __half2float(hi0)),
-                                      __float2half_rn(ps1 - __half2float(hi1)));
-      const int src1 = 4 * c + (g >> 1), src2 = 4 * (c + 4) + (g >> 1);
-      const uint32_t h1 = __shfl_sync(kFullMask, hip, src1);
-      const uint32_t l1 = __shfl_sync(kFullMask, lop, src1);
-      const uint32_t h2 = __shfl_sync(kFullMask, hip, src2);
-      const uint32_t l2 = __shfl_sync(kFullMask, lop, src2);
-      const uint32_t pb0 = (g & 1) ? l1 : h1;
-      const uint32_t pb1 = (g & 1) ? l2 : h2;
-
-      // ---- values: tokens (c, c+8) and (c+4, c+12), dims [g D/8, (g+1) D/8)
-      {
-        uint32_t a0[VWORDS], a1[VWORDS], b0[VWORDS], b1[VWORDS];
-        lds_words<VSLICE>(vc + c * VB + g * VSLICE, a0);
-        lds_words<VSLICE>(vc + (c + 8) * VB + g * VSLICE, a1);
-        lds_words<VSLICE>(vc + (c + 4) * VB + g * VSLICE, b0);
-        lds_words<VSLICE>(vc + (c + 12) * VB + g * VSLICE, b1);
-        uint32_t pa[VPAIRS], pb[VPAIRS];
-        vconv<BV, VWORDS>(a0, a1, pa);
-        vconv<BV, VWORDS>(b0, b1, pb);
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-          const uint32_t a[4] = {pa[2 * j], pa[2 * j + 1], pb[2 * j], pb[2 * j + 1]};
-          mma_16816(oacc[j], a, pb0, pb1);
-        }
-      }
+      m = mnew;
+    }
+    if (va) {
+      uint32_t pb0, pb1;
+      pfrag(sta, sa0 > -CUDART_INF_F ? ex2(sa0 - m) : 0.f,
+            sa1 > -CUDART_INF_F ? ex2(sa1 - m) : 0.f, pb0, pb1);
+      pv(sta, pb0, pb1);
+    }
+    if (vb) {
+      uint32_t pb0, pb1;
+      pfrag(stb, sb0 > -CUDART_INF_F ? ex2(sb0 - m) : 0.f,
+            sb1 > -CUDART_INF_F ? ex2(sb1 - m) : 0.f, pb0, pb1);
+      pv(stb, pb0, pb1);
     }
     __syncwarp();
-    if (lane == 0 && k + kDecodeStages < nk) issue(k + kDecodeStages);
+    if (k + NST < nk) {
+      const int pid = pid_of(k + NST);
+      if (lane == 0) issue(k + NST, pid);
+    }
+    if (k + 1 + NST < nk) {
+      const int pid = pid_of(k + 1 + NST);
+      if (lane == 0) issue(k + 1 + NST, pid);
+    }
   }
   if (timed_out) {
     if (lane == 0) flag_status(p.status, 0x8);
-    for (int kk = k; kk < nk && kk < k + kDecodeStages; ++kk)
-      (void)mbar_wait_bounded(bars + (kk % kDecodeStages), (kk / kDecodeStages) & 1);
+    for (int kk = k; kk < nk && kk < k + NST; ++kk)
+      (void)mbar_wait_bounded(bars + (kk % NST), (kk / NST) & 1);
   }
 
   // ---- warp partial -> shared, then CTA merge -> global partial
@@ -396,7 +477,7 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
       for (int w = 0; w < kDecodeWarps; ++w) {
         const float* row = mrg + (w * kMaxGroup + i) * (D + 2);
         const float mw = row[D];
-        if (mw != -CUDART_INF_F) r = __fmaf_rn(exp2f(mw - mm), row[d], r);
+        if (mw != -CUDART_INF_F) r = __fmaf_rn(ex2(mw - mm), row[d], r);
       }
     }
     part[i * (D + 2) + d] = r;
@@ -544,8 +625,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
   float* part = parts + static_cast<size_t>(split) * kMaxGroup * (D + 2);
   const bool is_window = split >= p.S;
 
-  // queries of the group: rotated and scaled by softmax_scale * log2(e) / n for
-  // the quantized splits, scaled only for the window split
+  // queries of the group (rotated and scaled inside the splits' prologue)
   for (int idx = tid; idx < kMaxGroup * D; idx += kThreads) {
     const int i = idx / D, d = idx - i * D;
     float x = 0.f;
@@ -561,33 +641,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
     mbar_init_fence();
   }
   __syncthreads();
-  if (!is_window) {
-    const int nb = p.had_block;
-    for (int hs = 1; hs < nb; hs <<= 1) {
-      for (int idx = tid; idx < kMaxGroup * (D / 2); idx += kThreads) {
-        const int i = idx / (D / 2), r = idx - i * (D / 2);
-        const int lo = (r / hs) * 2 * hs + (r % hs);
-        const float a = sm.qtab[i * D + lo], c = sm.qtab[i * D + lo + hs];
-        sm.qtab[i * D + lo] = a + c;
-        sm.qtab[i * D + lo + hs] = a - c;
-      }
-      __syncthreads();
-    }
-  }
-  const float qscale = is_window ? p.scale_log2 : p.scale_log2 / static_cast<float>(p.had_block);
-  for (int idx = tid; idx < kMaxGroup * D; idx += kThreads) sm.qtab[idx] *= qscale;
-  __syncthreads();
-  {
-    const int warp = tid >> 5, lane = tid & 31;
-    float s = 0.f;
-    for (int d = lane; d < D; d += 32) s += sm.qtab[warp * D + d];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFullMask, s, o);
-    if (lane == 0) sm.qsum[warp] = s;
-  }
-  __syncthreads();
 
   if (is_window) {
+    query_prologue<D>(p, sm, false);
     window_split<D>(p, sm, b, h, len, lq, part);
   } else {
     const int bk = p.geom.bits[h][0], bv = p.geom.bits[h][1];
@@ -634,12 +690,28 @@ size_t smem_bytes(const DecodeParams& p) {
   return header_bytes(D) + area;
 }
 
+// Lets decode_kernel<D> use up to the device's opt-in shared memory (set once
+// per device; never lowered, so any smaller size launches too).
+template <int D>
+cudaError_t allow_smem() {
+  static int done[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  int optin = 0;
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
+  return e;
+}
+
 template <int D>
 cudaError_t launch_d(const DecodeParams& p, cudaStream_t s) {
   const size_t bytes = smem_bytes<D>(p);
   if (bytes > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    const cudaError_t e = allow_smem<D>();
     if (e != cudaSuccess) return e;
   }
   const dim3 grid(p.NS, p.Hkv, p.B);
@@ -650,6 +722,21 @@ cudaError_t launch_d(const DecodeParams& p, cudaStream_t s) {
 }  // namespace
 
 int decode_max_splits() { return kMaxSplits; }
+
+int decode_blocks_per_sm(int head_dim, size_t smem) {
+  int n = 0;
+  cudaError_t e;
+  if (head_dim == 128) {
+    e = allow_smem<128>();
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<128>, kThreads, smem);
+  } else {
+    e = allow_smem<64>();
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<64>, kThreads, smem);
+  }
+  return e == cudaSuccess ? n : -1;
+}
 
 size_t decode_smem_bytes(const DecodeParams& p, int head_dim) {
   return head_dim == 128 ? smem_bytes<128>(p) : smem_bytes<64>(p);

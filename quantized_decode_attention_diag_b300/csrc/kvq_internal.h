@@ -54,12 +54,14 @@ struct DecodeParams {
 };
 
 constexpr int kDecodeWarps = 4;
-constexpr int kDecodeStages = 4;
+constexpr int kDecodeStages = 6;
 constexpr int kAppendWarps = 8;
 
 // Launchers (defined in the .cu files).  Return cudaSuccess or the launch error.
 cudaError_t launch_append(const AppendParams& p, int head_dim, int had_block, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, cudaStream_t s);
 size_t decode_smem_bytes(const DecodeParams& p, int head_dim);
+int decode_blocks_per_sm(int head_dim, size_t smem);   // resident CTAs per SM, -1 on error
+int decode_max_splits();
 
 }  // namespace kvq
