@@ -153,6 +153,33 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, int layer, const void* q, int
                            size_t ws_bytes, void* stream);
 
 /*
+ * kvq_decode_attn_static -- kvq_decode_attn without a caller workspace.
+ * The pages have no counterpart of this call: it exists for callers that cannot
+ * allocate device memory -- a plugin inside a host process whose device memory
+ * is owned and budgeted by that process's allocator, or a latency-critical path
+ * that must not reach cudaMalloc / cudaFree because they can synchronise the
+ * device.  It runs the same decode as kvq_decode_attn (same arguments minus
+ * workspace and ws_bytes) with its scratch in a fixed device array of
+ * KVQ_STATIC_WORKSPACE_BYTES owned by the library, which every GPU that loads
+ * the library holds until the process exits.  It calls no allocating routine.
+ *   - Its first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call shares the array and it keeps the last call's contents; the
+ *     call clears the part that must start at zero (an async memset on
+ *     `stream`) itself.  Calls whose work overlaps on the GPU (other streams,
+ *     other host threads) race on the array: serialise them.
+ *   - Returns KVQ_EWORKSPACE, launching nothing, when the decode needs more
+ *     scratch than KVQ_STATIC_WORKSPACE_BYTES (kvq_decode_workspace_bytes tells
+ *     how much); use kvq_decode_attn with a workspace then.
+ */
+#define KVQ_STATIC_WORKSPACE_BYTES (8 * 1024 * 1024)
+kvq_status kvq_decode_attn_static(const kvq_cache* cache, int layer, const void* q,
+                                  int q_is_fp32, const int32_t* page_table, int max_pages,
+                                  const int32_t* seq_lens, int B, int Hq, float softmax_scale,
+                                  float* o, void* stream);
+
+/*
  * kvq_alloc_bits -- RateQuant greedy marginal-gain bit allocation (host only).
  * Follows the RateQuant technical summary, Methodology section 1 (distortion
  * model D(b) = alpha * beta^-b, objective min sum_i w_i D_i(b_i) subject to

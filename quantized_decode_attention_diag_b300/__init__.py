@@ -66,6 +66,8 @@ _SIGS = {
     "kvq_decode_workspace_bytes": (_SZ, [ctypes.POINTER(kvq_cache), _I, _I, _I]),
     "kvq_decode_attn": (_I, [ctypes.POINTER(kvq_cache), _I, _P, _I, _P, _I, _P, _I, _I, _F, _P,
                              _P, _SZ, _P]),
+    "kvq_decode_attn_static": (_I, [ctypes.POINTER(kvq_cache), _I, _P, _I, _P, _I, _P, _I, _I,
+                                    _F, _P, _P]),
     "kvq_alloc_bits": (_I, [_P, _P, _I, _LL, _P, _P, _P]),
     "kvq_get_status": (_I, [ctypes.POINTER(kvq_cache), ctypes.POINTER(ctypes.c_int)]),
     "kvq_reset_status": (_I, [ctypes.POINTER(kvq_cache), _P]),
@@ -152,6 +154,23 @@ def kvq_decode_attn(desc: kvq_cache, layer: int, q, q_is_fp32: bool, page_table,
                                  _ptr(page_table), max_pages, _ptr(seq_lens), B, Hq,
                                  float(softmax_scale), _ptr(o), _ptr(workspace), int(ws_bytes),
                                  _stream(stream)))
+
+
+STATIC_WORKSPACE_BYTES = 8 * 1024 * 1024   # KVQ_STATIC_WORKSPACE_BYTES in kvq.h
+
+
+def kvq_decode_attn_static(desc: kvq_cache, layer: int, q, q_is_fp32: bool, page_table,
+                           max_pages: int, seq_lens, B: int, Hq: int, softmax_scale: float, o,
+                           stream=None) -> None:
+    """kvq_decode_attn with the library's own fixed scratch instead of a workspace.
+
+    For callers that may not allocate device memory (a plugin whose host owns
+    every device byte, a path that must not hit cudaMalloc).  Make the first
+    call on a device before any stream capture; calls that overlap on the GPU
+    share the scratch and race."""
+    _check(lib().kvq_decode_attn_static(ctypes.byref(desc), layer, _ptr(q), int(bool(q_is_fp32)),
+                                        _ptr(page_table), max_pages, _ptr(seq_lens), B, Hq,
+                                        float(softmax_scale), _ptr(o), _stream(stream)))
 
 
 def kvq_alloc_bits(w: Sequence[float], beta: Sequence[float], budget: int,
@@ -282,5 +301,6 @@ __all__ = [
     "KVQ_EWORKSPACE", "DEV_BAD_PAGE", "DEV_BAD_LENGTH", "DEV_NONFINITE", "DEV_COPY_TIMEOUT",
     "KvqError", "KvqLibraryMissing", "kvq_cache", "lib", "kvq_version", "kvq_last_error",
     "kvq_page_bytes", "kvq_append", "kvq_decode_workspace_bytes", "kvq_decode_attn",
+    "kvq_decode_attn_static", "STATIC_WORKSPACE_BYTES",
     "kvq_alloc_bits", "kvq_get_status", "kvq_reset_status", "mask_of", "Cache",
 ]

@@ -158,6 +158,12 @@ kvq_status plan_decode(const kvq_cache* c, const kvq::LayerGeom& g, int B, int m
 
 }  // namespace
 
+namespace kvq {
+kvq_status set_last_error(kvq_status status, const char* message) {
+  return fail(status, "%s", message);
+}
+}  // namespace kvq
+
 extern "C" {
 
 size_t kvq_page_bytes(const kvq_cache* cache, int layer) {

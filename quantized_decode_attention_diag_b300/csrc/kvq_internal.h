@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "kvq.h"
+
 namespace kvq {
 
 constexpr int kPage = 16;        // tokens per page (= MMA M dimension)
@@ -63,5 +65,8 @@ cudaError_t launch_decode(const DecodeParams& p, int head_dim, cudaStream_t s);
 size_t decode_smem_bytes(const DecodeParams& p, int head_dim);
 int decode_blocks_per_sm(int head_dim, size_t smem);   // resident CTAs per SM, -1 on error
 int decode_max_splits();
+
+// Records `message` for kvq_last_error() on this thread and returns `status`.
+kvq_status set_last_error(kvq_status status, const char* message);
 
 }  // namespace kvq
