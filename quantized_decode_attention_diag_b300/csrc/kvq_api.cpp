@@ -105,7 +105,7 @@ int sm_count() {
 }
 
 struct Plan {
-  int S, NS, pages_per_split, stage_bytes;
+  int S, NS, pages_per_split, stage_bytes, cluster;
   size_t counter_bytes, bytes;
 };
 
@@ -150,6 +150,7 @@ kvq_status plan_decode(const kvq_cache* c, const kvq::LayerGeom& g, int B, int m
   pl->pages_per_split = pps;
   pl->stage_bytes = probe.stage_bytes;
   pl->NS = pl->S + (c->window > 0 ? 1 : 0);
+  pl->cluster = pl->NS <= kvq::decode_max_cluster() ? 1 : 0;
   pl->counter_bytes = (static_cast<size_t>(units) * 4 + 255) / 256 * 256;
   pl->bytes = pl->counter_bytes + static_cast<size_t>(units) * pl->NS * kvq::kMaxGroup *
                                       (c->head_dim + 2) * sizeof(float);
@@ -282,6 +283,7 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, int layer, const void* q, int
   p.S = pl.S;
   p.NS = pl.NS;
   p.pages_per_split = pl.pages_per_split;
+  p.cluster = pl.cluster;
   p.stage_bytes = pl.stage_bytes;
   p.scale_log2 = scale * 1.4426950408889634f;
   const cudaError_t e = kvq::launch_decode(p, cache->head_dim, static_cast<cudaStream_t>(stream));

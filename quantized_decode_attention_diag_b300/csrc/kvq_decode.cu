@@ -10,14 +10,20 @@
 //
 // Grid (NS, Hkv, B): split s < S covers a contiguous range of quantized pages of
 // sequence b for KV head h and its G <= 4 query heads; split S (when R > 0)
-// covers the bf16 window.  Each CTA writes an online-softmax partial
-// (m, l, acc[d]) per query head; the last CTA of (b, h) to finish (an atomic
-// ticket, no waiting) merges them and writes o.
+// covers the bf16 window.  Each CTA merges its warps into one online-softmax
+// partial (m, l, rotated acc[d] per query head).  Merge of the NS partials of a
+// (b, h):
+//   - cluster mode (NS <= 8): the NS CTAs form a thread-block cluster; after a
+//     cluster barrier, CTA 0 reads every partial straight from the others'
+//     shared memory (distributed shared memory), un-rotates and writes o -- no
+//     global partials, fences or atomics;
+//   - ticket mode: partials go to global memory and the last CTA of (b, h) to
+//     finish (an atomic ticket, no waiting) merges them.
 //
 // Quantized split, per warp: pages w, w + 4, ... of the split stream through a
-// 4-stage ring of shared-memory buffers, each filled by one cp.async.bulk of
-// the (page, head) segment (TMA engine, completion on an mbarrier).  A page is
-// 16 tokens = the M dimension of one m16n8k16 tensor-core MMA:
+// ring of shared-memory stages, each filled by one cp.async.bulk of a whole
+// (page, head) segment (TMA engine, completion on an mbarrier).  A page is 16
+// tokens = the M dimension of one m16n8k16 tensor-core MMA:
 //   scores:  S[16 tok x 8] = C_K[16 tok x d] * Qhl[d x 8]
 //   output:  O[d x 8]     += C_V^T[d x 16 tok] * Phl[16 tok x 8]
 // where the 8 columns are the 4 query heads of the GQA group, each split into
@@ -36,53 +42,99 @@ namespace {
 
 constexpr int kThreads = kDecodeWarps * 32;
 constexpr int kMaxSplits = 256;
+constexpr int kMaxCluster = 8;    // portable cluster size
 
 struct Smem {
-  float* qtab;        // [kMaxGroup][D]   rotated, scaled queries (or raw for the window)
+  float* qtab;        // [kMaxGroup][D]   rotated query fragments (or raw query for the window)
   float* qsum;        // [kMaxGroup]
-  int* flag;
+  int* flag;          // last-arriver flag of the ticket
+  int* bad;           // a page id of this split was out of range
+  float* qscl;        // [kMaxGroup] power-of-two scale of the query fragments
   uint64_t* bars;     // [warps][stages]
-  uint8_t* area;      // stage buffers / merge / window / combine scratch
+  float* merge;       // [warps][kMaxGroup][D + 2] warp partials
+  float* cpart;       // [kMaxGroup * (D + 2)] this CTA's partial (layout as a global one)
+  uint8_t* area;      // stage buffers / window scores
 };
 
 template <int D>
-__device__ __forceinline__ Smem carve(uint8_t* base, int stage_bytes) {
+__host__ __device__ constexpr int merge_floats() { return kDecodeWarps * kMaxGroup * (D + 2); }
+
+__host__ __device__ constexpr int header_bytes(int d) {
+  return ((d * kMaxGroup * 4 + 64 + kDecodeWarps * kDecodeStages * 8 +
+           (kDecodeWarps + 1) * kMaxGroup * (d + 2) * 4) + 127) / 128 * 128 + 128;
+}
+
+template <int D>
+__device__ __forceinline__ Smem carve(uint8_t* base) {
   Smem s;
   s.qtab = reinterpret_cast<float*>(base);
-  s.qsum = s.qtab + kMaxGroup * D;
-  s.flag = reinterpret_cast<int*>(s.qsum + kMaxGroup);
-  s.bars = reinterpret_cast<uint64_t*>(base + kMaxGroup * D * 4 + 64);
-  s.area = base + kMaxGroup * D * 4 + 64 + kDecodeWarps * kDecodeStages * 8;
-  s.area = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s.area) + 127) & ~uintptr_t(127));
-  (void)stage_bytes;
+  uint8_t* misc = base + kMaxGroup * D * 4;
+  s.qsum = reinterpret_cast<float*>(misc);
+  s.flag = reinterpret_cast<int*>(misc + 16);
+  s.bad = reinterpret_cast<int*>(misc + 20);
+  s.qscl = reinterpret_cast<float*>(misc + 32);
+  s.bars = reinterpret_cast<uint64_t*>(misc + 64);
+  s.merge = reinterpret_cast<float*>(misc + 64 + kDecodeWarps * kDecodeStages * 8);
+  s.cpart = s.merge + merge_floats<D>();
+  uint8_t* a = reinterpret_cast<uint8_t*>(s.cpart + kMaxGroup * (D + 2));
+  s.area = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(a) + 127) & ~uintptr_t(127));
   return s;
 }
 
-__host__ __device__ constexpr int header_bytes(int d) {
-  return ((d * kMaxGroup * 4 + 64 + kDecodeWarps * kDecodeStages * 8) + 127) / 128 * 128 + 128;
+// A partial: acc [kMaxGroup][D] (fp32), then m [kMaxGroup] (log2 units) and
+// l [kMaxGroup]; kMaxGroup * (D + 2) floats, rows 16-byte aligned.
+template <int D>
+__device__ __forceinline__ float* part_acc(float* part, int i) { return part + i * D; }
+template <int D>
+__device__ __forceinline__ const float* part_acc(const float* part, int i) { return part + i * D; }
+template <int D>
+__device__ __forceinline__ float* part_m(float* part) { return part + kMaxGroup * D; }
+template <int D>
+__device__ __forceinline__ const float* part_m(const float* part) { return part + kMaxGroup * D; }
+template <int D>
+__device__ __forceinline__ float* part_l(float* part) { return part + kMaxGroup * D + kMaxGroup; }
+template <int D>
+__device__ __forceinline__ const float* part_l(const float* part) {
+  return part + kMaxGroup * D + kMaxGroup;
 }
 
-// ------------------------------------------------------------ load helpers --
+// Loads of NBYTES per lane from the shared-memory window (ld.shared, 32-bit
+// address).  volatile keeps them after the mbarrier wait that guards the data.
 template <int NBYTES>
-__device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t* w) {
-  if constexpr (NBYTES % 16 == 0) {
-#pragma unroll
-    for (int i = 0; i < NBYTES / 16; ++i) {
-      const uint4 x = reinterpret_cast<const uint4*>(p)[i];
-      w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
-    }
+__device__ __forceinline__ void lds_u32(uint32_t a, uint32_t* w) {
+  if constexpr (NBYTES == 32) {
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(a));
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]) : "r"(a + 16));
+  } else if constexpr (NBYTES == 16) {
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(a));
   } else if constexpr (NBYTES == 8) {
-    const uint2 x = *reinterpret_cast<const uint2*>(p);
-    w[0] = x.x; w[1] = x.y;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(a));
   } else if constexpr (NBYTES == 4) {
-    w[0] = *reinterpret_cast<const uint32_t*>(p);
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[0]) : "r"(a));
   } else {
     static_assert(NBYTES == 2, "unsupported row slice");
-    w[0] = *reinterpret_cast<const uint16_t*>(p);
+    uint16_t x;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(x) : "r"(a));
+    w[0] = x;
   }
 }
 
+__device__ __forceinline__ float2 lds_half2(uint32_t a) {
+  uint32_t x;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x) : "r"(a));
+  return __half22float2(*reinterpret_cast<const __half2*>(&x));
+}
+
 // ------------------------------------------------- K codes -> fp16 pairs ----
+// Exact fp16 integers: a code's bits OR-ed into the mantissa of 1024.0 give
+// 1024 + c * 2^k (k its bit position), brought back to c by one packed fp16
+// subtract or multiply-add.  (Feeding 1024 + c * 2^k to the MMA and taking the
+// offset off afterwards would save that instruction, but the offset inflates
+// the fp32 partial sums of the MMA by up to ~100x, which costs too much score
+// precision on keys with large outlier channels.)
 // Pairs come out in the order whose dims kpair_dims() reports.
 template <int BITS, int NWORDS>
 __device__ __forceinline__ void kconv(const uint32_t* w, uint32_t* pr) {
@@ -190,34 +242,87 @@ __device__ __forceinline__ float warp_sum_group(float x) {
 __device__ __forceinline__ float hi_part(float x) { return __half2float(__float2half_rn(x)); }
 
 // ------------------------------------------------------- query prologue --
-// qtab <- the group's queries scaled by softmax_scale * log2(e) (and, for the
-// quantized splits, rotated: q'' = H q / n); qsum[i] = sum_d qtab[i][d].
+// Per-warp register layout of one D-vector: lane l holds dims [E l, E l + E),
+// E = D / 32.  Warp i < G loads query head h * G + i of sequence b (zeros for
+// i >= G), exactly (bf16 or fp32 to fp32).
+__device__ __forceinline__ uint32_t ldg_nc_u32(const void* ptr) {
+  uint32_t x;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(x) : "l"(ptr));
+  return x;
+}
+__device__ __forceinline__ uint32_t ldg_nc_u16(const void* ptr) {
+  uint16_t x;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(x) : "l"(ptr));
+  return x;
+}
+
 template <int D>
-__device__ void query_prologue(const DecodeParams& p, const Smem& sm, bool rotate) {
-  const int tid = threadIdx.x;
-  if (rotate) {
-    const int nb = p.had_block;
-    for (int hs = 1; hs < nb; hs <<= 1) {
-      for (int idx = tid; idx < kMaxGroup * (D / 2); idx += kThreads) {
-        const int i = idx / (D / 2), r = idx - i * (D / 2);
-        const int lo = (r / hs) * 2 * hs + (r % hs);
-        const float a = sm.qtab[i * D + lo], c = sm.qtab[i * D + lo + hs];
-        sm.qtab[i * D + lo] = a + c;
-        sm.qtab[i * D + lo + hs] = a - c;
-      }
-      __syncthreads();
+__device__ __forceinline__ void load_query(const DecodeParams& p, int b, int h, float (&v)[D / 32]) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = 0.f;
+  if (warp < p.G) {
+    const size_t off = (static_cast<size_t>(b) * p.Hq + h * p.G + warp) * D + E * lane;
+    if (p.q_fp32) {
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        v[e] = __uint_as_float(ldg_nc_u32(reinterpret_cast<const float*>(p.q) + off + e));
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        v[e] = __uint_as_float(ldg_nc_u16(reinterpret_cast<const uint16_t*>(p.q) + off + e) << 16);
     }
   }
-  const float qscale = rotate ? p.scale_log2 / static_cast<float>(p.had_block) : p.scale_log2;
-  for (int idx = tid; idx < kMaxGroup * D; idx += kThreads) sm.qtab[idx] *= qscale;
-  __syncthreads();
-  const int warp = tid >> 5, lane = tid & 31;
-  float s = 0.f;
-  for (int d = lane; d < D; d += 32) s += sm.qtab[warp * D + d];
+}
+
+// First chunk of this warp's page ids (pages first + 4 k, k < 32, lane k),
+// bounded by the page-table row only, so that it can be issued before the
+// sequence length is known; 0 past the row.
+__device__ __forceinline__ int load_page_chunk0(const DecodeParams& p, int b, int split) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pg = split * p.pages_per_split + warp + kDecodeWarps * lane;
+  if (pg >= p.max_pages) return 0;
+  return static_cast<int>(ldg_nc_u32(p.page_table + static_cast<size_t>(b) * p.max_pages + pg));
+}
+
+// Unnormalised block-diagonal Sylvester transform (blocks of nb) of a D-vector
+// held in the per-warp layout: stage hs adds and subtracts the elements
+// (i, i + hs) of every block, first inside a lane, then across lanes.
+template <int E>
+__device__ __forceinline__ void warp_fwht(float (&v)[E], int nb) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFullMask, s, o);
-  if (lane == 0) sm.qsum[warp] = s;
-  __syncthreads();
+  for (int hs = 1; hs < E; hs <<= 1) {
+    if (hs >= nb) break;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if (!(e & hs)) {
+        const float a = v[e], c = v[e + hs];
+        v[e] = a + c;
+        v[e + hs] = a - c;
+      }
+    }
+  }
+  for (int m = 1; m * E < nb; m <<= 1) {  // partner lane = lane ^ m
+    const bool upper = lane & m;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float o = __shfl_xor_sync(kFullMask, v[e], m);
+      v[e] = upper ? o - v[e] : v[e] + o;
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFullMask, x, o);
+  return x;
+}
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kFullMask, x, o));
+  return x;
 }
 
 // 2^x with the hardware approximation (relative error ~2^-22); 2^-inf = 0
@@ -227,10 +332,116 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// fp16 (hi, lo) split of x: hi = fp16(x) in the low half, lo = fp16(x - hi) high.
+__device__ __forceinline__ uint32_t hilo_pair(float x) {
+  const float hi = hi_part(x);
+  const __half2 r = __floats2half2_rn(x, x - hi);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Quantized splits: q'' = (H q / n) * softmax_scale * log2(e) for each query
+// head of the group (warp i: head i).  A power-of-two scale e_i puts
+// max_d |q''| in [2^13, 2^14), so that both fp16 parts of x = e_i q''_d
+// (hi = fp16(x), lo = fp16(x - hi)) stay normal and together carry ~22 bits
+// of x.  Writes qtab[i][d] = the packed pair (hi, lo) (as raw bits),
+// qsum[i] = e_i sum_d q''_d and qscl[i] = 1 / e_i.
+template <int D>
+__device__ void query_quant_prologue(const DecodeParams& p, const Smem& sm, float (&v)[D / 32]) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= kMaxGroup) {
+    __syncthreads();
+    return;
+  }
+  warp_fwht<E>(v, p.had_block);
+  const float qscale = p.scale_log2 / static_cast<float>(p.had_block);
+  float s = 0.f, amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    v[e] *= qscale;
+    s += v[e];
+    amax = fmaxf(amax, fabsf(v[e]));
+  }
+  s = warp_sum(s);
+  amax = warp_max(amax);
+  int ex = 13;
+  if (amax > 0.f && isfinite(amax)) {
+    const int e2 = ((__float_as_int(amax) >> 23) & 0xff) - 127;   // amax in [2^e2, 2^(e2+1))
+    ex = max(-100, min(100, 13 - e2));
+  }
+  const float scl = ldexpf(1.f, ex);
+  uint32_t* qt = reinterpret_cast<uint32_t*>(sm.qtab) + warp * D + E * lane;
+#pragma unroll
+  for (int e = 0; e < E; ++e) qt[e] = hilo_pair(v[e] * scl);
+  if (lane == 0) {
+    sm.qsum[warp] = s * scl;
+    sm.qscl[warp] = ldexpf(1.f, -ex);
+  }
+  __syncthreads();
+}
+
+// Window split: qtab[i][d] = q_d * softmax_scale * log2(e), not rotated.
+template <int D>
+__device__ void query_window_prologue(const DecodeParams& p, const Smem& sm, const float (&v)[D / 32]) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < kMaxGroup) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) sm.qtab[warp * D + E * lane + e] = v[e] * p.scale_log2;
+  }
+  __syncthreads();
+}
+
 // ------------------------------------------------------------ quantized split
+// movmatrix: 8x8 transpose of 16-bit elements across the warp.  In: lane
+// (g, c) holds row g, columns (2c, 2c+1); out: row g of the transpose.
+__device__ __forceinline__ uint32_t movm_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+// CTA merge, warp i: the partials of query head i of the kDecodeWarps warps
+// (merge region) -> the CTA's partial of head i in `out`; `drop` empties it.
+template <int D>
+__device__ __forceinline__ void merge_warps(const Smem& sm, int i, bool drop, float* out) {
+  constexpr int E = D / 32;
+  const int lane = threadIdx.x & 31;
+  const float* macc = sm.merge;
+  const float* mml = macc + kDecodeWarps * kMaxGroup * D;
+  float mw[kDecodeWarps], mm = -CUDART_INF_F;
+#pragma unroll
+  for (int w = 0; w < kDecodeWarps; ++w) {
+    mw[w] = drop ? -CUDART_INF_F : mml[w * kMaxGroup + i];
+    mm = fmaxf(mm, mw[w]);
+  }
+  float acc[E], ll = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll
+  for (int w = 0; w < kDecodeWarps; ++w) {
+    const float f = mw[w] == -CUDART_INF_F ? 0.f : ex2(mw[w] - mm);
+    if (f != 0.f) {
+      ll = __fmaf_rn(f, mml[kDecodeWarps * kMaxGroup + w * kMaxGroup + i], ll);
+      const float* row = macc + (w * kMaxGroup + i) * D + E * lane;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(f, row[e], acc[e]);
+    }
+  }
+  float* dst = part_acc<D>(out, i) + E * lane;
+#pragma unroll
+  for (int e = 0; e < E; ++e) dst[e] = acc[e];
+  if (lane == 0) {
+    part_m<D>(out)[i] = mm;
+    part_l<D>(out)[i] = ll;
+  }
+}
+
+// One split of one (sequence, KV head): pages [split * pps, (split + 1) * pps)
+// of the quantized part; warp w takes pages w, w + 4, ... two at a time.
 template <int D, int BK, int BV>
 __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h, int split,
-                            int lq, float* part) {
+                            int lq, float (&qv)[D / 32], int chunk0) {
   constexpr int KB = D * BK / 8;                 // K code bytes per token
   constexpr int VB = D * BV / 8;
   constexpr int CHUNK = kPage * (KB + VB + 8);   // one (page, head) segment
@@ -244,42 +455,58 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   constexpr int VPAIRS = (BV == 2 ? 16 : BV == 4 ? 8 : 4) * VWORDS;
   static_assert(VPAIRS >= 2 * NJ, "value slice too small");
   constexpr int NST = kDecodeStages;
+  static_assert(NST % 2 == 0, "stages are consumed in pairs");
+  constexpr uint32_t KSZ = kPage * (KB + VB);    // offset of the K (s, z) pairs
+  constexpr uint32_t VSZ = KSZ + 4 * kPage;      // offset of the V (s, z) pairs
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
+  const int num_pages = p.num_pages;
+  const uint32_t stage_bytes = static_cast<uint32_t>(p.stage_bytes);
 
   // ---- this warp's pages: first + 4 k, k < nk; their ids in registers,
-  //      32 per chunk (lane i holds page k = 32 * chunk + i)
+  //      32 per chunk (lane i holds page k = 32 * chunk + i).  Ids outside
+  //      [0, num_pages) are reported, replaced by page 0 so that every copy
+  //      stays in bounds, and the whole split is dropped at the end.
   const int npages = (lq + kPage - 1) / kPage;
   const int pg0 = split * p.pages_per_split;
   const int pg1 = min(npages, pg0 + p.pages_per_split);
   const int first = pg0 + warp;
   const int nk = pg1 > first ? (pg1 - first + kDecodeWarps - 1) / kDecodeWarps : 0;
   const int32_t* ptab = p.page_table + static_cast<size_t>(b) * p.max_pages + first;
+  auto check_chunk = [&](int ch, int pid) -> int {
+    const int kk = 32 * ch + lane;
+    if (kk >= nk) pid = 0;
+    const bool bad = pid < 0 || pid >= num_pages;
+    if (__any_sync(kFullMask, bad)) {
+      if (bad) {
+        flag_status(p.status, KVQ_DEV_BAD_PAGE);
+        *reinterpret_cast<volatile int*>(sm.bad) = 1;
+      }
+      if (bad) pid = 0;
+    }
+    return pid;
+  };
   auto load_chunk = [&](int ch) -> int {
     const int kk = 32 * ch + lane;
-    return kk < nk ? __ldg(ptab + kDecodeWarps * kk) : -1;
+    return check_chunk(ch, kk < nk ? __ldg(ptab + kDecodeWarps * kk) : 0);
   };
   int chunk = 0;
-  int pid_cur = load_chunk(0);
-  int pid_nxt = nk > 32 ? load_chunk(1) : -1;
+  int pid_cur = check_chunk(0, chunk0);
+  int pid_nxt = nk > 32 ? load_chunk(1) : 0;
   auto pid_of = [&](int kk) -> int {  // warp-uniform kk in [32 chunk, 32 chunk + 64)
     const int v = (kk >> 5) == chunk ? pid_cur : pid_nxt;
     return __shfl_sync(kFullMask, v, kk & 31);
   };
-  uint8_t* stages = sm.area + static_cast<size_t>(warp) * NST * p.stage_bytes;
+  uint8_t* stages = sm.area + static_cast<size_t>(warp) * NST * stage_bytes;
+  const uint32_t st0 = smem_u32(stages);        // shared-window address of stage 0
   uint64_t* bars = sm.bars + warp * NST;
   const uint8_t* head_base = p.pool + p.geom.head_off[h];
-  auto issue = [&](int kk, int pid) {  // lane 0 only
-    uint64_t* bar = bars + (kk % NST);
-    if (pid < 0 || pid >= p.num_pages) {
-      flag_status(p.status, 0x1);
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-      return;
-    }
+  const long long page_bytes = p.geom.page_bytes;
+  auto issue = [&](int slot, int pid) {  // lane 0 only; pid already validated
+    uint64_t* bar = bars + slot;
     mbar_expect_tx(bar, CHUNK);
-    bulk_g2s(stages + (kk % NST) * p.stage_bytes,
-             head_base + static_cast<size_t>(pid) * p.geom.page_bytes, CHUNK, bar);
+    bulk_g2s(stages + slot * stage_bytes, head_base + pid * page_bytes, CHUNK, bar);
   };
   // start streaming before the query prologue
   for (int kk = 0; kk < nk && kk < NST; ++kk) {
@@ -287,88 +514,82 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     if (lane == 0) issue(kk, pid);
   }
 
-  query_prologue<D>(p, sm, true);
+  query_quant_prologue<D>(p, sm, qv);
 
-  // ---- B fragments of the rotated, scaled query (hi / lo split), column n = g
+  // ---- B fragments of the K-side MMA: column n = g is query head g / 2, its
+  //      hi part for even g and lo part for odd g
   uint32_t bq[NJ][2];
   {
-    const float* qh = sm.qtab + (g >> 1) * D;
-    const bool lo_part = g & 1;
+    const uint32_t* qh = reinterpret_cast<const uint32_t*>(sm.qtab) + (g >> 1) * D;
+    const int sh = (g & 1) ? 16 : 0;
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
 #pragma unroll
       for (int s2 = 0; s2 < 2; ++s2) {
         int d0, d1;
         kpair_dims<D, BK>(c, 2 * j + s2, d0, d1);
-        float x0 = qh[d0], x1 = qh[d1];
-        if (lo_part) { x0 -= hi_part(x0); x1 -= hi_part(x1); }
-        const __half2 hv = __floats2half2_rn(x0, x1);
-        bq[j][s2] = *reinterpret_cast<const uint32_t*>(&hv);
+        bq[j][s2] = ((qh[d0] >> sh) & 0xffffu) | (((qh[d1] >> sh) & 0xffffu) << 16);
       }
     }
   }
-  const float qs = sm.qsum[c];
+  const float qs = sm.qsum[c];          // scaled sum of the query (head c)
+  const float iscl = sm.qscl[c];        // scores are scaled by 1 / iscl
 
-  float m = -CUDART_INF_F, l = 0.f, zacc = 0.f;
+  // running softmax state of head c in scaled units: m_s = m / iscl
+  float m_s = -CUDART_INF_F, mneg = CUDART_INF_F;  // mneg = -m (true units)
+  float l = 0.f, zacc = 0.f;
   float oacc[NJ][4];
 #pragma unroll
   for (int j = 0; j < NJ; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
 
-  // scores of tokens (g, g + 8) of one staged page, log2 units, -inf if masked
-  auto scores = [&](const uint8_t* st, int tok0, float& sc0, float& sc1) {
-    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+  // per-lane offsets inside a stage
+  const uint32_t koff = g * KB + c * KSLICE;                       // K row g, slice c
+  const uint32_t voff = kPage * KB + g * VSLICE + 2 * c * VB;      // V row 2c, slice g
+
+  // scaled scores of tokens (g, g + 8) of the page staged at `st`
+  auto scores = [&](uint32_t st, float& sc0, float& sc1) {
     uint32_t w0[KWORDS], w1[KWORDS];
-    lds_words<KSLICE>(st + g * KB + c * KSLICE, w0);
-    lds_words<KSLICE>(st + (g + 8) * KB + c * KSLICE, w1);
+    lds_u32<KSLICE>(st + koff, w0);
+    lds_u32<KSLICE>(st + koff + 8 * KB, w1);
+    const float2 k0 = lds_half2(st + KSZ + 4 * g);
+    const float2 k1 = lds_half2(st + KSZ + 4 * g + 32);
     uint32_t p0[2 * NJ], p1[2 * NJ];
     kconv<BK, KWORDS>(w0, p0);
     kconv<BK, KWORDS>(w1, p1);
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < NJ; j += 2) {   // two independent accumulator chains
+    for (int j = 0; j < NJ; ++j) {
       const uint32_t x[4] = {p0[2 * j], p1[2 * j], p0[2 * j + 1], p1[2 * j + 1]};
-      mma_16816(a0, x, bq[j][0], bq[j][1]);
-      const uint32_t y[4] = {p0[2 * j + 2], p1[2 * j + 2], p0[2 * j + 3], p1[2 * j + 3]};
-      mma_16816(a1, y, bq[j + 1][0], bq[j + 1][1]);
+      mma_16816(a, x, bq[j][0], bq[j][1]);
     }
-    const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + kPage * (KB + VB));
-    const float2 k0 = __half22float2(*reinterpret_cast<const __half2*>(ksz + g));
-    const float2 k1 = __half22float2(*reinterpret_cast<const __half2*>(ksz + g + 8));
-    sc0 = tok0 + g < lq ? __fmaf_rn(k0.x, (a0[0] + a0[1]) + (a1[0] + a1[1]), k0.y * qs)
-                        : -CUDART_INF_F;
-    sc1 = tok0 + g + 8 < lq ? __fmaf_rn(k1.x, (a0[2] + a0[3]) + (a1[2] + a1[3]), k1.y * qs)
-                            : -CUDART_INF_F;
+    sc0 = __fmaf_rn(k0.x, a[0] + a[1], k0.y * qs);
+    sc1 = __fmaf_rn(k1.x, a[2] + a[3], k1.y * qs);
   };
-  // p (already exp'ed, 0 if masked) -> B fragments of the PV MMA; l, zacc
-  auto pfrag = [&](const uint8_t* st, float p0, float p1, uint32_t& pb0, uint32_t& pb1) {
-    const uint32_t* vsz = reinterpret_cast<const uint32_t*>(st + kPage * (KB + VB)) + kPage;
-    const float2 v0 = __half22float2(*reinterpret_cast<const __half2*>(vsz + g));
-    const float2 v1 = __half22float2(*reinterpret_cast<const __half2*>(vsz + g + 8));
-    const float ps0 = p0 > 0.f ? p0 * v0.x : 0.f;   // masked tokens: garbage s, z ignored
-    const float ps1 = p1 > 0.f ? p1 * v1.x : 0.f;
-    if (p0 > 0.f) zacc = __fmaf_rn(p0, v0.y, zacc);
-    if (p1 > 0.f) zacc = __fmaf_rn(p1, v1.y, zacc);
+  // p -> B fragments of the V-side MMA (via two 8x8 transposes); l, zacc.
+  // With `guard`, a token with p = 0 (masked) contributes nothing even if its
+  // slot holds a non-finite scale or zero.
+  auto pfrag = [&](uint32_t st, float p0, float p1, bool guard, uint32_t& pb0, uint32_t& pb1) {
+    const float2 v0 = lds_half2(st + VSZ + 4 * g);
+    const float2 v1 = lds_half2(st + VSZ + 4 * g + 32);
+    float ps0 = p0 * v0.x, ps1 = p1 * v1.x;
+    float z0 = v0.y, z1 = v1.y;
+    if (guard) {
+      if (!(p0 > 0.f)) { ps0 = 0.f; z0 = 0.f; }
+      if (!(p1 > 0.f)) { ps1 = 0.f; z1 = 0.f; }
+    }
+    zacc = __fmaf_rn(p0, z0, zacc);
+    zacc = __fmaf_rn(p1, z1, zacc);
     l += p0 + p1;
-    const __half2 hi = __floats2half2_rn(ps0, ps1);
-    const float2 hf = __half22float2(hi);
-    const __half2 lo = __floats2half2_rn(ps0 - hf.x, ps1 - hf.y);
-    const uint32_t hip = *reinterpret_cast<const uint32_t*>(&hi);
-    const uint32_t lop = *reinterpret_cast<const uint32_t*>(&lo);
-    const int src1 = 4 * c + (g >> 1), src2 = src1 + 16;
-    const uint32_t h1 = __shfl_sync(kFullMask, hip, src1);
-    const uint32_t l1 = __shfl_sync(kFullMask, lop, src1);
-    const uint32_t h2 = __shfl_sync(kFullMask, hip, src2);
-    const uint32_t l2 = __shfl_sync(kFullMask, lop, src2);
-    pb0 = (g & 1) ? l1 : h1;
-    pb1 = (g & 1) ? l2 : h2;
+    pb0 = movm_trans(hilo_pair(ps0));
+    pb1 = movm_trans(hilo_pair(ps1));
   };
-  // values: tokens (c, c+8) and (c+4, c+12), dims [g D/8, (g+1) D/8)
-  auto pv = [&](const uint8_t* st, uint32_t pb0, uint32_t pb1) {
-    const uint8_t* vc = st + kPage * KB;
+  // values: token pairs (2c, 2c+1) and (2c+8, 2c+9), dims [g D/8, (g+1) D/8)
+  auto pv = [&](uint32_t st, uint32_t pb0, uint32_t pb1) {
     uint32_t a0[VWORDS], a1[VWORDS], b0[VWORDS], b1[VWORDS];
-    lds_words<VSLICE>(vc + c * VB + g * VSLICE, a0);
-    lds_words<VSLICE>(vc + (c + 8) * VB + g * VSLICE, a1);
-    lds_words<VSLICE>(vc + (c + 4) * VB + g * VSLICE, b0);
-    lds_words<VSLICE>(vc + (c + 12) * VB + g * VSLICE, b1);
+    lds_u32<VSLICE>(st + voff, a0);
+    lds_u32<VSLICE>(st + voff + VB, a1);
+    lds_u32<VSLICE>(st + voff + 8 * VB, b0);
+    lds_u32<VSLICE>(st + voff + 9 * VB, b1);
     uint32_t pa[VPAIRS], pb[VPAIRS];
     vconv<BV, VWORDS>(a0, a1, pa);
     vconv<BV, VWORDS>(b0, b1, pb);
@@ -378,109 +599,126 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
       mma_16816(oacc[j], x, pb0, pb1);
     }
   };
+  // raise the running maximum of head c to cover m_loc (scaled units)
+  auto rescale = [&](float m_loc) {
+    const float mnew = fmaxf(m_s, warp_max_group(m_loc));
+    const bool grow = mnew > m_s;
+    const float alpha = grow ? ex2((m_s - mnew) * iscl) : 1.f;
+    l *= alpha;
+    zacc *= alpha;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      oacc[j][0] *= alpha; oacc[j][1] *= alpha; oacc[j][2] *= alpha; oacc[j][3] *= alpha;
+    }
+    if (grow) {
+      m_s = mnew;
+      mneg = -mnew * iscl;
+    }
+  };
+  // one round: pages A (stage at sta) and, if has_b, B (the next stage); mask
+  // hides the tokens at or beyond lq (only the last page of a sequence has any)
+  auto round = [&](uint32_t sta, bool has_b, bool mask, int tok_a) {
+    const uint32_t stb = sta + stage_bytes;
+    float sa0, sa1, sb0 = -CUDART_INF_F, sb1 = -CUDART_INF_F;
+    scores(sta, sa0, sa1);
+    if (has_b) scores(stb, sb0, sb1);
+    if (mask) {
+      const int tok_b = tok_a + kDecodeWarps * kPage;
+      if (tok_a + g >= lq) sa0 = -CUDART_INF_F;
+      if (tok_a + g + 8 >= lq) sa1 = -CUDART_INF_F;
+      if (tok_b + g >= lq) sb0 = -CUDART_INF_F;
+      if (tok_b + g + 8 >= lq) sb1 = -CUDART_INF_F;
+    }
+    const float m_loc = fmaxf(fmaxf(sa0, sa1), fmaxf(sb0, sb1));
+    if (__any_sync(kFullMask, m_loc > m_s)) rescale(m_loc);
+    uint32_t pa0, pa1, pb0, pb1;
+    pfrag(sta, ex2(__fmaf_rn(sa0, iscl, mneg)), ex2(__fmaf_rn(sa1, iscl, mneg)), mask, pa0, pa1);
+    if (has_b)
+      pfrag(stb, ex2(__fmaf_rn(sb0, iscl, mneg)), ex2(__fmaf_rn(sb1, iscl, mneg)), mask, pb0,
+            pb1);
+    pv(sta, pa0, pa1);
+    if (has_b) pv(stb, pb0, pb1);
+  };
+
+  // the last page of the sequence is partial unless lq is a multiple of 16
+  const bool last_partial = (lq % kPage) != 0 && nk > 0 &&
+                            first + kDecodeWarps * (nk - 1) == npages - 1;
+  const int nfull = nk - (last_partial ? 1 : 0);
 
   bool timed_out = false;
-  int k = 0;
-  for (; k < nk; k += 2) {                    // two pages per iteration
+  int k = 0, sa = 0;
+  unsigned ph = 0;
+  // full rounds: RP full pages each
+  constexpr int RP = kDecodeRoundPages;
+  for (; k + RP <= nfull;) {
+    bool ok = mbar_wait_bounded(bars + sa, ph);
+    if constexpr (RP == 2) ok = mbar_wait_bounded(bars + sa + 1, ph) & ok;
+    if (!__all_sync(kFullMask, ok)) {
+      timed_out = true;
+      break;
+    }
+    round(st0 + sa * stage_bytes, RP == 2, false, 0);
+    // refill the round's stages with pages k + NST (, k + NST + 1)
+    const int pid0 = pid_of(k + NST);
+    const int pid1 = RP == 2 ? pid_of(k + NST + 1) : 0;
+    __syncwarp();
+    if (lane == 0) {
+      if (k + NST < nk) issue(sa, pid0);
+      if (RP == 2 && k + NST + 1 < nk) issue(sa + 1, pid1);
+    }
+    k += RP;
+    sa += RP;
+    if (sa == NST) {
+      sa = 0;
+      ph ^= 1u;
+    }
     if (k >= 32 * (chunk + 1)) {
       ++chunk;
       pid_cur = pid_nxt;
       pid_nxt = load_chunk(chunk + 1);
     }
-    const bool has_b = k + 1 < nk;            // warp-uniform
-    const int pid_a = pid_of(k);
-    const int pid_b = has_b ? pid_of(k + 1) : -1;
-    bool ok = mbar_wait_bounded(bars + (k % NST), (k / NST) & 1);
-    if (has_b) ok = mbar_wait_bounded(bars + ((k + 1) % NST), ((k + 1) / NST) & 1) && ok;
+  }
+  // the rest: at most RP pages, the last maybe partial
+  if (!timed_out && k < nk) {
+    const bool has_b = RP == 2 && k + 1 < nk;
+    bool ok = mbar_wait_bounded(bars + sa, ph);
+    if (has_b) ok = mbar_wait_bounded(bars + sa + 1, ph) && ok;
     if (!__all_sync(kFullMask, ok)) {
       timed_out = true;
-      break;
-    }
-    const bool va = pid_a >= 0 && pid_a < p.num_pages;
-    const bool vb = has_b && pid_b >= 0 && pid_b < p.num_pages;
-    const uint8_t* sta = stages + (k % NST) * p.stage_bytes;
-    const uint8_t* stb = stages + ((k + 1) % NST) * p.stage_bytes;
-    const int tok_a = (first + kDecodeWarps * k) * kPage;
-    const int tok_b = tok_a + kDecodeWarps * kPage;
-
-    float sa0 = -CUDART_INF_F, sa1 = -CUDART_INF_F, sb0 = -CUDART_INF_F, sb1 = -CUDART_INF_F;
-    if (va) scores(sta, tok_a, sa0, sa1);
-    if (vb) scores(stb, tok_b, sb0, sb1);
-
-    // online softmax over the 32 tokens, per query head c
-    const float mnew = fmaxf(m, warp_max_group(fmaxf(fmaxf(sa0, sa1), fmaxf(sb0, sb1))));
-    const bool grow = mnew > m;
-    if (__any_sync(kFullMask, grow)) {
-      const float alpha = grow ? ex2(m - mnew) : 1.f;
-      l *= alpha;
-      zacc *= alpha;
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        oacc[j][0] *= alpha; oacc[j][1] *= alpha; oacc[j][2] *= alpha; oacc[j][3] *= alpha;
-      }
-      m = mnew;
-    }
-    if (va) {
-      uint32_t pb0, pb1;
-      pfrag(sta, sa0 > -CUDART_INF_F ? ex2(sa0 - m) : 0.f,
-            sa1 > -CUDART_INF_F ? ex2(sa1 - m) : 0.f, pb0, pb1);
-      pv(sta, pb0, pb1);
-    }
-    if (vb) {
-      uint32_t pb0, pb1;
-      pfrag(stb, sb0 > -CUDART_INF_F ? ex2(sb0 - m) : 0.f,
-            sb1 > -CUDART_INF_F ? ex2(sb1 - m) : 0.f, pb0, pb1);
-      pv(stb, pb0, pb1);
-    }
-    __syncwarp();
-    if (k + NST < nk) {
-      const int pid = pid_of(k + NST);
-      if (lane == 0) issue(k + NST, pid);
-    }
-    if (k + 1 + NST < nk) {
-      const int pid = pid_of(k + 1 + NST);
-      if (lane == 0) issue(k + 1 + NST, pid);
+    } else {
+      round(st0 + sa * stage_bytes, has_b, last_partial, (first + kDecodeWarps * k) * kPage);
     }
   }
   if (timed_out) {
-    if (lane == 0) flag_status(p.status, 0x8);
-    for (int kk = k; kk < nk && kk < k + NST; ++kk)
-      (void)mbar_wait_bounded(bars + (kk % NST), (kk / NST) & 1);
+    if (lane == 0) flag_status(p.status, KVQ_DEV_COPY_TIMEOUT);
+    // drain the copies still in flight (pages k .. k + NST - 1)
+    int s = sa;
+    unsigned q = ph;
+    for (int kk = k; kk < nk && kk < k + NST; ++kk) {
+      (void)mbar_wait_bounded(bars + s, q);
+      if (++s == NST) {
+        s = 0;
+        q ^= 1u;
+      }
+    }
   }
 
-  // ---- warp partial -> shared, then CTA merge -> global partial
+  // ---- warp partial -> the merge region (the caller merges the warps)
   l = warp_sum_group(l);
   zacc = warp_sum_group(zacc);
+  const float m = m_s == -CUDART_INF_F ? -CUDART_INF_F : m_s * iscl;
   __syncthreads();  // every warp is done with its stage buffers
-  float* mrg = reinterpret_cast<float*>(sm.area);   // [warps][kMaxGroup][D + 2]
-  float* wrow = mrg + (warp * kMaxGroup + c) * (D + 2);
+  float* macc = sm.merge;                                    // [warps][kMaxGroup][D]
+  float* mml = macc + kDecodeWarps * kMaxGroup * D;          // m, l: [warps][kMaxGroup] each
+  float* wrow = macc + (warp * kMaxGroup + c) * D;
 #pragma unroll
   for (int j = 0; j < NJ; ++j) {
     wrow[g * (D / 8) + 2 * j] = oacc[j][0] + oacc[j][1] + zacc;
     wrow[g * (D / 8) + 2 * j + 1] = oacc[j][2] + oacc[j][3] + zacc;
   }
   if (g == 0) {
-    wrow[D] = m;
-    wrow[D + 1] = l;
-  }
-  __syncthreads();
-  for (int idx = tid; idx < p.G * (D + 2); idx += kThreads) {
-    const int i = idx / (D + 2), d = idx - i * (D + 2);
-    float mm = -CUDART_INF_F;
-#pragma unroll
-    for (int w = 0; w < kDecodeWarps; ++w) mm = fmaxf(mm, mrg[(w * kMaxGroup + i) * (D + 2) + D]);
-    float r = 0.f;
-    if (d == D) {
-      r = mm;
-    } else if (mm != -CUDART_INF_F) {
-#pragma unroll
-      for (int w = 0; w < kDecodeWarps; ++w) {
-        const float* row = mrg + (w * kMaxGroup + i) * (D + 2);
-        const float mw = row[D];
-        if (mw != -CUDART_INF_F) r = __fmaf_rn(ex2(mw - mm), row[d], r);
-      }
-    }
-    part[i * (D + 2) + d] = r;
+    mml[warp * kMaxGroup + c] = m;
+    mml[kDecodeWarps * kMaxGroup + warp * kMaxGroup + c] = l;
   }
 }
 
@@ -496,7 +734,7 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
   const uint16_t* vring = kring + static_cast<size_t>(R) * D;
   for (int t = tid; t < nw; t += kThreads) {
     const uint4* kr = reinterpret_cast<const uint4*>(kring + static_cast<size_t>((lq + t) % R) * D);
-    float acc[kMaxGroup] = {0.f, 0.f, 0.f, 0.f};
+    float acc[kMaxGroup] = {};
     for (int i8 = 0; i8 < D / 8; ++i8) {
       const uint4 w = kr[i8];
       const float x[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
@@ -513,19 +751,17 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
   if (warp < p.G) {  // warp i: softmax statistics of query head i
     float mm = -CUDART_INF_F;
     for (int t = lane; t < nw; t += 32) mm = fmaxf(mm, sc[warp * R + t]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(kFullMask, mm, o));
+    mm = warp_max(mm);
     float ll = 0.f;
     for (int t = lane; t < nw; t += 32) {
       const float e = exp2f(sc[warp * R + t] - mm);
       sc[warp * R + t] = e;
       ll += e;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ll += __shfl_xor_sync(kFullMask, ll, o);
+    ll = warp_sum(ll);
     if (lane == 0) {
-      part[warp * (D + 2) + D] = nw > 0 ? mm : -CUDART_INF_F;
-      part[warp * (D + 2) + D + 1] = ll;
+      part_m<D>(part)[warp] = nw > 0 ? mm : -CUDART_INF_F;
+      part_l<D>(part)[warp] = ll;
     }
   }
   __syncthreads();
@@ -536,132 +772,240 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
       const uint16_t raw = vring[static_cast<size_t>((lq + t) % R) * D + d];
       acc = __fmaf_rn(sc[i * R + t], __uint_as_float(static_cast<uint32_t>(raw) << 16), acc);
     }
-    part[i * (D + 2) + d] = acc;
+    part_acc<D>(part, i)[d] = acc;
   }
 }
 
-// -------------------------------------------------------------- the combine
+// E consecutive floats (E = 4 or 2; 16- or 8-byte aligned) bypassing L1.
+template <int E>
+__device__ __forceinline__ void ldcg_vec(const float* ptr, float (&v)[E]) {
+  if constexpr (E == 4) {
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(ptr));
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  } else {
+    const float2 x = __ldcg(reinterpret_cast<const float2*>(ptr));
+    v[0] = x.x; v[1] = x.y;
+  }
+}
+
+// Ticket mode.  Warp i merges query head i of (b, h) over its NS global
+// partials: the softmax weights of the splits (lane k holds split s0 + k of
+// each group of 32), the weighted sum of the quantized splits' rotated
+// accumulators (E dims per lane), the inverse rotation x = H u / n, the window
+// split's accumulator (already in the model's basis), and o.  Loads are
+// grouped so that a few round trips to L2 cover any split count.
 template <int D>
-__device__ void combine(const DecodeParams& p, const Smem& sm, int b, int h,
-                        const float* parts) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  float* wts = reinterpret_cast<float*>(sm.area);         // [kMaxGroup][NS]
-  float* lsum = wts + kMaxGroup * (kMaxSplits + 1);       // [kMaxGroup]
-  float* orot = lsum + kMaxGroup;                          // [kMaxGroup][D]
-  const int NS = p.NS;
-  if (warp < p.G) {
-    float mm = -CUDART_INF_F;
-    for (int s = lane; s < NS; s += 32)
-      mm = fmaxf(mm, __ldcg(parts + (static_cast<size_t>(s) * kMaxGroup + warp) * (D + 2) + D));
+__device__ void combine_global(const DecodeParams& p, int b, int h, const float* parts) {
+  constexpr int E = D / 32;
+  constexpr int PS = kMaxGroup * (D + 2);   // floats per partial
+  constexpr int UN = 8;                     // partial rows in flight at once
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= p.G) return;
+  const int i = warp, NS = p.NS, nq = p.S;
+  float mm = -CUDART_INF_F;
+  for (int s = lane; s < NS; s += 32) mm = fmaxf(mm, __ldcg(part_m<D>(parts + s * PS) + i));
+  mm = warp_max(mm);
+  float ll = 0.f, acc[E], ww = 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(kFullMask, mm, o));
-    float ll = 0.f;
-    for (int s = lane; s < NS; s += 32) {
-      const float* row = parts + (static_cast<size_t>(s) * kMaxGroup + warp) * (D + 2);
-      const float ms = __ldcg(row + D);
-      const float w = (ms == -CUDART_INF_F) ? 0.f : exp2f(ms - mm);
-      wts[warp * (kMaxSplits + 1) + s] = w;
-      if (w != 0.f) ll = __fmaf_rn(w, __ldcg(row + D + 1), ll);
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int s0 = 0; s0 < NS; s0 += 32) {
+    float w = 0.f;
+    if (s0 + lane < NS) {
+      const float ms = __ldcg(part_m<D>(parts + (s0 + lane) * PS) + i);
+      if (ms != -CUDART_INF_F) {
+        w = exp2f(ms - mm);
+        ll = __fmaf_rn(w, __ldcg(part_l<D>(parts + (s0 + lane) * PS) + i), ll);
+      }
     }
+    if (NS > nq && nq >= s0 && nq < s0 + 32) ww = __shfl_sync(kFullMask, w, nq - s0);
+    const int cnt = min(32, nq - s0);   // quantized splits of this group
+    for (int k0 = 0; k0 < cnt; k0 += UN) {
+      float rows[UN][E];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ll += __shfl_xor_sync(kFullMask, ll, o);
-    if (lane == 0) lsum[warp] = ll;
-  }
-  __syncthreads();
-  for (int idx = tid; idx < p.G * D; idx += kThreads) {
-    const int i = idx / D, d = idx - i * D;
-    float acc = 0.f;
-    for (int s = 0; s < p.S; ++s) {
-      const float w = wts[i * (kMaxSplits + 1) + s];
-      if (w != 0.f)
-        acc = __fmaf_rn(w, __ldcg(parts + (static_cast<size_t>(s) * kMaxGroup + i) * (D + 2) + d),
-                        acc);
+      for (int k = 0; k < UN; ++k) {
+        if (k0 + k < cnt) {
+          ldcg_vec<E>(part_acc<D>(parts + (s0 + k0 + k) * PS, i) + E * lane, rows[k]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) rows[k][e] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < UN; ++k) {
+        const float wk = __shfl_sync(kFullMask, w, (k0 + k) & 31);
+        const float wv = k0 + k < cnt ? wk : 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(wv, rows[k][e], acc[e]);
+      }
     }
-    orot[i * D + d] = acc;
   }
-  __syncthreads();
-  // undo the rotation of the value accumulator: x = H u / n (block-diagonal)
-  const int nb = p.had_block;
-  for (int hs = 1; hs < nb; hs <<= 1) {
-    for (int idx = tid; idx < p.G * (D / 2); idx += kThreads) {
-      const int i = idx / (D / 2), r = idx - i * (D / 2);
-      const int lo = (r / hs) * 2 * hs + (r % hs);
-      const float a = orot[i * D + lo], c = orot[i * D + lo + hs];
-      orot[i * D + lo] = a + c;
-      orot[i * D + lo + hs] = a - c;
+  ll = warp_sum(ll);
+  warp_fwht<E>(acc, p.had_block);
+  const float inv_nb = 1.f / static_cast<float>(p.had_block);
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] *= inv_nb;
+  if (NS > nq && ww != 0.f) {
+    float row[E];
+    ldcg_vec<E>(part_acc<D>(parts + nq * PS, i) + E * lane, row);
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(ww, row[e], acc[e]);
+  }
+  float* o = p.o + (static_cast<size_t>(b) * p.Hq + h * p.G + i) * D + E * lane;
+#pragma unroll
+  for (int e = 0; e < E; ++e) o[e] = ll > 0.f ? acc[e] / ll : 0.f;
+}
+
+// ---------------------------------------------------------- cluster merge --
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_dsmem(uint32_t a) {
+  float x;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(x) : "r"(a));
+  return x;
+}
+template <int E>
+__device__ __forceinline__ void ld_dsmem_vec(uint32_t a, float (&v)[E]) {
+  if constexpr (E == 4) {
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(a));
+  } else {
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v[0]), "=f"(v[1]) : "r"(a));
+  }
+}
+
+// Cluster mode (called by CTA 0 of the cluster, after a cluster barrier).
+// Warp i merges query head i of (b, h) over the NS partials held in the
+// cluster's shared memory (cpart of CTA rank s is split s), as combine_global.
+template <int D>
+__device__ void combine_cluster(const DecodeParams& p, const Smem& sm, int b, int h) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= p.G) return;
+  const int i = warp, NS = p.NS, nq = p.S;
+  const float* mine = sm.cpart;
+  // lane s < NS: m and l of split s
+  float ms = -CUDART_INF_F, ls = 0.f;
+  if (lane < NS) {
+    ms = ld_dsmem(dsmem_addr(part_m<D>(mine) + i, lane));
+    ls = ld_dsmem(dsmem_addr(part_l<D>(mine) + i, lane));
+  }
+  const float mm = warp_max(ms);
+  const float w = ms == -CUDART_INF_F ? 0.f : exp2f(ms - mm);
+  const float ll = warp_sum(w * ls);
+  float rows[kMaxCluster][E];
+#pragma unroll
+  for (int s = 0; s < kMaxCluster; ++s) {
+    if (s < NS) {
+      ld_dsmem_vec<E>(dsmem_addr(part_acc<D>(mine, i) + E * lane, s), rows[s]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) rows[s][e] = 0.f;
     }
-    __syncthreads();
   }
-  const float inv_nb = 1.f / static_cast<float>(nb);
-  for (int idx = tid; idx < p.G * D; idx += kThreads) {
-    const int i = idx / D, d = idx - i * D;
-    float val = orot[i * D + d] * inv_nb;
-    if (p.R > 0) {
-      const float ww = wts[i * (kMaxSplits + 1) + p.S];
-      if (ww != 0.f)
-        val = __fmaf_rn(ww, __ldcg(parts + (static_cast<size_t>(p.S) * kMaxGroup + i) * (D + 2) + d),
-                        val);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll
+  for (int s = 0; s < kMaxCluster; ++s) {
+    const float ws = __shfl_sync(kFullMask, w, s);
+    if (s < nq) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(ws, rows[s][e], acc[e]);
     }
-    const float ll = lsum[i];
-    p.o[(static_cast<size_t>(b) * p.Hq + h * p.G + i) * D + d] = ll > 0.f ? val / ll : 0.f;
   }
+  warp_fwht<E>(acc, p.had_block);
+  const float inv_nb = 1.f / static_cast<float>(p.had_block);
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] *= inv_nb;
+  if (NS > nq) {
+    const float ws = __shfl_sync(kFullMask, w, nq);
+#pragma unroll
+    for (int s = 0; s < kMaxCluster; ++s)
+      if (s == nq) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(ws, rows[s][e], acc[e]);
+      }
+  }
+  float* o = p.o + (static_cast<size_t>(b) * p.Hq + h * p.G + i) * D + E * lane;
+#pragma unroll
+  for (int e = 0; e < E; ++e) o[e] = ll > 0.f ? acc[e] / ll : 0.f;
 }
 
 // -------------------------------------------------------------- the kernel --
 template <int D>
-__global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  const Smem sm = carve<D>(smem_raw, p.stage_bytes);
+  const Smem sm = carve<D>(smem_raw);
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5;
 
-  int len = __ldg(p.seq_lens + b);
+  // The query, page-id and length loads go out first: the page copies issued
+  // next fill the memory system for microseconds, and a load queued behind
+  // them would stall the CTA for as long.
+  float qv[D / 32];
+  load_query<D>(p, b, h, qv);
+  const int chunk0 = split < p.S ? load_page_chunk0(p, b, split) : 0;
+  int len = static_cast<int>(ldg_nc_u32(p.seq_lens + b));
   if (len < 0 || len > p.max_pages * kPage) {
-    if (tid == 0) flag_status(p.status, 0x2);
+    if (tid == 0) flag_status(p.status, KVQ_DEV_BAD_LENGTH);
     len = 0;
   }
   const int lq = p.R ? max(0, len - p.R) : len;
-  float* parts = p.partials + (static_cast<size_t>(b) * p.Hkv + h) * p.NS * kMaxGroup * (D + 2);
-  float* part = parts + static_cast<size_t>(split) * kMaxGroup * (D + 2);
   const bool is_window = split >= p.S;
 
-  // queries of the group (rotated and scaled inside the splits' prologue)
-  for (int idx = tid; idx < kMaxGroup * D; idx += kThreads) {
-    const int i = idx / D, d = idx - i * D;
-    float x = 0.f;
-    if (i < p.G) {
-      const size_t off = (static_cast<size_t>(b) * p.Hq + h * p.G + i) * D + d;
-      x = p.q_fp32 ? reinterpret_cast<const float*>(p.q)[off]
-                   : __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(p.q)[off]) << 16);
-    }
-    sm.qtab[idx] = x;
-  }
   if (tid == 0) {
     for (int i = 0; i < kDecodeWarps * kDecodeStages; ++i) mbar_init(sm.bars + i, 1);
+    *sm.bad = 0;
     mbar_init_fence();
   }
   __syncthreads();
 
   if (is_window) {
-    query_prologue<D>(p, sm, false);
-    window_split<D>(p, sm, b, h, len, lq, part);
+    query_window_prologue<D>(p, sm, qv);
+    window_split<D>(p, sm, b, h, len, lq, sm.cpart);
   } else {
     const int bk = p.geom.bits[h][0], bv = p.geom.bits[h][1];
     switch (bk * 16 + bv) {
-      case 0x22: quant_split<D, 2, 2>(p, sm, b, h, split, lq, part); break;
-      case 0x24: quant_split<D, 2, 4>(p, sm, b, h, split, lq, part); break;
-      case 0x28: quant_split<D, 2, 8>(p, sm, b, h, split, lq, part); break;
-      case 0x42: quant_split<D, 4, 2>(p, sm, b, h, split, lq, part); break;
-      case 0x44: quant_split<D, 4, 4>(p, sm, b, h, split, lq, part); break;
-      case 0x48: quant_split<D, 4, 8>(p, sm, b, h, split, lq, part); break;
-      case 0x82: quant_split<D, 8, 2>(p, sm, b, h, split, lq, part); break;
-      case 0x84: quant_split<D, 8, 4>(p, sm, b, h, split, lq, part); break;
-      case 0x88: quant_split<D, 8, 8>(p, sm, b, h, split, lq, part); break;
+      case 0x22: quant_split<D, 2, 2>(p, sm, b, h, split, lq, qv, chunk0); break;
+      case 0x24: quant_split<D, 2, 4>(p, sm, b, h, split, lq, qv, chunk0); break;
+      case 0x28: quant_split<D, 2, 8>(p, sm, b, h, split, lq, qv, chunk0); break;
+      case 0x42: quant_split<D, 4, 2>(p, sm, b, h, split, lq, qv, chunk0); break;
+      case 0x44: quant_split<D, 4, 4>(p, sm, b, h, split, lq, qv, chunk0); break;
+      case 0x48: quant_split<D, 4, 8>(p, sm, b, h, split, lq, qv, chunk0); break;
+      case 0x82: quant_split<D, 8, 2>(p, sm, b, h, split, lq, qv, chunk0); break;
+      case 0x84: quant_split<D, 8, 4>(p, sm, b, h, split, lq, qv, chunk0); break;
+      case 0x88: quant_split<D, 8, 8>(p, sm, b, h, split, lq, qv, chunk0); break;
       default: break;
     }
+    __syncthreads();   // the warps' partials are in the merge region
+    if (warp < p.G) merge_warps<D>(sm, warp, *reinterpret_cast<volatile int*>(sm.bad) != 0, sm.cpart);
   }
+  __syncthreads();     // this CTA's partial is complete in sm.cpart
 
-  // ---- ticket: the last CTA of (b, h) merges every split
+  if (p.cluster) {
+    cluster_sync();    // every partial of (b, h) is complete in its CTA
+    if (cluster_rank() == 0) combine_cluster<D>(p, sm, b, h);
+    cluster_sync();    // no CTA leaves while its partial may still be read
+    return;
+  }
+  // ticket mode: partial to global memory; the last CTA of (b, h) merges
+  constexpr int PS = kMaxGroup * (D + 2);
+  float* parts = p.partials + (static_cast<size_t>(b) * p.Hkv + h) * p.NS * PS;
+  float* part = parts + static_cast<size_t>(split) * PS;
+  for (int k = tid; k < PS; k += kThreads) part[k] = sm.cpart[k];
   __threadfence();
   __syncthreads();
   if (tid == 0) {
@@ -671,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
   __syncthreads();
   if (*sm.flag) {
     __threadfence();
-    combine<D>(p, sm, b, h, parts);
+    combine_global<D>(p, b, h, parts);
     if (tid == 0) p.counters[b * p.Hkv + h] = 0u;
   }
 }
@@ -679,15 +1023,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
 template <int D>
 size_t smem_bytes(const DecodeParams& p) {
   const size_t stages = static_cast<size_t>(kDecodeWarps) * kDecodeStages * p.stage_bytes;
-  const size_t merge = static_cast<size_t>(kDecodeWarps) * kMaxGroup * (D + 2) * 4;
   const size_t win = static_cast<size_t>(kMaxGroup) * p.R * 4;
-  const size_t comb = (static_cast<size_t>(kMaxGroup) * (kMaxSplits + 1) + kMaxGroup +
-                       kMaxGroup * D) * 4;
-  size_t area = stages;
-  if (merge > area) area = merge;
-  if (win > area) area = win;
-  if (comb > area) area = comb;
-  return header_bytes(D) + area;
+  return header_bytes(D) + (stages > win ? stages : win);
 }
 
 // Lets decode_kernel<D> use up to the device's opt-in shared memory (set once
@@ -714,14 +1051,27 @@ cudaError_t launch_d(const DecodeParams& p, cudaStream_t s) {
     const cudaError_t e = allow_smem<D>();
     if (e != cudaSuccess) return e;
   }
-  const dim3 grid(p.NS, p.Hkv, p.B);
-  decode_kernel<D><<<grid, kThreads, bytes, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.NS, p.Hkv, p.B);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (p.cluster) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.NS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D>, p);
 }
 
 }  // namespace
 
 int decode_max_splits() { return kMaxSplits; }
+int decode_max_cluster() { return kMaxCluster; }
 
 int decode_blocks_per_sm(int head_dim, size_t smem) {
   int n = 0;

@@ -43,20 +43,42 @@ struct DecodeParams {
   const int32_t* page_table;
   const int32_t* seq_lens;       // [B], including the window
   float* o;                      // fp32 [B][Hq][D]
-  float* partials;               // fp32 [B][Hkv][NS][kMaxGroup][D + 2]
-  unsigned int* counters;        // [B][Hkv]
+  float* partials;               // fp32 [B][Hkv][NS][kMaxGroup][D + 2] (ticket mode)
+  unsigned int* counters;        // [B][Hkv] tickets (ticket mode)
   int* status;
   int q_fp32, max_pages, B, Hq, Hkv, G, R, num_pages, had_block;
-  int S;                         // quantized-token splits
+  int S;                         // quantized-token splits per (sequence, KV head)
   int NS;                        // S + (R > 0): the window gets its own split
   int pages_per_split;
+  int cluster;                   // 1: the NS CTAs of a unit form a cluster and merge
+                                 // through distributed shared memory (NS <= 8)
   int stage_bytes;               // bytes of one pipeline stage buffer
   float scale_log2;              // softmax_scale * log2(e)
   LayerGeom geom;
 };
 
-constexpr int kDecodeWarps = 4;
-constexpr int kDecodeStages = 6;
+// Decode kernel shape (build-time tuning knobs): warps per CTA, pipeline
+// stages per warp, pages consumed per softmax round (1 or 2), and the minimum
+// resident CTAs per SM the register allocation is sized for.
+#ifndef KVQ_DECODE_WARPS
+#define KVQ_DECODE_WARPS 4
+#endif
+#ifndef KVQ_DECODE_STAGES
+#define KVQ_DECODE_STAGES 4
+#endif
+#ifndef KVQ_DECODE_ROUND
+#define KVQ_DECODE_ROUND 2
+#endif
+#ifndef KVQ_DECODE_MIN_BLOCKS
+#define KVQ_DECODE_MIN_BLOCKS 4
+#endif
+constexpr int kDecodeWarps = KVQ_DECODE_WARPS;
+constexpr int kDecodeStages = KVQ_DECODE_STAGES;
+constexpr int kDecodeRoundPages = KVQ_DECODE_ROUND;
+constexpr int kDecodeMinBlocks = KVQ_DECODE_MIN_BLOCKS;
+static_assert(kDecodeWarps >= 4, "the query prologue uses one warp per query head");
+static_assert(kDecodeRoundPages == 1 || kDecodeRoundPages == 2, "1 or 2 pages per round");
+static_assert(kDecodeStages % kDecodeRoundPages == 0, "stages are consumed a round at a time");
 constexpr int kAppendWarps = 8;
 
 // Launchers (defined in the .cu files).  Return cudaSuccess or the launch error.
@@ -65,6 +87,7 @@ cudaError_t launch_decode(const DecodeParams& p, int head_dim, cudaStream_t s);
 size_t decode_smem_bytes(const DecodeParams& p, int head_dim);
 int decode_blocks_per_sm(int head_dim, size_t smem);   // resident CTAs per SM, -1 on error
 int decode_max_splits();
+int decode_max_cluster();                               // largest cluster the merge uses
 
 // Records `message` for kvq_last_error() on this thread and returns `status`.
 kvq_status set_last_error(kvq_status status, const char* message);
