@@ -11,20 +11,22 @@ Llama-3-8B-shaped decode layer -- batch 16, 32 query / 8 KV heads, head_dim
 replicated over 32 distinct layer caches (2.3 GB of packed KV, far above the
 126 MB L2), so every step streams its cache from HBM.
 
-A step is one serving decode step through all 32 layers: per layer, kvq_append
-quantizes the new token of each of the 16 sequences into the paged cache
-(rotation, scale/zero, codes, paged store) and kvq_decode_attn runs split-K
+A step is one serving decode step through all 32 layers: per layer, one
+kvq_decode_step call quantizes the new token of each of the 16 sequences into
+the paged cache (rotation, scale/zero, codes, paged store) and runs split-K
 attention over the 4096 cached tokens (query rotation, page streaming,
-dequantization in registers, online softmax, combine).  The bit-widths come
-from kvq_alloc_bits at set-up (this workload's widths are uniform: 4 and 4).
-The step is captured once in a CUDA graph and replayed.
+dequantization in registers, online softmax, merge) in a single launch.  The
+bit-widths come from kvq_alloc_bits at set-up (this workload's widths are
+uniform: 4 and 4).  The step is captured once in a CUDA graph and replayed.
 
-value = algorithmic decode bytes of a step (packed codes + fp16 scale/zero per
-(token, KV head): 136 B for K4V4) / step time, summed over ranks.  The
-"roofline" object is the decode kernel alone, timed by CUDA-event nodes around
-each decode launch inside the replayed step.  "append" adds the quantize-on-
-append sweep (8 sequences x 8192 new tokens, every Hadamard block and bit
-width) in tokens/s.  "cpu_baseline" times the CPU oracle on a bounded sample.
+value = algorithmic bytes of a step / step time, summed over ranks.  Bytes per
+layer: packed codes + fp16 scale/zero of the cached tokens (136 B per (token,
+KV head) for K4V4), the new tokens' bf16 K/V read and their codes written, q
+read, o written, the page-table rows read.  The "roofline" object is the
+decode-step kernel alone, timed by CUDA-event nodes around each launch inside
+the replayed step.  "append" adds the quantize-on-append sweep (8 sequences x
+8192 new tokens, every Hadamard block and bit width) in tokens/s.
+"cpu_baseline" times the CPU oracle on a bounded sample.
 
 --impl reference times the CPU oracle itself as the reference arm (this
 library has no third-party reference implementation to install).
@@ -58,7 +60,13 @@ def unit_bytes(d: int, bk: int, bv: int) -> int:
 
 
 def decode_bytes_per_layer() -> int:
-    return W.batch * W.ctx * W.hkv * unit_bytes(W.head_dim, 4, 4)
+    """Algorithmic bytes one decode step of one layer moves (see the module docstring)."""
+    d, hkv, hq, bsz, ctx = W.head_dim, W.hkv, W.hq, W.batch, W.ctx
+    cache = bsz * ctx * hkv * unit_bytes(d, 4, 4)      # codes + (s, z) read
+    new_tok = bsz * hkv * 2 * (2 * d + d * 4 // 8 + 4)  # bf16 K, V read; codes, (s, z) written
+    q_o = bsz * hq * d * (2 + 4)                        # bf16 q read, fp32 o written
+    ptab = bsz * (ctx // 16) * 4
+    return cache + new_tok + q_o + ptab
 
 
 def peaks() -> dict:
@@ -167,7 +175,7 @@ class OracleSample:
                       np.zeros(n_seqs, np.int32))
         self.q = queries(W.seed, 0, n_seqs, W.hq, d, False).astype(np.float64)
         self.before = np.full(n_seqs, ctx - 1, np.int32)
-        self.nbytes = n_seqs * ctx * hkv * unit_bytes(d, 4, 4)
+        self.nbytes = decode_bytes_per_layer() * n_seqs // W.batch   # same byte count, pro rata
 
     def step(self) -> float:
         from oracle import attention, cache as ocache
@@ -218,7 +226,8 @@ def config_dict() -> dict:
     return {"workload": "llama3-8b-decode-layer x 32 layer caches",
             "batch": W.batch, "q_heads": W.hq, "kv_heads": W.hkv, "head_dim": W.head_dim,
             "context": W.ctx, "bits": "K4V4", "had_block": W.had_block, "page": 16,
-            "layers": N_LAYERS, "step": "per layer: append 1 token/seq + split-K decode",
+            "layers": N_LAYERS,
+            "step": "per layer: kvq_decode_step (append 1 token/seq fused with split-K decode)",
             "l2": (f"inputs larger than L2: {N_LAYERS} distinct layer caches, "
                    f"{N_LAYERS * decode_bytes_per_layer() / 1e9:.2f} GB of packed KV per step"),
             "parallelism": "replicas (weak scaling), no collective on the data path"}
@@ -267,8 +276,8 @@ def run_kvq(args) -> None:
     zero = torch.zeros(bsz, dtype=torch.int32, device=dev)
     for l in range(N_LAYERS):
         cache.append(l, kd[:, :ctx - 1].contiguous(), vd[:, :ctx - 1].contiguous(), pt, zero)
-    knew = kd[:, ctx - 1:].contiguous().unsqueeze(0).repeat(N_LAYERS, 1, 1, 1, 1).contiguous()
-    vnew = vd[:, ctx - 1:].contiguous().unsqueeze(0).repeat(N_LAYERS, 1, 1, 1, 1).contiguous()
+    knew = kd[:, ctx - 1].contiguous().unsqueeze(0).repeat(N_LAYERS, 1, 1, 1).contiguous()
+    vnew = vd[:, ctx - 1].contiguous().unsqueeze(0).repeat(N_LAYERS, 1, 1, 1).contiguous()
     del kd, vd
     q_host = np.stack([queries(W.seed, l, bsz, hq, d, False) for l in range(N_LAYERS)])
     q_all = torch.from_numpy(q_host).to(dev).to(torch.bfloat16)
@@ -285,9 +294,8 @@ def run_kvq(args) -> None:
 
     def step():
         for l in range(N_LAYERS):
-            cache.append(l, knew[l], vnew[l], pt, before)
             ev[l][0].record()
-            cache.decode(l, q_all[l], pt, after, o=o_all[l], workspace=ws)
+            cache.decode_step(l, knew[l], vnew[l], q_all[l], pt, after, o=o_all[l], workspace=ws)
             ev[l][1].record()
 
     with torch.cuda.stream(stream):
@@ -369,7 +377,8 @@ def run_kvq(args) -> None:
         "dtype": "u4 codes, fp16 MMA, fp32 accumulate", "data": "synthetic",
         "config": config_dict(),
         "frac_of_hbm": round(gbs / world / pk["hbm_gbs"], 4),
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel<128> (split-K decode + combine)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "decode_kernel<128> (decode step: append + split-K decode + merge)",
                      "achieved": round(achieved, 2), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / pk["hbm_gbs"], 4),
                      "peak_source": pk["source"], "traffic": None,
@@ -378,7 +387,7 @@ def run_kvq(args) -> None:
         "e2e": {"value": round(world * step_bytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(ms_e2e, 4)},
-        "gpu_launches": 2 * N_LAYERS * args.steps,
+        "gpu_launches": N_LAYERS * args.steps,
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
         "append": append,

@@ -89,7 +89,10 @@ typedef struct kvq_cache {
   void* const* layer_pools;  /* host array [num_layers] of device pointers, each
                                 num_pages * kvq_page_bytes(layer) bytes, 16-byte aligned */
   void* const* window_bufs;  /* host array [num_layers] of device pointers to bf16
-                                [max_batch][Hkv][2][R][head_dim], or NULL when R == 0 */
+                                [max_batch][Hkv][2][R][head_dim], or NULL when R == 0.
+                                Sequence b of a call uses row b; a call for a subset
+                                of a batch (e.g. a one-sequence prefill) passes a
+                                descriptor whose pointers are offset to its rows. */
   int* status_dev;           /* device int, the sticky status word (may be NULL) */
 } kvq_cache;
 
@@ -148,6 +151,33 @@ size_t kvq_decode_workspace_bytes(const kvq_cache* cache, int B, int Hq, int max
  * One kernel launch.  Returns KVQ_OK once enqueued.
  */
 kvq_status kvq_decode_attn(const kvq_cache* cache, int layer, const void* q, int q_is_fp32,
+                           const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                           int B, int Hq, float softmax_scale, float* o, void* workspace,
+                           size_t ws_bytes, void* stream);
+
+/*
+ * kvq_decode_step -- one decode step with the new token fused in: the same
+ * result, in the cache and in o, as kvq_append of one token per sequence
+ * followed by kvq_decode_attn, in a single launch.
+ * Follows "SAW-INT4 ..." section 3 (the fused engine: rotation and
+ * quantization of the newest token happen inside the same memory pass as the
+ * attention that reads the compact cache) and "LogQuant ..." Methodology
+ * section 2 (the newest token enters the full-precision window).
+ *
+ *   K_new, V_new device bf16 [B][Hkv][head_dim], 16-byte aligned: this step's
+ *                token of every sequence.
+ *   seq_lens     device int32 [B]: tokens per sequence INCLUDING this step's
+ *                token (>= 1; a length below 1 sets KVQ_DEV_BAD_LENGTH and
+ *                the sequence is skipped).
+ *   Every other argument as for kvq_decode_attn.
+ * Position len - 1 of sequence b takes the new token.  Without a window it is
+ * quantized into its page slot; with R > 0 it enters ring slot (len - 1) % R,
+ * and the token it replaces (position len - 1 - R, if any) is quantized into
+ * its page slot.  Two steps on one cache must be stream-ordered.  One kernel
+ * launch.  Returns KVQ_OK once enqueued.
+ */
+kvq_status kvq_decode_step(const kvq_cache* cache, int layer, const void* K_new,
+                           const void* V_new, const void* q, int q_is_fp32,
                            const int32_t* page_table, int max_pages, const int32_t* seq_lens,
                            int B, int Hq, float softmax_scale, float* o, void* workspace,
                            size_t ws_bytes, void* stream);

@@ -63,8 +63,11 @@ def new_state(num_layers: int, num_pages: int, head_dim: int, had_block: int,
 
 
 def append(state: CacheState, layer: int, k: np.ndarray, v: np.ndarray,
-           page_table: np.ndarray, seq_lens: np.ndarray) -> dict:
+           page_table: np.ndarray, seq_lens: np.ndarray, window_row: int = 0) -> dict:
     """Append k, v [B, T_new, Hkv, d] (bf16-exact float32) after seq_lens[b] tokens.
+
+    Sequence b of the call uses window row window_row + b (its page-table row is
+    page_table[b]).
 
     Mutates ``state`` and returns, for tests, a dict keyed by (b, h, kv) of
     (positions, codes, s, z, u32): the positions quantized by this call, what
@@ -90,7 +93,7 @@ def append(state: CacheState, layer: int, k: np.ndarray, v: np.ndarray,
                 bits = int(state.bits[layer, h, kv])
                 vecs = np.empty((len(pos), d), dtype=np.float32)
                 if from_ring.any():
-                    vecs[from_ring] = state.windows[layer][b, h, kv, pos[from_ring] % r]
+                    vecs[from_ring] = state.windows[layer][window_row + b, h, kv, pos[from_ring] % r]
                 if (~from_ring).any():
                     vecs[~from_ring] = src[b, pos[~from_ring] - l0, h]
                 codes, s, z, u32 = rotate_and_quantize(vecs, state.had_block, bits)
@@ -99,6 +102,6 @@ def append(state: CacheState, layer: int, k: np.ndarray, v: np.ndarray,
                 written[(b, h, kv)] = (pos, codes, s, z, u32)
         if r:
             for p in range(max(l0, q_new), l_end):
-                state.windows[layer][b, :, 0, p % r] = k[b, p - l0]
-                state.windows[layer][b, :, 1, p % r] = v[b, p - l0]
+                state.windows[layer][window_row + b, :, 0, p % r] = k[b, p - l0]
+                state.windows[layer][window_row + b, :, 1, p % r] = v[b, p - l0]
     return written

@@ -68,6 +68,8 @@ _SIGS = {
                              _P, _SZ, _P]),
     "kvq_decode_attn_static": (_I, [ctypes.POINTER(kvq_cache), _I, _P, _I, _P, _I, _P, _I, _I,
                                     _F, _P, _P]),
+    "kvq_decode_step": (_I, [ctypes.POINTER(kvq_cache), _I, _P, _P, _P, _I, _P, _I, _P, _I, _I, _F,
+                             _P, _P, _SZ, _P]),
     "kvq_alloc_bits": (_I, [_P, _P, _I, _LL, _P, _P, _P]),
     "kvq_get_status": (_I, [ctypes.POINTER(kvq_cache), ctypes.POINTER(ctypes.c_int)]),
     "kvq_reset_status": (_I, [ctypes.POINTER(kvq_cache), _P]),
@@ -154,6 +156,16 @@ def kvq_decode_attn(desc: kvq_cache, layer: int, q, q_is_fp32: bool, page_table,
                                  _ptr(page_table), max_pages, _ptr(seq_lens), B, Hq,
                                  float(softmax_scale), _ptr(o), _ptr(workspace), int(ws_bytes),
                                  _stream(stream)))
+
+
+def kvq_decode_step(desc: kvq_cache, layer: int, K_new, V_new, q, q_is_fp32: bool, page_table,
+                    max_pages: int, seq_lens, B: int, Hq: int, softmax_scale: float, o, workspace,
+                    ws_bytes: int, stream=None) -> None:
+    """Append of one token per sequence fused with the decode (seq_lens include the token)."""
+    _check(lib().kvq_decode_step(ctypes.byref(desc), layer, _ptr(K_new), _ptr(V_new), _ptr(q),
+                                 int(bool(q_is_fp32)), _ptr(page_table), max_pages,
+                                 _ptr(seq_lens), B, Hq, float(softmax_scale), _ptr(o),
+                                 _ptr(workspace), int(ws_bytes), _stream(stream)))
 
 
 STATIC_WORKSPACE_BYTES = 8 * 1024 * 1024   # KVQ_STATIC_WORKSPACE_BYTES in kvq.h
@@ -250,11 +262,28 @@ class Cache:
         self._ws = {}
 
     # -- calls ------------------------------------------------------------------------------
-    def append(self, layer: int, K, V, page_table, seq_lens, stream=None) -> None:
-        """K, V bf16 [B][T_new][Hkv][d]; page_table int32 [B][max_pages]; seq_lens int32 [B]."""
+    def append(self, layer: int, K, V, page_table, seq_lens, stream=None,
+               window_row: int = 0) -> None:
+        """K, V bf16 [B][T_new][Hkv][d]; page_table int32 [B][max_pages]; seq_lens int32 [B].
+
+        Sequence b of the call uses window row window_row + b: a call for fewer
+        sequences than the batch (a one-sequence prefill) addresses its rows
+        through a descriptor whose window pointers are offset."""
         B, T = int(K.shape[0]), int(K.shape[1])
-        kvq_append(self.desc, layer, K, V, page_table, int(page_table.shape[1]), seq_lens, B, T,
+        desc = self.desc
+        if window_row and self.windows:
+            desc = self._shifted(window_row)
+        kvq_append(desc, layer, K, V, page_table, int(page_table.shape[1]), seq_lens, B, T,
                    stream)
+
+    def _shifted(self, row: int) -> kvq_cache:
+        """A copy of the descriptor whose window buffers start at window row `row`."""
+        d = kvq_cache.from_buffer_copy(self.desc)
+        step = self.num_kv_heads * 2 * self.window * self.head_dim * 2
+        self._tmp_win = (ctypes.c_void_p * self.num_layers)(
+            *[w.data_ptr() + row * step for w in self.windows])
+        d.window_bufs = self._tmp_win
+        return d
 
     def workspace(self, B: int, Hq: int, max_pages: int):
         import torch
@@ -276,6 +305,21 @@ class Cache:
         ws = workspace if workspace is not None else self.workspace(B, Hq, max_pages)
         kvq_decode_attn(self.desc, layer, q, q.dtype == torch.float32, page_table, max_pages,
                         seq_lens, B, Hq, softmax_scale, o, ws, ws.numel(), stream)
+        return o
+
+    def decode_step(self, layer: int, K_new, V_new, q, page_table, seq_lens, o=None,
+                    softmax_scale: float = 0.0, workspace=None, stream=None):
+        """Append K_new, V_new (bf16 [B][Hkv][d]) at position seq_lens - 1 and decode.
+
+        seq_lens (int32 [B]) count the new token; returns o fp32 [B][Hq][d]."""
+        import torch
+        B, Hq = int(q.shape[0]), int(q.shape[1])
+        max_pages = int(page_table.shape[1])
+        if o is None:
+            o = torch.empty((B, Hq, self.head_dim), dtype=torch.float32, device=q.device)
+        ws = workspace if workspace is not None else self.workspace(B, Hq, max_pages)
+        kvq_decode_step(self.desc, layer, K_new, V_new, q, q.dtype == torch.float32, page_table,
+                        max_pages, seq_lens, B, Hq, softmax_scale, o, ws, ws.numel(), stream)
         return o
 
     def get_status(self) -> int:
@@ -301,6 +345,6 @@ __all__ = [
     "KVQ_EWORKSPACE", "DEV_BAD_PAGE", "DEV_BAD_LENGTH", "DEV_NONFINITE", "DEV_COPY_TIMEOUT",
     "KvqError", "KvqLibraryMissing", "kvq_cache", "lib", "kvq_version", "kvq_last_error",
     "kvq_page_bytes", "kvq_append", "kvq_decode_workspace_bytes", "kvq_decode_attn",
-    "kvq_decode_attn_static", "STATIC_WORKSPACE_BYTES",
+    "kvq_decode_attn_static", "kvq_decode_step", "STATIC_WORKSPACE_BYTES",
     "kvq_alloc_bits", "kvq_get_status", "kvq_reset_status", "mask_of", "Cache",
 ]

@@ -165,6 +165,77 @@ kvq_status set_last_error(kvq_status status, const char* message) {
 }
 }  // namespace kvq
 
+namespace {
+
+kvq_status decode_impl(const kvq_cache* cache, int layer, const void* K_new, const void* V_new,
+                       const void* q, int q_is_fp32, const int32_t* page_table, int max_pages,
+                       const int32_t* seq_lens, int B, int Hq, float softmax_scale, float* o,
+                       void* workspace, size_t ws_bytes, void* stream) {
+  kvq::DecodeParams p;
+  std::memset(&p, 0, sizeof p);
+  kvq_status st = check_cache(cache, layer, &p.geom);
+  if (st != KVQ_OK) return st;
+  if (B < 1 || max_pages < 1) return fail(KVQ_EINVAL, "B and max_pages must be >= 1");
+  if (B > 65535) return fail(KVQ_EUNSUPPORTED, "B %d above the grid limit 65535", B);
+  if (!q || !o || !page_table || !seq_lens || !workspace)
+    return fail(KVQ_EINVAL, "q, o, page_table, seq_lens and workspace must be non-NULL");
+  const bool step = K_new != nullptr || V_new != nullptr;
+  if (step && (!K_new || !V_new)) return fail(KVQ_EINVAL, "K_new and V_new must both be non-NULL");
+  if (step && (!aligned(K_new, 16) || !aligned(V_new, 16)))
+    return fail(KVQ_EINVAL, "K_new and V_new must be 16-byte aligned");
+  if (!aligned(q, 4) || !aligned(o, 4) || !aligned(page_table, 4) || !aligned(seq_lens, 4))
+    return fail(KVQ_EINVAL, "q, o, page_table and seq_lens must be 4-byte aligned");
+  if (!aligned(workspace, 16)) return fail(KVQ_EINVAL, "workspace must be 16-byte aligned");
+  const int hkv = cache->num_kv_heads;
+  if (Hq < hkv || Hq % hkv) return fail(KVQ_EINVAL, "Hq %d is not a multiple of Hkv %d", Hq, hkv);
+  const int G = Hq / hkv;
+  if (G != 1 && G != 2 && G != 4)
+    return fail(KVQ_EUNSUPPORTED, "GQA group %d not built (1, 2, 4)", G);
+  if (cache->window > 0 && B > cache->max_batch)
+    return fail(KVQ_EINVAL, "B %d exceeds the window buffers' max_batch %d", B, cache->max_batch);
+  if (!std::isfinite(softmax_scale) || softmax_scale < 0.f)
+    return fail(KVQ_EINVAL, "softmax_scale must be finite and >= 0");
+  Plan pl;
+  st = plan_decode(cache, p.geom, B, max_pages, &pl);
+  if (st != KVQ_OK) return st;
+  if (ws_bytes < pl.bytes)
+    return fail(KVQ_EWORKSPACE, "workspace of %zu bytes < %zu required", ws_bytes, pl.bytes);
+  const float scale =
+      softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cache->head_dim));
+  p.pool = static_cast<const uint8_t*>(cache->layer_pools[layer]);
+  p.window = cache->window > 0 ? static_cast<const uint16_t*>(cache->window_bufs[layer]) : nullptr;
+  p.q = q;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.o = o;
+  p.counters = static_cast<unsigned int*>(workspace);
+  p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.counter_bytes);
+  p.status = cache->status_dev;
+  p.q_fp32 = q_is_fp32 ? 1 : 0;
+  p.max_pages = max_pages;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = hkv;
+  p.G = G;
+  p.R = cache->window;
+  p.num_pages = cache->num_pages;
+  p.had_block = cache->had_block;
+  p.S = pl.S;
+  p.NS = pl.NS;
+  p.pages_per_split = pl.pages_per_split;
+  p.cluster = pl.cluster;
+  p.stage_bytes = pl.stage_bytes;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.step = step ? 1 : 0;
+  p.k_new = static_cast<const uint16_t*>(K_new);
+  p.v_new = static_cast<const uint16_t*>(V_new);
+  const cudaError_t e = kvq::launch_decode(p, cache->head_dim, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "decode launch: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t kvq_page_bytes(const kvq_cache* cache, int layer) {
@@ -235,60 +306,17 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, int layer, const void* q, int
                            const int32_t* page_table, int max_pages, const int32_t* seq_lens,
                            int B, int Hq, float softmax_scale, float* o, void* workspace,
                            size_t ws_bytes, void* stream) {
-  kvq::DecodeParams p;
-  std::memset(&p, 0, sizeof p);
-  kvq_status st = check_cache(cache, layer, &p.geom);
-  if (st != KVQ_OK) return st;
-  if (B < 1 || max_pages < 1) return fail(KVQ_EINVAL, "B and max_pages must be >= 1");
-  if (B > 65535) return fail(KVQ_EUNSUPPORTED, "B %d above the grid limit 65535", B);
-  if (!q || !o || !page_table || !seq_lens || !workspace)
-    return fail(KVQ_EINVAL, "q, o, page_table, seq_lens and workspace must be non-NULL");
-  if (!aligned(q, 4) || !aligned(o, 4) || !aligned(page_table, 4) || !aligned(seq_lens, 4))
-    return fail(KVQ_EINVAL, "q, o, page_table and seq_lens must be 4-byte aligned");
-  if (!aligned(workspace, 16)) return fail(KVQ_EINVAL, "workspace must be 16-byte aligned");
-  const int hkv = cache->num_kv_heads;
-  if (Hq < hkv || Hq % hkv) return fail(KVQ_EINVAL, "Hq %d is not a multiple of Hkv %d", Hq, hkv);
-  const int G = Hq / hkv;
-  if (G != 1 && G != 2 && G != 4)
-    return fail(KVQ_EUNSUPPORTED, "GQA group %d not built (1, 2, 4)", G);
-  if (cache->window > 0 && B > cache->max_batch)
-    return fail(KVQ_EINVAL, "B %d exceeds the window buffers' max_batch %d", B, cache->max_batch);
-  if (!std::isfinite(softmax_scale) || softmax_scale < 0.f)
-    return fail(KVQ_EINVAL, "softmax_scale must be finite and >= 0");
-  Plan pl;
-  st = plan_decode(cache, p.geom, B, max_pages, &pl);
-  if (st != KVQ_OK) return st;
-  if (ws_bytes < pl.bytes)
-    return fail(KVQ_EWORKSPACE, "workspace of %zu bytes < %zu required", ws_bytes, pl.bytes);
-  const float scale =
-      softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cache->head_dim));
-  p.pool = static_cast<const uint8_t*>(cache->layer_pools[layer]);
-  p.window = cache->window > 0 ? static_cast<const uint16_t*>(cache->window_bufs[layer]) : nullptr;
-  p.q = q;
-  p.page_table = page_table;
-  p.seq_lens = seq_lens;
-  p.o = o;
-  p.counters = static_cast<unsigned int*>(workspace);
-  p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.counter_bytes);
-  p.status = cache->status_dev;
-  p.q_fp32 = q_is_fp32 ? 1 : 0;
-  p.max_pages = max_pages;
-  p.B = B;
-  p.Hq = Hq;
-  p.Hkv = hkv;
-  p.G = G;
-  p.R = cache->window;
-  p.num_pages = cache->num_pages;
-  p.had_block = cache->had_block;
-  p.S = pl.S;
-  p.NS = pl.NS;
-  p.pages_per_split = pl.pages_per_split;
-  p.cluster = pl.cluster;
-  p.stage_bytes = pl.stage_bytes;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  const cudaError_t e = kvq::launch_decode(p, cache->head_dim, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return fail(KVQ_ECUDA, "decode launch: %s", cudaGetErrorString(e));
-  return KVQ_OK;
+  return decode_impl(cache, layer, nullptr, nullptr, q, q_is_fp32, page_table, max_pages, seq_lens,
+                     B, Hq, softmax_scale, o, workspace, ws_bytes, stream);
+}
+
+kvq_status kvq_decode_step(const kvq_cache* cache, int layer, const void* K_new, const void* V_new,
+                           const void* q, int q_is_fp32, const int32_t* page_table, int max_pages,
+                           const int32_t* seq_lens, int B, int Hq, float softmax_scale, float* o,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  if (!K_new || !V_new) return fail(KVQ_EINVAL, "K_new and V_new must be non-NULL");
+  return decode_impl(cache, layer, K_new, V_new, q, q_is_fp32, page_table, max_pages, seq_lens, B,
+                     Hq, softmax_scale, o, workspace, ws_bytes, stream);
 }
 
 kvq_status kvq_alloc_bits(const double* w, const double* beta, int n, long long budget,

@@ -16,22 +16,18 @@
 // min/max reduction takes one more shuffle; scale and zero are formed with
 // explicitly rounded operations (see the header for the exact rule); codes are
 // packed in registers and written with 16-byte stores.
-#include "kvq_device.cuh"
+#include "kvq_quant.cuh"
 
 namespace kvq {
 
 namespace {
 
-constexpr float kMagicRound = 12582912.0f;  // 1.5 * 2^23: x + magic rounds x to an integer
-
 template <int D, int NB, int BITS>
 __device__ __forceinline__ void append_warp(const AppendParams& p, int h, int kv, int chunk,
                                             int lane) {
   constexpr int E = D / 2;                 // elements per lane
-  constexpr int M = (1 << BITS) - 1;
   constexpr int LANE_BYTES = D * BITS / 16;  // packed code bytes per lane
   constexpr int NW = LANE_BYTES / 4;       // 32-bit words per lane
-  constexpr int CPW = 32 / BITS;           // codes per word
 
   const int row = lane >> 1;
   const int u = lane & 1;
@@ -85,95 +81,21 @@ __device__ __forceinline__ void append_warp(const AppendParams& p, int h, int kv
     }
   }
 
-  // ---- load this lane's half of the row (bf16 -> fp32, exact)
+  // ---- this lane's half of the row, rotated and quantized with its partner
   float v[E];
-  if (src != nullptr) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(src + u * E);
-    uint4 w[D / 16];
-#pragma unroll
-    for (int i = 0; i < D / 16; ++i) w[i] = s4[i];
-#pragma unroll
-    for (int i = 0; i < D / 16; ++i) {
-      v[8 * i + 0] = bf16lo(w[i].x); v[8 * i + 1] = bf16hi(w[i].x);
-      v[8 * i + 2] = bf16lo(w[i].y); v[8 * i + 3] = bf16hi(w[i].y);
-      v[8 * i + 4] = bf16lo(w[i].z); v[8 * i + 5] = bf16hi(w[i].z);
-      v[8 * i + 6] = bf16lo(w[i].w); v[8 * i + 7] = bf16hi(w[i].w);
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < E; ++e) v[e] = 0.f;
-  }
-
-  // ---- Sylvester butterflies, natural order: stage hs pairs (i, i + hs)
-  constexpr int IN_REG = NB < E ? NB : E;
-#pragma unroll
-  for (int e = 0; e < E; e += 2) {  // hs = 1
-    const float a = v[e], c = v[e + 1];
-    v[e] = a + c;
-    v[e + 1] = a - c;
-  }
-#pragma unroll
-  for (int hs = 2; hs < IN_REG; hs <<= 1) {
-#pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      if (!(e & hs)) addsub2(v[e], v[e + 1], v[e + hs], v[e + hs + 1]);
-    }
-  }
-  if constexpr (NB > E) {  // the block spans both lanes: lane 0 holds the lower half
-    const float sgn = u ? -1.f : 1.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const float o = __shfl_xor_sync(kFullMask, v[e], 1);
-      v[e] = __fmaf_rn(sgn, v[e], o);  // u = 0: a + b, u = 1: a - b
-    }
-  }
-
-  // ---- per-vector min / max over both lanes
-  float mn = v[0], mx = v[0];
-#pragma unroll
-  for (int e = 1; e < E; ++e) {
-    mn = fminf(mn, v[e]);
-    mx = fmaxf(mx, v[e]);
-  }
-  mn = fminf(mn, __shfl_xor_sync(kFullMask, mn, 1));
-  mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 1));
-
-  // ---- fp16 zero (round down) and scale (round up)
-  const __half zh = __float2half_rd(mn);
-  const float zf = __half2float(zh);
-  const float span = __fsub_rn(mx, zf);
-  const __half sh = __float2half_ru(__fdiv_rn(span, static_cast<float>(M)));
-  const float sf = __half2float(sh);
-  const float inv = sf > 0.f ? __frcp_rn(sf) : 0.f;
+  load_half_row<D>(src, u, v);
+  uint32_t words[NW];
+  __half sh, zh;
+  rotate_quantize_half<D, NB, BITS>(v, u, words, sh, zh);
 
   if (src != nullptr) {
-    if (u == 0 && !(isfinite(sf) && isfinite(zf))) flag_status(p.status, 0x4);
-    // ---- codes: round-half-even((u - z) * inv) via the magic-number add
-    uint32_t words[NW];
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      uint32_t acc = 0;
-#pragma unroll
-      for (int i = 0; i < CPW; ++i) {
-        const float f = __fmaf_rn(__fsub_rn(v[w * CPW + i], zf), inv, kMagicRound);
-        acc |= (__float_as_uint(f) & static_cast<uint32_t>(M)) << (BITS * i);
-      }
-      words[w] = acc;
-    }
+    if (u == 0 && !(isfinite(__half2float(sh)) && isfinite(__half2float(zh))))
+      flag_status(p.status, KVQ_DEV_NONFINITE);
     const int slot = dst % kPage;
     const int kb = D * p.geom.bits[h][0] / 8;  // K code bytes per token
     const int vb = D * p.geom.bits[h][1] / 8;
-    uint8_t* cbase = seg + (kv ? kPage * kb : 0) + slot * (D * BITS / 8) + u * LANE_BYTES;
-    if constexpr (NW % 4 == 0) {
-#pragma unroll
-      for (int i = 0; i < NW / 4; ++i)
-        reinterpret_cast<uint4*>(cbase)[i] =
-            make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]);
-    } else if constexpr (NW == 2) {
-      *reinterpret_cast<uint2*>(cbase) = make_uint2(words[0], words[1]);
-    } else {
-      *reinterpret_cast<uint32_t*>(cbase) = words[0];
-    }
+    store_code_words<NW>(seg + (kv ? kPage * kb : 0) + slot * (D * BITS / 8) + u * LANE_BYTES,
+                         words);
     if (u == 0) {
       uint8_t* sz = seg + kPage * (kb + vb) + (kv ? kPage * 4 : 0) + slot * 4;
       *reinterpret_cast<uint32_t*>(sz) = pack_half2(sh, zh);

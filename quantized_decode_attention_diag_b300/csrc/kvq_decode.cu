@@ -34,7 +34,7 @@
 // sum_t p_t deq(v_t) = sum_t (p_t s_t) c_t + sum_t p_t z_t.
 #include <math_constants.h>
 
-#include "kvq_device.cuh"
+#include "kvq_quant.cuh"
 
 namespace kvq {
 
@@ -437,11 +437,120 @@ __device__ __forceinline__ void merge_warps(const Smem& sm, int i, bool drop, fl
   }
 }
 
+// ------------------------------------------------------------ decode step --
+// This lane's part of the decode step's new token, loaded at kernel start:
+// lanes 0-15 hold K elements [F l, F l + F), lanes 16-31 the same of V
+// (F = D / 16), as packed bf16 pairs.
+template <int D>
+__device__ __forceinline__ void load_new_token(const DecodeParams& p, int b, int h,
+                                               uint32_t (&w)[D / 32]) {
+  constexpr int F = D / 16;
+  const int lane = threadIdx.x & 31;
+  const uint16_t* src = (lane < 16 ? p.k_new : p.v_new) +
+                        (static_cast<size_t>(b) * p.Hkv + h) * D + F * (lane & 15);
+#pragma unroll
+  for (int i = 0; i < F / 2; ++i) w[i] = ldg_nc_u32(src + 2 * i);
+}
+
+// Stores n = F * bits / 8 bytes (1, 2, 4 or 8; naturally aligned) of codes.
+__device__ __forceinline__ void store_codes(uint8_t* dst, const uint32_t (&c)[2], int n) {
+  if (n == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(c[0], c[1]);
+  else if (n == 4) *reinterpret_cast<uint32_t*>(dst) = c[0];
+  else if (n == 2) *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(c[0]);
+  else *dst = static_cast<uint8_t>(c[0]);
+}
+
+// Decode step, the warp that owns page pos / 16 (pos = the last quantized
+// position): quantizes the K (lanes 0-15) and V (lanes 16-31) vectors of
+// position pos -- the new token itself without a window; with one, the token
+// that leaves the ring now, whose slot then takes the new token -- and writes
+// them to the cache page (for later calls) and to `pbuf` in shared memory
+// (K codes [KB], V codes [VB], K (s, z), V (s, z)), from which this launch's
+// staged copy of the page gets patched.  Same rule and same bits as kvq_append.
+template <int D>
+__device__ void step_append(const DecodeParams& p, int b, int h, int pos, int bk, int bv,
+                            const uint32_t (&tok)[D / 32], uint8_t* pbuf) {
+  constexpr int F = D / 16;
+  const int lane = threadIdx.x & 31, half = lane >> 4, l = lane & 15;
+  const int bits = half ? bv : bk;
+  const int KB = D * bk / 8, VB = D * bv / 8;
+  const int rowb = half ? VB : KB;              // code bytes of this vector's row
+  const int nb = F * bits / 8;                  // code bytes of this lane
+  uint16_t* ring = nullptr;                     // this lane's elements of the ring slot
+  if (p.R > 0)
+    ring = const_cast<uint16_t*>(p.window) + ((static_cast<size_t>(b) * p.Hkv + h) * 2 + half) *
+                                                  p.R * D +
+           static_cast<size_t>(pos % p.R) * D + F * l;
+  float v[F];
+  if (ring) {                                   // the token leaving the ring
+#pragma unroll
+    for (int i = 0; i < F / 2; ++i) {
+      const uint32_t x = *reinterpret_cast<const uint32_t*>(ring + 2 * i);
+      v[2 * i] = bf16lo(x);
+      v[2 * i + 1] = bf16hi(x);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < F / 2; ++i) {
+      v[2 * i] = bf16lo(tok[i]);
+      v[2 * i + 1] = bf16hi(tok[i]);
+    }
+  }
+  uint32_t codes[2];
+  __half sh, zh;
+  rotate_quantize_halfwarp<D>(v, p.had_block, bits, codes, sh, zh);
+  const int pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pos / kPage);
+  uint8_t* seg = nullptr;
+  if (pid >= 0 && pid < p.num_pages) {
+    seg = const_cast<uint8_t*>(p.pool) + static_cast<size_t>(pid) * p.geom.page_bytes +
+          p.geom.head_off[h];
+  } else if (lane == 0) {
+    flag_status(p.status, KVQ_DEV_BAD_PAGE);
+  }
+  const int slot = pos % kPage;
+  store_codes(pbuf + (half ? KB : 0) + nb * l, codes, nb);
+  if (seg) store_codes(seg + (half ? kPage * KB : 0) + slot * rowb + nb * l, codes, nb);
+  if (l == 0) {
+    if (!(isfinite(__half2float(sh)) && isfinite(__half2float(zh))))
+      flag_status(p.status, KVQ_DEV_NONFINITE);
+    const uint32_t sz = pack_half2(sh, zh);
+    *reinterpret_cast<uint32_t*>(pbuf + KB + VB + 4 * half) = sz;
+    if (seg) *reinterpret_cast<uint32_t*>(seg + kPage * (KB + VB) + 4 * kPage * half + slot * 4) = sz;
+  }
+  if (ring) {                                   // the new token takes the slot
+#pragma unroll
+    for (int i = 0; i < F / 2; ++i) *reinterpret_cast<uint32_t*>(ring + 2 * i) = tok[i];
+  }
+  __syncwarp();
+}
+
+// Copies the patch (step_append's pbuf) into slot `slot` of the staged page
+// at shared-window address st, once its copy has landed.
+template <int D, int BK, int BV>
+__device__ __forceinline__ void patch_stage(uint32_t st, const uint8_t* pbuf, int slot) {
+  constexpr int KB = D * BK / 8, VB = D * BV / 8;
+  const int lane = threadIdx.x & 31;
+  const uint32_t src = smem_u32(pbuf);
+  for (int w = lane; w < (KB + VB) / 4 + 2; w += 32) {
+    uint32_t x;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x) : "r"(src + 4 * w));
+    uint32_t dst;
+    if (w < KB / 4) dst = st + slot * KB + 4 * w;
+    else if (w < (KB + VB) / 4) dst = st + kPage * KB + slot * VB + 4 * w - KB;
+    else if (w == (KB + VB) / 4) dst = st + kPage * (KB + VB) + slot * 4;
+    else dst = st + kPage * (KB + VB) + 4 * kPage + slot * 4;
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(dst), "r"(x) : "memory");
+  }
+  // these generic writes come before any later bulk copy into the stage
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+}
+
 // One split of one (sequence, KV head): pages [split * pps, (split + 1) * pps)
 // of the quantized part; warp w takes pages w, w + 4, ... two at a time.
 template <int D, int BK, int BV>
 __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h, int split,
-                            int lq, float (&qv)[D / 32], int chunk0) {
+                            int lq, float (&qv)[D / 32], int chunk0, const uint32_t (&tok)[D / 32]) {
   constexpr int KB = D * BK / 8;                 // K code bytes per token
   constexpr int VB = D * BV / 8;
   constexpr int CHUNK = kPage * (KB + VB + 8);   // one (page, head) segment
@@ -513,6 +622,19 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     const int pid = pid_of(kk);
     if (lane == 0) issue(kk, pid);
   }
+
+  // decode step: the warp owning the page of the last quantized position
+  // quantizes the token there while its first copies are in flight
+  int kpatch = -1;
+  uint8_t* pbuf = reinterpret_cast<uint8_t*>(sm.merge);
+  if (p.step && lq > 0) {
+    const int pl = npages - 1;
+    if (pl >= pg0 && pl < pg1 && (pl - pg0) % kDecodeWarps == warp) {
+      kpatch = (pl - pg0) / kDecodeWarps;
+      step_append<D>(p, b, h, lq - 1, BK, BV, tok, pbuf);
+    }
+  }
+  const int pslot = (lq - 1) % kPage;
 
   query_quant_prologue<D>(p, sm, qv);
 
@@ -657,6 +779,8 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
       timed_out = true;
       break;
     }
+    if (kpatch >= 0 && (kpatch - k) >= 0 && (kpatch - k) < RP)
+      patch_stage<D, BK, BV>(st0 + (sa + kpatch - k) * stage_bytes, pbuf, pslot);
     round(st0 + sa * stage_bytes, RP == 2, false, 0);
     // refill the round's stages with pages k + NST (, k + NST + 1)
     const int pid0 = pid_of(k + NST);
@@ -686,6 +810,8 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     if (!__all_sync(kFullMask, ok)) {
       timed_out = true;
     } else {
+      if (kpatch >= 0 && (kpatch - k) >= 0 && (kpatch - k) < (has_b ? 2 : 1))
+        patch_stage<D, BK, BV>(st0 + (sa + kpatch - k) * stage_bytes, pbuf, pslot);
       round(st0 + sa * stage_bytes, has_b, last_partial, (first + kDecodeWarps * k) * kPage);
     }
   }
@@ -732,8 +858,14 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
   const int R = p.R;
   const uint16_t* kring = p.window + ((static_cast<size_t>(b) * p.Hkv + h) * 2 + 0) * R * D;
   const uint16_t* vring = kring + static_cast<size_t>(R) * D;
+  // decode step: the newest position (len - 1) is this launch's token, read
+  // from the input (its ring slot is being rewritten by this launch)
+  const int tnew = p.step ? nw - 1 : -1;
+  const uint16_t* knew = p.step ? p.k_new + (static_cast<size_t>(b) * p.Hkv + h) * D : nullptr;
+  const uint16_t* vnew = p.step ? p.v_new + (static_cast<size_t>(b) * p.Hkv + h) * D : nullptr;
   for (int t = tid; t < nw; t += kThreads) {
-    const uint4* kr = reinterpret_cast<const uint4*>(kring + static_cast<size_t>((lq + t) % R) * D);
+    const uint4* kr = reinterpret_cast<const uint4*>(
+        t == tnew ? knew : kring + static_cast<size_t>((lq + t) % R) * D);
     float acc[kMaxGroup] = {};
     for (int i8 = 0; i8 < D / 8; ++i8) {
       const uint4 w = kr[i8];
@@ -769,10 +901,20 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
     const int i = idx / D, d = idx - i * D;
     float acc = 0.f;
     for (int t = 0; t < nw; ++t) {
-      const uint16_t raw = vring[static_cast<size_t>((lq + t) % R) * D + d];
+      const uint16_t raw = t == tnew ? vnew[d] : vring[static_cast<size_t>((lq + t) % R) * D + d];
       acc = __fmaf_rn(sc[i * R + t], __uint_as_float(static_cast<uint32_t>(raw) << 16), acc);
     }
     part_acc<D>(part, i)[d] = acc;
+  }
+  // decode step on a sequence no longer than the window: no token leaves the
+  // ring, so nobody else writes the new token into it
+  if (p.step && lq == 0 && nw > 0) {
+    uint16_t* kslot = const_cast<uint16_t*>(kring) + static_cast<size_t>((len - 1) % R) * D;
+    uint16_t* vslot = kslot + static_cast<size_t>(R) * D;
+    for (int d = tid; d < D; d += kThreads) {
+      kslot[d] = knew[d];
+      vslot[d] = vnew[d];
+    }
   }
 }
 
@@ -958,8 +1100,10 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
   float qv[D / 32];
   load_query<D>(p, b, h, qv);
   const int chunk0 = split < p.S ? load_page_chunk0(p, b, split) : 0;
+  uint32_t tok[D / 32];                 // decode step: this lane's part of the new token
+  if (p.step && split < p.S) load_new_token<D>(p, b, h, tok);
   int len = static_cast<int>(ldg_nc_u32(p.seq_lens + b));
-  if (len < 0 || len > p.max_pages * kPage) {
+  if (len < p.step || len > p.max_pages * kPage) {   // a step appends one token: len >= 1
     if (tid == 0) flag_status(p.status, KVQ_DEV_BAD_LENGTH);
     len = 0;
   }
@@ -979,15 +1123,15 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
   } else {
     const int bk = p.geom.bits[h][0], bv = p.geom.bits[h][1];
     switch (bk * 16 + bv) {
-      case 0x22: quant_split<D, 2, 2>(p, sm, b, h, split, lq, qv, chunk0); break;
-      case 0x24: quant_split<D, 2, 4>(p, sm, b, h, split, lq, qv, chunk0); break;
-      case 0x28: quant_split<D, 2, 8>(p, sm, b, h, split, lq, qv, chunk0); break;
-      case 0x42: quant_split<D, 4, 2>(p, sm, b, h, split, lq, qv, chunk0); break;
-      case 0x44: quant_split<D, 4, 4>(p, sm, b, h, split, lq, qv, chunk0); break;
-      case 0x48: quant_split<D, 4, 8>(p, sm, b, h, split, lq, qv, chunk0); break;
-      case 0x82: quant_split<D, 8, 2>(p, sm, b, h, split, lq, qv, chunk0); break;
-      case 0x84: quant_split<D, 8, 4>(p, sm, b, h, split, lq, qv, chunk0); break;
-      case 0x88: quant_split<D, 8, 8>(p, sm, b, h, split, lq, qv, chunk0); break;
+      case 0x22: quant_split<D, 2, 2>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x24: quant_split<D, 2, 4>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x28: quant_split<D, 2, 8>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x42: quant_split<D, 4, 2>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x44: quant_split<D, 4, 4>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x48: quant_split<D, 4, 8>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x82: quant_split<D, 8, 2>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x84: quant_split<D, 8, 4>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x88: quant_split<D, 8, 8>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
       default: break;
     }
     __syncthreads();   // the warps' partials are in the merge region

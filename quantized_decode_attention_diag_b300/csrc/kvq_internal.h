@@ -52,6 +52,10 @@ struct DecodeParams {
   int pages_per_split;
   int cluster;                   // 1: the NS CTAs of a unit form a cluster and merge
                                  // through distributed shared memory (NS <= 8)
+  int step;                      // 1: decode step -- the new token (k_new, v_new) is
+                                 // appended by this launch (seq_lens include it)
+  const uint16_t* k_new;         // step: bf16 [B][Hkv][D]
+  const uint16_t* v_new;
   int stage_bytes;               // bytes of one pipeline stage buffer
   float scale_log2;              // softmax_scale * log2(e)
   LayerGeom geom;

@@ -1,0 +1,192 @@
+// Rotation and quantization of one K or V head vector by a pair of lanes,
+// shared by the append kernel and the decode step (sm_103a).
+//
+// Method: "SAW-INT4: System-Aware 4-Bit KV-Cache Quantization for Real-World LLM
+// Serving" (section 2: rotate each head vector with a block-diagonal Hadamard
+// transform before quantizing it token-wise) and the RateQuant technical
+// summary, Methodology section 3 (asymmetric per-token quantization with its
+// own bit-width per head and K/V).  The exact rule (Sylvester order,
+// unnormalised transform, fp16 zero rounded down and scale rounded up, codes
+// by round-half-even of (u - z) * (1 / s) in fp32) is stated in kvq.h.
+#pragma once
+
+#include "kvq_device.cuh"
+
+namespace kvq {
+
+constexpr float kMagicRound = 12582912.0f;  // 1.5 * 2^23: x + magic rounds x to an integer
+
+// Lane u (0 or 1) of a pair loads half u of a bf16 head vector (dims
+// [u D/2, (u+1) D/2)) as exact fp32; zeros when row is null.
+template <int D>
+__device__ __forceinline__ void load_half_row(const uint16_t* row, int u, float (&v)[D / 2]) {
+  constexpr int E = D / 2;
+  if (row != nullptr) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(row + u * E);
+    uint4 w[D / 16];
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) w[i] = s4[i];
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      v[8 * i + 0] = bf16lo(w[i].x); v[8 * i + 1] = bf16hi(w[i].x);
+      v[8 * i + 2] = bf16lo(w[i].y); v[8 * i + 3] = bf16hi(w[i].y);
+      v[8 * i + 4] = bf16lo(w[i].z); v[8 * i + 5] = bf16hi(w[i].z);
+      v[8 * i + 6] = bf16lo(w[i].w); v[8 * i + 7] = bf16hi(w[i].w);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = 0.f;
+  }
+}
+
+// Rotates the vector held by the lane pair (lane ^ 1 is the partner; every
+// lane of the warp must call this) and quantizes it: this lane's packed codes
+// (half u of the row, D * BITS / 16 bytes as 32-bit words), and the pair's
+// fp16 scale and zero.
+template <int D, int NB, int BITS>
+__device__ __forceinline__ void rotate_quantize_half(float (&v)[D / 2], int u,
+                                                     uint32_t (&words)[D * BITS / 64], __half& sh,
+                                                     __half& zh) {
+  constexpr int E = D / 2;                 // elements per lane
+  constexpr int M = (1 << BITS) - 1;
+  constexpr int NW = D * BITS / 64;        // 32-bit words per lane
+  constexpr int CPW = 32 / BITS;           // codes per word
+
+  // ---- Sylvester butterflies, natural order: stage hs pairs (i, i + hs)
+  constexpr int IN_REG = NB < E ? NB : E;
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {  // hs = 1
+    const float a = v[e], c = v[e + 1];
+    v[e] = a + c;
+    v[e + 1] = a - c;
+  }
+#pragma unroll
+  for (int hs = 2; hs < IN_REG; hs <<= 1) {
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      if (!(e & hs)) addsub2(v[e], v[e + 1], v[e + hs], v[e + hs + 1]);
+    }
+  }
+  if constexpr (NB > E) {  // the block spans both lanes: lane 0 holds the lower half
+    const float sgn = u ? -1.f : 1.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float o = __shfl_xor_sync(kFullMask, v[e], 1);
+      v[e] = __fmaf_rn(sgn, v[e], o);  // u = 0: a + b, u = 1: a - b
+    }
+  }
+
+  // ---- per-vector min / max over both lanes
+  float mn = v[0], mx = v[0];
+#pragma unroll
+  for (int e = 1; e < E; ++e) {
+    mn = fminf(mn, v[e]);
+    mx = fmaxf(mx, v[e]);
+  }
+  mn = fminf(mn, __shfl_xor_sync(kFullMask, mn, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 1));
+
+  // ---- fp16 zero (round down) and scale (round up)
+  zh = __float2half_rd(mn);
+  const float zf = __half2float(zh);
+  const float span = __fsub_rn(mx, zf);
+  sh = __float2half_ru(__fdiv_rn(span, static_cast<float>(M)));
+  const float sf = __half2float(sh);
+  const float inv = sf > 0.f ? __frcp_rn(sf) : 0.f;
+
+  // ---- codes: round-half-even((u - z) * inv) via the magic-number add
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    uint32_t acc = 0;
+#pragma unroll
+    for (int i = 0; i < CPW; ++i) {
+      const float f = __fmaf_rn(__fsub_rn(v[w * CPW + i], zf), inv, kMagicRound);
+      acc |= (__float_as_uint(f) & static_cast<uint32_t>(M)) << (BITS * i);
+    }
+    words[w] = acc;
+  }
+}
+
+// Stores this lane's packed code words (NW of them) at dst (16-, 8- or
+// 4-byte aligned according to their size).
+template <int NW>
+__device__ __forceinline__ void store_code_words(uint8_t* dst, const uint32_t (&words)[NW]) {
+  if constexpr (NW % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW / 4; ++i)
+      reinterpret_cast<uint4*>(dst)[i] =
+          make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]);
+  } else if constexpr (NW == 2) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(words[0], words[1]);
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = words[0];
+  }
+}
+
+// ------------------------------------------------------------------------
+// The same rotation and quantization for two vectors at once, one per
+// half-warp (lanes 0-15: vector A with BITS_A, lanes 16-31: vector B with
+// BITS_B); lane l of a half holds the 8 (D = 128) or 4 (D = 64) consecutive
+// elements [F (l % 16), F (l % 16) + F).  Every element goes through the same
+// fp32 operations as in rotate_quantize_half (a + b and a - b stage by stage,
+// the same min / max, scale, zero and rounding), so the codes are identical;
+// only the placement across lanes differs.  Writes this lane's codes (F codes,
+// little-endian, packed into `code_bits` bits of `codes`) and the vector's
+// (s, z).  Every lane of the warp must call it; nb is the Hadamard block.
+template <int D>
+__device__ __forceinline__ void rotate_quantize_halfwarp(float (&v)[D / 16], int nb, int bits,
+                                                         uint32_t (&codes)[2], __half& sh,
+                                                         __half& zh) {
+  constexpr int F = D / 16;   // elements per lane
+  const int lane = threadIdx.x & 31;
+  // butterflies inside the lane: stages hs < F
+#pragma unroll
+  for (int hs = 1; hs < F; hs <<= 1) {
+#pragma unroll
+    for (int e = 0; e < F; ++e) {
+      if (!(e & hs) && hs < nb) {
+        const float a = v[e], c = v[e + hs];
+        v[e] = a + c;
+        v[e + hs] = a - c;
+      }
+    }
+  }
+  // across lanes: stage hs = F m pairs lanes l and l ^ m (within the half)
+  for (int m = 1; m * F < nb; m <<= 1) {
+    const float sgn = (lane & m) ? -1.f : 1.f;
+#pragma unroll
+    for (int e = 0; e < F; ++e) {
+      const float o = __shfl_xor_sync(kFullMask, v[e], m);
+      v[e] = __fmaf_rn(sgn, v[e], o);   // lower: a + b, upper: a - b
+    }
+  }
+  float mn = v[0], mx = v[0];
+#pragma unroll
+  for (int e = 1; e < F; ++e) {
+    mn = fminf(mn, v[e]);
+    mx = fmaxf(mx, v[e]);
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(kFullMask, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, o));
+  }
+  const float M = static_cast<float>((1 << bits) - 1);
+  zh = __float2half_rd(mn);
+  const float zf = __half2float(zh);
+  const float span = __fsub_rn(mx, zf);
+  sh = __float2half_ru(__fdiv_rn(span, M));
+  const float sf = __half2float(sh);
+  const float inv = sf > 0.f ? __frcp_rn(sf) : 0.f;
+  const uint32_t mask = (1u << bits) - 1u;
+  uint64_t acc = 0;
+#pragma unroll
+  for (int e = 0; e < F; ++e) {
+    const float f = __fmaf_rn(__fsub_rn(v[e], zf), inv, kMagicRound);
+    acc |= static_cast<uint64_t>(__float_as_uint(f) & mask) << (bits * e);
+  }
+  codes[0] = static_cast<uint32_t>(acc);
+  codes[1] = static_cast<uint32_t>(acc >> 32);
+}
+
+}  // namespace kvq
