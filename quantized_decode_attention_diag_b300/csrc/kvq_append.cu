@@ -8,131 +8,276 @@
 // Methodology section 3 (separate K and V widths per head), "LogQuant ...",
 // Methodology section 2 (full-precision recent window).
 //
-// Work decomposition: one warp handles 16 vectors that share (KV head, K|V) --
-// hence one bit-width -- with two lanes per vector.  Lane u of a pair loads the
-// contiguous half [u*D/2, (u+1)*D/2) of the bf16 row (16-byte loads), runs the
-// in-register butterflies of the Sylvester transform on it, and a single
-// shuffle stage joins the halves when the Hadamard block spans both.  The
-// min/max reduction takes one more shuffle; scale and zero are formed with
+// Work decomposition: a chunk is 16 vectors that share (KV head, K|V) -- hence
+// one bit-width -- quantized by one warp, two lanes per vector.  A wave of
+// warps loops over the chunks; each warp prefetches its next chunk's bf16 rows
+// into shared memory (cp.async) while it quantizes the current one.  Lane u of
+// a pair takes the half [u*D/2, (u+1)*D/2) of its row, runs the in-register
+// butterflies of the Sylvester transform on it (packed fp32 pairs), and a
+// single shuffle stage joins the halves when the Hadamard block spans both.
+// The min/max reduction takes one more shuffle; scale and zero are formed with
 // explicitly rounded operations (see the header for the exact rule); codes are
-// packed in registers and written with 16-byte stores.
+// computed on packed fp32 pairs, packed by shifted sums and written with
+// 16-byte stores.
+#include <climits>
+
 #include "kvq_quant.cuh"
 
 namespace kvq {
 
 namespace {
 
+// This lane's row of chunk c: (KV head, K|V) group and its (sequence, token),
+// b = -1 past the batch.  Computed once per chunk.
+struct RowRef {
+  int grp, b, t;
+};
+__device__ __forceinline__ RowRef row_ref(const AppendParams& p, int c) {
+  const int row = (threadIdx.x & 31) >> 1;
+  RowRef rr;
+  rr.grp = c / p.warps_per_group;
+  const int r = (c - rr.grp * p.warps_per_group) * 16 + row;
+  if (r < p.B * p.T) {
+    rr.b = r / p.T;
+    rr.t = r - rr.b * p.T;
+  } else {
+    rr.b = -1;
+    rr.t = 0;
+  }
+  return rr;
+}
+
+// Sequence length before the append (INT_MIN past the batch).
+__device__ __forceinline__ int row_len0(const AppendParams& p, const RowRef& rr) {
+  return rr.b < 0 ? INT_MIN : __ldg(p.seq_lens + rr.b);
+}
+
+// Position the row quantizes (-1: none; see append_chunk).
+__device__ __forceinline__ int row_dst(const AppendParams& p, const RowRef& rr, int l0) {
+  if (l0 == INT_MIN || l0 < 0 ||
+      static_cast<long long>(l0) + p.T > static_cast<long long>(p.max_pages) * kPage)
+    return -1;
+  const int pos = l0 + rr.t, len = l0 + p.T;
+  const int qlim = p.R ? max(0, len - p.R) : len;
+  if (pos < qlim) return pos;
+  return pos - p.R * ((pos - l0) / p.R + 1);   // the ring slot's old occupant, if >= 0
+}
+
+// Physical page of that position (-1: none).
+__device__ __forceinline__ int row_pid(const AppendParams& p, const RowRef& rr, int l0) {
+  const int dst = row_dst(p, rr, l0);
+  if (dst < 0) return -1;
+  return __ldg(p.page_table + static_cast<size_t>(rr.b) * p.max_pages + dst / kPage);
+}
+
+// Row chunk of a warp: 16 vectors (rows) of one (KV head, K|V), 16 consecutive
+// (sequence, token) pairs.  The warp's lane pair (row = lane / 2, u = lane % 2)
+// holds half u of row `row`.  Rows are prefetched into a per-warp shared-memory
+// buffer with cp.async, one chunk ahead of the one being quantized; 16-byte
+// chunk ci of row r sits at position ci ^ ((2 r + ci / (D / 16)) & 7), so that
+// the eight lanes of a 16-byte shared-memory phase hit distinct banks.
+template <int D>
+__device__ __forceinline__ int swz(int row, int ci) {
+  return ci ^ ((2 * row + ci / (D / 16)) & 7);
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
+template <int D>
+__device__ __forceinline__ void prefetch_chunk(const AppendParams& p, const RowRef& rr, uint4* buf) {
+  const int lane = threadIdx.x & 31, row = lane >> 1, u = lane & 1;
+  if (rr.b >= 0) {
+    const int h = rr.grp >> 1, kv = rr.grp & 1;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        (kv ? p.V : p.K) + ((static_cast<size_t>(rr.b) * p.T + rr.t) * p.Hkv + h) * D);
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      const int ci = u * (D / 16) + i;
+      cp_async16(buf + row * (D / 8) + swz<D>(row, ci), src + ci);
+    }
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void half_row_from_smem(const uint4* buf, int row, int u,
+                                                   float (&v)[D / 2]) {
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) {
+    const uint4 w = buf[row * (D / 8) + swz<D>(row, u * (D / 16) + i)];
+    v[8 * i + 0] = bf16lo(w.x); v[8 * i + 1] = bf16hi(w.x);
+    v[8 * i + 2] = bf16lo(w.y); v[8 * i + 3] = bf16hi(w.y);
+    v[8 * i + 4] = bf16lo(w.z); v[8 * i + 5] = bf16hi(w.z);
+    v[8 * i + 6] = bf16lo(w.w); v[8 * i + 7] = bf16hi(w.w);
+  }
+}
+
+// Quantize-on-append of chunk c whose input rows are in `buf`.
 template <int D, int NB, int BITS>
-__device__ __forceinline__ void append_warp(const AppendParams& p, int h, int kv, int chunk,
-                                            int lane) {
+__device__ __forceinline__ void append_chunk(const AppendParams& p, const RowRef& rr,
+                                             const uint4* buf, int l0, int pid) {
   constexpr int E = D / 2;                 // elements per lane
   constexpr int LANE_BYTES = D * BITS / 16;  // packed code bytes per lane
   constexpr int NW = LANE_BYTES / 4;       // 32-bit words per lane
-
-  const int row = lane >> 1;
-  const int u = lane & 1;
-  const int r = chunk * 16 + row;
-  bool active = r < p.B * p.T;
-  int b = 0, t = 0, l0 = 0;
-  if (active) {
-    b = r / p.T;
-    t = r - b * p.T;
-    l0 = __ldg(p.seq_lens + b);
-    if (l0 < 0 || static_cast<long long>(l0) + p.T > static_cast<long long>(p.max_pages) * kPage) {
-      if (u == 0) flag_status(p.status, 0x2);
-      active = false;
-    }
+  const int lane = threadIdx.x & 31, row = lane >> 1, u = lane & 1;
+  const int h = rr.grp >> 1, kv = rr.grp & 1;
+  const int b = rr.b < 0 ? 0 : rr.b, t = rr.t;
+  bool active = rr.b >= 0;
+  if (active &&
+      (l0 < 0 || static_cast<long long>(l0) + p.T > static_cast<long long>(p.max_pages) * kPage)) {
+    if (u == 0) flag_status(p.status, KVQ_DEV_BAD_LENGTH);
+    active = false;
   }
+  if (!active) l0 = 0;
   const int pos = l0 + t;
   const int len = l0 + p.T;
   const int qlim = p.R ? max(0, len - p.R) : len;
 
-  const uint16_t* in_row =
-      (kv ? p.V : p.K) + (static_cast<size_t>(b) * p.T + t) * p.Hkv * D + static_cast<size_t>(h) * D;
-  const uint16_t* src = nullptr;
+  // where the quantized vector comes from (the input row in smem, or the ring
+  // slot it leaves) and which position it fills; ring slot the input enters
+  const uint16_t* from_ring = nullptr;
   uint16_t* ring_slot = nullptr;
   int dst = -1;
   if (active) {
     if (pos < qlim) {
-      src = in_row;  // never enters the window
+      // never enters the window: quantized straight from the input row
       dst = pos;
     } else {
       // enters the ring; the slot's previous occupant (the position of the old
       // window congruent to pos mod R) leaves the window now
-      ring_slot = p.window +
-                  ((static_cast<size_t>(b) * p.Hkv + h) * 2 + kv) * p.R * D +
+      ring_slot = p.window + ((static_cast<size_t>(b) * p.Hkv + h) * 2 + kv) * p.R * D +
                   static_cast<size_t>(pos % p.R) * D;
       const int pold = pos - p.R * ((pos - l0) / p.R + 1);
       if (pold >= 0) {
-        src = ring_slot;
+        from_ring = ring_slot;
         dst = pold;
       }
     }
   }
   uint8_t* seg = nullptr;
   if (dst >= 0) {
-    const int pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + dst / kPage);
     if (pid < 0 || pid >= p.num_pages) {
-      if (u == 0) flag_status(p.status, 0x1);
-      src = nullptr;
+      if (u == 0) flag_status(p.status, KVQ_DEV_BAD_PAGE);
+      from_ring = nullptr;
       dst = -1;
     } else {
       seg = p.pool + static_cast<size_t>(pid) * p.geom.page_bytes + p.geom.head_off[h];
     }
   }
 
-  // ---- this lane's half of the row, rotated and quantized with its partner
+  // ---- this lane's half of the row, rotated and quantized with its partner;
+  //      rows past the batch quantize whatever the buffer holds, unused
   float v[E];
-  load_half_row<D>(src, u, v);
+  if (from_ring == nullptr) {
+    half_row_from_smem<D>(buf, row, u, v);
+  } else {
+    load_half_row<D>(from_ring, u, v);   // only with a window
+  }
   uint32_t words[NW];
   __half sh, zh;
   rotate_quantize_half<D, NB, BITS>(v, u, words, sh, zh);
 
-  if (src != nullptr) {
-    if (u == 0 && !(isfinite(__half2float(sh)) && isfinite(__half2float(zh))))
-      flag_status(p.status, KVQ_DEV_NONFINITE);
+  if (dst >= 0) {
     const int slot = dst % kPage;
     const int kb = D * p.geom.bits[h][0] / 8;  // K code bytes per token
     const int vb = D * p.geom.bits[h][1] / 8;
     store_code_words<NW>(seg + (kv ? kPage * kb : 0) + slot * (D * BITS / 8) + u * LANE_BYTES,
                          words);
-    if (u == 0) {
-      uint8_t* sz = seg + kPage * (kb + vb) + (kv ? kPage * 4 : 0) + slot * 4;
-      *reinterpret_cast<uint32_t*>(sz) = pack_half2(sh, zh);
-    }
+    uint32_t* sz = reinterpret_cast<uint32_t*>(seg + kPage * (kb + vb) + (kv ? kPage * 4 : 0) +
+                                               slot * 4);
+    const uint32_t szv = pack_half2(sh, zh);
+    if (u == 0) *sz = szv;
+    if (!(isfinite(__half2float(sh)) && isfinite(__half2float(zh))) && u == 0)
+      flag_status(p.status, KVQ_DEV_NONFINITE);
   }
 
   // ---- copy the new token into its ring slot (after the old one was read)
   if (ring_slot != nullptr) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(in_row + u * E);
-    uint4* d4 = reinterpret_cast<uint4*>(ring_slot + u * E);
+    uint4* d4 = reinterpret_cast<uint4*>(ring_slot) + u * (D / 16);
 #pragma unroll
-    for (int i = 0; i < D / 16; ++i) d4[i] = s4[i];
+    for (int i = 0; i < D / 16; ++i) d4[i] = buf[row * (D / 8) + swz<D>(row, u * (D / 16) + i)];
   }
 }
 
 template <int D, int NB>
-__global__ void __launch_bounds__(kAppendWarps * 32)
+__global__ void __launch_bounds__(kAppendWarps * 32, 2)
     append_kernel(const __grid_constant__ AppendParams p) {
-  const int warp = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  const int grp = warp / p.warps_per_group;
-  if (grp >= 2 * p.Hkv) return;  // whole warp
-  const int chunk = warp - grp * p.warps_per_group;
-  const int h = grp >> 1, kv = grp & 1;
-  switch (p.geom.bits[h][kv]) {  // warp-uniform
-    case 2: append_warp<D, NB, 2>(p, h, kv, chunk, lane); break;
-    case 4: append_warp<D, NB, 4>(p, h, kv, chunk, lane); break;
-    case 8: append_warp<D, NB, 8>(p, h, kv, chunk, lane); break;
-    default: break;
+  extern __shared__ uint4 abuf[];           // [warps][2][16 rows][D / 8] 16-byte chunks
+  const int warp = threadIdx.x >> 5;
+  const int total = 2 * p.Hkv * p.warps_per_group;
+  const int stride = gridDim.x * kAppendWarps;
+  uint4* mine = abuf + warp * 2 * 16 * (D / 8);
+  int c = blockIdx.x * kAppendWarps + warp;
+  // metadata pipeline: lengths two chunks ahead, page ids one chunk ahead
+  RowRef rc = row_ref(p, c < total ? c : 0);
+  RowRef rn = row_ref(p, c + stride < total ? c + stride : 0);
+  int l0_c = c < total ? row_len0(p, rc) : INT_MIN;
+  int l0_n = c + stride < total ? row_len0(p, rn) : INT_MIN;
+  int pid_c = c < total ? row_pid(p, rc, l0_c) : -1;
+  if (c < total) prefetch_chunk<D>(p, rc, mine);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  for (int it = 0; c < total; c += stride, ++it) {
+    const int cn = c + stride, cnn = cn + stride;
+    const RowRef rnn = row_ref(p, cnn < total ? cnn : 0);
+    int pid_n = -1, l0_nn = INT_MIN;
+    if (cn < total) {
+      prefetch_chunk<D>(p, rn, mine + ((it + 1) & 1) * 16 * (D / 8));
+      pid_n = row_pid(p, rn, l0_n);
+    }
+    if (cnn < total) l0_nn = row_len0(p, rnn);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    __syncwarp();
+    const uint4* buf = mine + (it & 1) * 16 * (D / 8);
+    switch (p.geom.bits[rc.grp >> 1][rc.grp & 1]) {  // warp-uniform
+      case 2: append_chunk<D, NB, 2>(p, rc, buf, l0_c, pid_c); break;
+      case 4: append_chunk<D, NB, 4>(p, rc, buf, l0_c, pid_c); break;
+      case 8: append_chunk<D, NB, 8>(p, rc, buf, l0_c, pid_c); break;
+      default: break;
+    }
+    __syncwarp();
+    rc = rn;
+    rn = rnn;
+    l0_c = l0_n;
+    pid_c = pid_n;
+    l0_n = l0_nn;
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+int sm_count_cached() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
 }
 
 template <int D, int NB>
 cudaError_t launch(const AppendParams& p, cudaStream_t s) {
-  const long long warps = 2ll * p.Hkv * p.warps_per_group;
+  constexpr size_t smem = static_cast<size_t>(kAppendWarps) * 2 * 16 * D * 2;
+  static int attr_set[64] = {0};   // per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(append_kernel<D, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = 1;
+  }
+  const long long chunks = 2ll * p.Hkv * p.warps_per_group;
+  // one resident wave of warps (two CTAs per SM), each looping over its chunks
+  const long long wave = 2ll * kAppendWarps * sm_count_cached();
+  const long long warps = chunks < wave ? chunks : wave;
   const unsigned blocks = static_cast<unsigned>((warps + kAppendWarps - 1) / kAppendWarps);
-  append_kernel<D, NB><<<blocks, kAppendWarps * 32, 0, s>>>(p);
+  append_kernel<D, NB><<<blocks, kAppendWarps * 32, smem, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -46,6 +46,22 @@ __device__ __forceinline__ void addsub2(float& a0, float& a1, float& b0, float& 
   a0 = s0; a1 = s1; b0 = d0; b1 = d1;
 }
 
+// f = fma(x - z, inv, c) on a pair of fp32 values, round-to-nearest per
+// element (packed f32x2, sm_100+); returns the raw bits of both results.
+__device__ __forceinline__ void subfma2(float x0, float x1, float z, float inv, float c,
+                                        uint32_t& r0, uint32_t& r1) {
+  asm("{\n\t.reg .b64 rx, rz, rd, ri, rc, rr;\n\t"
+      "mov.b64 rx, {%2, %3};\n\t"
+      "mov.b64 rz, {%4, %4};\n\t"
+      "mov.b64 ri, {%5, %5};\n\t"
+      "mov.b64 rc, {%6, %6};\n\t"
+      "sub.rn.f32x2 rd, rx, rz;\n\t"
+      "fma.rn.f32x2 rr, rd, ri, rc;\n\t"
+      "mov.b64 {%0, %1}, rr;\n\t}"
+      : "=r"(r0), "=r"(r1)
+      : "f"(x0), "f"(x1), "f"(z), "f"(inv), "f"(c));
+}
+
 // ------------------------------------------------------ mbarrier + bulk ----
 __device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

@@ -76,15 +76,30 @@ __device__ __forceinline__ void rotate_quantize_half(float (&v)[D / 2], int u,
     }
   }
 
-  // ---- per-vector min / max over both lanes
-  float mn = v[0], mx = v[0];
+  // ---- per-vector min / max over both lanes (eight independent chains: min
+  //      and max are exact, so the order does not matter)
+  constexpr int RK = E >= 8 ? 8 : E;
+  float mnk[RK], mxk[RK];
 #pragma unroll
-  for (int e = 1; e < E; ++e) {
-    mn = fminf(mn, v[e]);
-    mx = fmaxf(mx, v[e]);
+  for (int j = 0; j < RK; ++j) mnk[j] = mxk[j] = v[j];
+#pragma unroll
+  for (int e = RK; e < E; e += RK) {
+#pragma unroll
+    for (int j = 0; j < RK; ++j) {
+      mnk[j] = fminf(mnk[j], v[e + j]);
+      mxk[j] = fmaxf(mxk[j], v[e + j]);
+    }
   }
-  mn = fminf(mn, __shfl_xor_sync(kFullMask, mn, 1));
-  mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 1));
+#pragma unroll
+  for (int w = RK / 2; w > 0; w >>= 1) {
+#pragma unroll
+    for (int j = 0; j < w; ++j) {
+      mnk[j] = fminf(mnk[j], mnk[j + w]);
+      mxk[j] = fmaxf(mxk[j], mxk[j + w]);
+    }
+  }
+  float mn = fminf(mnk[0], __shfl_xor_sync(kFullMask, mnk[0], 1));
+  float mx = fmaxf(mxk[0], __shfl_xor_sync(kFullMask, mxk[0], 1));
 
   // ---- fp16 zero (round down) and scale (round up)
   zh = __float2half_rd(mn);
@@ -94,17 +109,25 @@ __device__ __forceinline__ void rotate_quantize_half(float (&v)[D / 2], int u,
   const float sf = __half2float(sh);
   const float inv = sf > 0.f ? __frcp_rn(sf) : 0.f;
 
-  // ---- codes: round-half-even((u - z) * inv) via the magic-number add
+  // ---- codes: round-half-even((u - z) * inv) via the magic-number add; the
+  //      result's bits are 0x4B400000 + code, so the packed word is the sum of
+  //      the bit patterns shifted into place minus the shifted constants
+  constexpr uint32_t kMagicBits = 0x4B400000u;
+  uint32_t ksum = 0;
+#pragma unroll
+  for (int i = 0; i < CPW; ++i) ksum += kMagicBits << (BITS * i);
 #pragma unroll
   for (int w = 0; w < NW; ++w) {
-    uint32_t acc = 0;
+    uint32_t acc = 0u - ksum;
 #pragma unroll
-    for (int i = 0; i < CPW; ++i) {
-      const float f = __fmaf_rn(__fsub_rn(v[w * CPW + i], zf), inv, kMagicRound);
-      acc |= (__float_as_uint(f) & static_cast<uint32_t>(M)) << (BITS * i);
+    for (int i = 0; i < CPW; i += 2) {
+      uint32_t f0, f1;
+      subfma2(v[w * CPW + i], v[w * CPW + i + 1], zf, inv, kMagicRound, f0, f1);
+      acc += (f0 << (BITS * i)) + (f1 << (BITS * (i + 1)));
     }
     words[w] = acc;
   }
+  (void)M;
 }
 
 // Stores this lane's packed code words (NW of them) at dst (16-, 8- or
