@@ -13,10 +13,11 @@
 // covers the bf16 window.  Each CTA merges its warps into one online-softmax
 // partial (m, l, rotated acc[d] per query head).  Merge of the NS partials of a
 // (b, h):
-//   - cluster mode (NS <= 8): the NS CTAs form a thread-block cluster; after a
-//     cluster barrier, CTA 0 reads every partial straight from the others'
-//     shared memory (distributed shared memory), un-rotates and writes o -- no
-//     global partials, fences or atomics;
+//   - cluster mode (NS <= 4): the NS CTAs form a thread-block cluster; each
+//     CTA stores its partial straight into CTA 0's shared memory (distributed
+//     shared memory), arrives on the cluster barrier and exits; CTA 0 waits on
+//     the barrier, merges, un-rotates and writes o -- no global partials,
+//     fences or atomics;
 //   - ticket mode: partials go to global memory and the last CTA of (b, h) to
 //     finish (an atomic ticket, no waiting) merges them.
 //
@@ -42,7 +43,7 @@ namespace {
 
 constexpr int kThreads = kDecodeWarps * 32;
 constexpr int kMaxSplits = 256;
-constexpr int kMaxCluster = 8;    // portable cluster size
+constexpr int kMaxCluster = 4;    // largest cluster the merge uses (CTA 0 holds its partials)
 
 struct Smem {
   float* qtab;        // [kMaxGroup][D]   rotated query fragments (or raw query for the window)
@@ -61,7 +62,7 @@ __host__ __device__ constexpr int merge_floats() { return kDecodeWarps * kMaxGro
 
 __host__ __device__ constexpr int header_bytes(int d) {
   return ((d * kMaxGroup * 4 + 64 + kDecodeWarps * kDecodeStages * 8 +
-           (kDecodeWarps + 1) * kMaxGroup * (d + 2) * 4) + 127) / 128 * 128 + 128;
+           (kDecodeWarps + 1 + kMaxCluster) * kMaxGroup * (d + 2) * 4) + 127) / 128 * 128 + 128;
 }
 
 template <int D>
@@ -76,10 +77,16 @@ __device__ __forceinline__ Smem carve(uint8_t* base) {
   s.bars = reinterpret_cast<uint64_t*>(misc + 64);
   s.merge = reinterpret_cast<float*>(misc + 64 + kDecodeWarps * kDecodeStages * 8);
   s.cpart = s.merge + merge_floats<D>();
-  uint8_t* a = reinterpret_cast<uint8_t*>(s.cpart + kMaxGroup * (D + 2));
+  // then rbuf [kMaxCluster][kMaxGroup * (D + 2)] (cluster mode, CTA 0: every
+  // CTA's partial, pushed there through distributed shared memory; see rbuf())
+  uint8_t* a = reinterpret_cast<uint8_t*>(s.cpart + (1 + kMaxCluster) * kMaxGroup * (D + 2));
   s.area = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(a) + 127) & ~uintptr_t(127));
   return s;
 }
+
+// Cluster receive buffer (right after cpart).
+template <int D>
+__device__ __forceinline__ float* rbuf(const Smem& sm) { return sm.cpart + kMaxGroup * (D + 2); }
 
 // A partial: acc [kMaxGroup][D] (fp32), then m [kMaxGroup] (log2 units) and
 // l [kMaxGroup]; kMaxGroup * (D + 2) floats, rows 16-byte aligned.
@@ -998,10 +1005,6 @@ __device__ void combine_global(const DecodeParams& p, int b, int h, const float*
 }
 
 // ---------------------------------------------------------- cluster merge --
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -1013,50 +1016,25 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank)
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float ld_dsmem(uint32_t a) {
-  float x;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(x) : "r"(a));
-  return x;
-}
-template <int E>
-__device__ __forceinline__ void ld_dsmem_vec(uint32_t a, float (&v)[E]) {
-  if constexpr (E == 4) {
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(a));
-  } else {
-    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v[0]), "=f"(v[1]) : "r"(a));
-  }
-}
-
-// Cluster mode (called by CTA 0 of the cluster, after a cluster barrier).
-// Warp i merges query head i of (b, h) over the NS partials held in the
-// cluster's shared memory (cpart of CTA rank s is split s), as combine_global.
+// Cluster mode, CTA 0 after the cluster barrier: warp i merges query head i
+// of (b, h) over the NS partials in rbuf (partial s from CTA rank s), as
+// combine_global.
 template <int D>
 __device__ void combine_cluster(const DecodeParams& p, const Smem& sm, int b, int h) {
   constexpr int E = D / 32;
+  constexpr int PS = kMaxGroup * (D + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= p.G) return;
   const int i = warp, NS = p.NS, nq = p.S;
-  const float* mine = sm.cpart;
-  // lane s < NS: m and l of split s
+  const float* rb = rbuf<D>(sm);
   float ms = -CUDART_INF_F, ls = 0.f;
   if (lane < NS) {
-    ms = ld_dsmem(dsmem_addr(part_m<D>(mine) + i, lane));
-    ls = ld_dsmem(dsmem_addr(part_l<D>(mine) + i, lane));
+    ms = part_m<D>(rb + lane * PS)[i];
+    ls = part_l<D>(rb + lane * PS)[i];
   }
   const float mm = warp_max(ms);
   const float w = ms == -CUDART_INF_F ? 0.f : exp2f(ms - mm);
   const float ll = warp_sum(w * ls);
-  float rows[kMaxCluster][E];
-#pragma unroll
-  for (int s = 0; s < kMaxCluster; ++s) {
-    if (s < NS) {
-      ld_dsmem_vec<E>(dsmem_addr(part_acc<D>(mine, i) + E * lane, s), rows[s]);
-    } else {
-#pragma unroll
-      for (int e = 0; e < E; ++e) rows[s][e] = 0.f;
-    }
-  }
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
@@ -1064,8 +1042,9 @@ __device__ void combine_cluster(const DecodeParams& p, const Smem& sm, int b, in
   for (int s = 0; s < kMaxCluster; ++s) {
     const float ws = __shfl_sync(kFullMask, w, s);
     if (s < nq) {
+      const float* row = part_acc<D>(rb + s * PS, i) + E * lane;
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(ws, rows[s][e], acc[e]);
+      for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(ws, row[e], acc[e]);
     }
   }
   warp_fwht<E>(acc, p.had_block);
@@ -1074,16 +1053,28 @@ __device__ void combine_cluster(const DecodeParams& p, const Smem& sm, int b, in
   for (int e = 0; e < E; ++e) acc[e] *= inv_nb;
   if (NS > nq) {
     const float ws = __shfl_sync(kFullMask, w, nq);
+    const float* row = part_acc<D>(rb + nq * PS, i) + E * lane;
 #pragma unroll
-    for (int s = 0; s < kMaxCluster; ++s)
-      if (s == nq) {
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(ws, rows[s][e], acc[e]);
-      }
+    for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(ws, row[e], acc[e]);
   }
   float* o = p.o + (static_cast<size_t>(b) * p.Hq + h * p.G + i) * D + E * lane;
 #pragma unroll
   for (int e = 0; e < E; ++e) o[e] = ll > 0.f ? acc[e] / ll : 0.f;
+}
+
+// Stores this CTA's partial (cpart) into slot `rank` of CTA 0's rbuf.
+template <int D>
+__device__ __forceinline__ void push_partial(const Smem& sm, uint32_t rank) {
+  constexpr int PS = kMaxGroup * (D + 2);
+  static_assert(PS % 4 == 0, "partials move as float4");
+  const uint32_t dst = dsmem_addr(rbuf<D>(sm) + rank * PS, 0);
+  const float4* src = reinterpret_cast<const float4*>(sm.cpart);
+  for (int k = threadIdx.x; k < PS / 4; k += kThreads) {
+    const float4 x = src[k];
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16 * k),
+                 "f"(x.x), "f"(x.y), "f"(x.z), "f"(x.w)
+                 : "memory");
+  }
 }
 
 // -------------------------------------------------------------- the kernel --
@@ -1140,9 +1131,12 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
   __syncthreads();     // this CTA's partial is complete in sm.cpart
 
   if (p.cluster) {
-    cluster_sync();    // every partial of (b, h) is complete in its CTA
-    if (cluster_rank() == 0) combine_cluster<D>(p, sm, b, h);
-    cluster_sync();    // no CTA leaves while its partial may still be read
+    const uint32_t rank = cluster_rank();
+    push_partial<D>(sm, rank);
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    if (rank != 0) return;     // nothing reads this CTA's shared memory
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    combine_cluster<D>(p, sm, b, h);
     return;
   }
   // ticket mode: partial to global memory; the last CTA of (b, h) merges
