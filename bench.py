@@ -78,6 +78,24 @@ def peaks() -> dict:
     return {"hbm_gbs": 6400.0, "source": "fallback"}
 
 
+def ncu_traffic() -> "int | None":
+    """DRAM bytes (read + write) of one decode-step launch from the committed ncu
+    capture (profiles/traffic.json), or None once the kernel sources changed."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get("decode_kernel<128> llama3-8b-decode-layer step")
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for name in rec["sources"]:
+        with open(os.path.join(ROOT, "quantized_decode_attention_diag_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return int(rec["per_launch_bytes"]) if h.hexdigest()[:16] == rec["source_sha256_16"] else None
+
+
 # ------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -381,7 +399,7 @@ def run_kvq(args) -> None:
                      "kernel": "decode_kernel<128> (decode step: append + split-K decode + merge)",
                      "achieved": round(achieved, 2), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / pk["hbm_gbs"], 4),
-                     "peak_source": pk["source"], "traffic": None,
+                     "peak_source": pk["source"], "traffic": ncu_traffic(),
                      "algorithmic_bytes_per_launch": decode_bytes_per_layer(),
                      "avg_launch_us": round(dec_avg * 1e3, 3)},
         "e2e": {"value": round(world * step_bytes / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
