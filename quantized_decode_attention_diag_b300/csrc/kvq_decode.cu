@@ -44,6 +44,8 @@ namespace {
 constexpr int kThreads = kDecodeWarps * 32;
 constexpr int kMaxSplits = 256;
 constexpr int kMaxCluster = 4;    // largest cluster the merge uses (CTA 0 holds its partials)
+constexpr float kMaxSlack = 8.f;  // p <= 2^kMaxSlack under the lazy running maximum
+constexpr float kMaxPS = 16384.f; // largest p s taken into an fp16 (hi, lo) pair
 
 struct Smem {
   float* qtab;        // [kMaxGroup][D]   rotated query fragments (or raw query for the window)
@@ -694,13 +696,11 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     sc0 = __fmaf_rn(k0.x, a[0] + a[1], k0.y * qs);
     sc1 = __fmaf_rn(k1.x, a[2] + a[3], k1.y * qs);
   };
-  // p -> B fragments of the V-side MMA (via two 8x8 transposes); l, zacc.
+  // p s -> B fragments of the V-side MMA (via two 8x8 transposes); l, zacc.
   // With `guard`, a token with p = 0 (masked) contributes nothing even if its
   // slot holds a non-finite scale or zero.
-  auto pfrag = [&](uint32_t st, float p0, float p1, bool guard, uint32_t& pb0, uint32_t& pb1) {
-    const float2 v0 = lds_half2(st + VSZ + 4 * g);
-    const float2 v1 = lds_half2(st + VSZ + 4 * g + 32);
-    float ps0 = p0 * v0.x, ps1 = p1 * v1.x;
+  auto pfrag = [&](float p0, float p1, float ps0, float ps1, float2 v0, float2 v1, bool guard,
+                   uint32_t& pb0, uint32_t& pb1) {
     float z0 = v0.y, z1 = v1.y;
     if (guard) {
       if (!(p0 > 0.f)) { ps0 = 0.f; z0 = 0.f; }
@@ -728,6 +728,12 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
       mma_16816(oacc[j], x, pb0, pb1);
     }
   };
+  // Lazy running maximum (log2 units): m is raised only when a score exceeds
+  // it by more than kMaxSlack, so p = 2^(score - m) <= 2^kMaxSlack; any m
+  // gives the same o = acc / l once acc, l and zacc are rescaled with it.
+  // thr = m + kMaxSlack in scaled units.
+  const float slack = kMaxSlack / iscl;
+  float thr = -CUDART_INF_F;
   // raise the running maximum of head c to cover m_loc (scaled units)
   auto rescale = [&](float m_loc) {
     const float mnew = fmaxf(m_s, warp_max_group(m_loc));
@@ -742,6 +748,7 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     if (grow) {
       m_s = mnew;
       mneg = -mnew * iscl;
+      thr = mnew + slack;
     }
   };
   // one round: pages A (stage at sta) and, if has_b, B (the next stage); mask
@@ -759,12 +766,34 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
       if (tok_b + g + 8 >= lq) sb1 = -CUDART_INF_F;
     }
     const float m_loc = fmaxf(fmaxf(sa0, sa1), fmaxf(sb0, sb1));
-    if (__any_sync(kFullMask, m_loc > m_s)) rescale(m_loc);
+    if (__any_sync(kFullMask, m_loc > thr)) rescale(m_loc);
+    const float2 va0 = lds_half2(sta + VSZ + 4 * g), va1 = lds_half2(sta + VSZ + 4 * g + 32);
+    float2 vb0 = make_float2(0.f, 0.f), vb1 = vb0;
+    if (has_b) {
+      vb0 = lds_half2(stb + VSZ + 4 * g);
+      vb1 = lds_half2(stb + VSZ + 4 * g + 32);
+    }
+    float p[4], ps[4];
+    auto probs = [&]() {
+      p[0] = ex2(__fmaf_rn(sa0, iscl, mneg));
+      p[1] = ex2(__fmaf_rn(sa1, iscl, mneg));
+      p[2] = ex2(__fmaf_rn(sb0, iscl, mneg));
+      p[3] = ex2(__fmaf_rn(sb1, iscl, mneg));
+      ps[0] = p[0] * va0.x;
+      ps[1] = p[1] * va1.x;
+      ps[2] = p[2] * vb0.x;
+      ps[3] = p[3] * vb1.x;
+    };
+    probs();
+    // p s must fit fp16: a very large value scale takes the exact maximum
+    // (p <= 1, p s <= s) for this round
+    if (__any_sync(kFullMask, fmaxf(fmaxf(ps[0], ps[1]), fmaxf(ps[2], ps[3])) > kMaxPS)) {
+      rescale(m_loc);
+      probs();
+    }
     uint32_t pa0, pa1, pb0, pb1;
-    pfrag(sta, ex2(__fmaf_rn(sa0, iscl, mneg)), ex2(__fmaf_rn(sa1, iscl, mneg)), mask, pa0, pa1);
-    if (has_b)
-      pfrag(stb, ex2(__fmaf_rn(sb0, iscl, mneg)), ex2(__fmaf_rn(sb1, iscl, mneg)), mask, pb0,
-            pb1);
+    pfrag(p[0], p[1], ps[0], ps[1], va0, va1, mask, pa0, pa1);
+    if (has_b) pfrag(p[2], p[3], ps[2], ps[3], vb0, vb1, mask, pb0, pb1);
     pv(sta, pa0, pa1);
     if (has_b) pv(stb, pb0, pb1);
   };
@@ -772,7 +801,9 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   // the last page of the sequence is partial unless lq is a multiple of 16
   const bool last_partial = (lq % kPage) != 0 && nk > 0 &&
                             first + kDecodeWarps * (nk - 1) == npages - 1;
-  const int nfull = nk - (last_partial ? 1 : 0);
+  // the main loop covers full pages without the new token (kpatch, when set,
+  // is this warp's last page); the final round takes the rest
+  const int nfull = nk - ((last_partial || kpatch >= 0) ? 1 : 0);
 
   bool timed_out = false;
   int k = 0, sa = 0;
@@ -786,8 +817,6 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
       timed_out = true;
       break;
     }
-    if (kpatch >= 0 && (kpatch - k) >= 0 && (kpatch - k) < RP)
-      patch_stage<D, BK, BV>(st0 + (sa + kpatch - k) * stage_bytes, pbuf, pslot);
     round(st0 + sa * stage_bytes, RP == 2, false, 0);
     // refill the round's stages with pages k + NST (, k + NST + 1)
     const int pid0 = pid_of(k + NST);

@@ -229,3 +229,44 @@ def test_bad_page_id_sets_status_and_skips():
     pr.gpu.reset_status()
     torch.cuda.synchronize()
     assert pr.gpu.get_status() == 0
+
+
+# ------------------------------------------------------- running maximum of the softmax
+
+def test_decode_rising_scores():
+    """Scores that climb across the sequence: the running maximum is raised in
+    many steps and lags the scores in between (p > 1 within the slack)."""
+    hkv, d, g, bsz, t = 2, 128, 4, 2, 700
+    pr = Pair(hkv, d, 128, (4, 4), bsz * 48, max_batch=bsz)
+    pt = page_table(131, bsz, 48)
+    k, v = _kv(131, bsz, t, hkv, d, outl=0)
+    ramp = 1.8 * np.arange(t, dtype=np.float32) / t
+    k = k + ramp[None, :, None, None]
+    k = torch.from_numpy(k).to(torch.bfloat16).float().numpy()    # bf16-exact
+    pr.append(0, k, v, pt, np.zeros(bsz, np.int32))
+    q = queries(131, 0, bsz, hkv * g, d, False) + 2.0
+    q = torch.from_numpy(q).to(torch.bfloat16).float().numpy()
+    pr.decode_check(0, q, pt, np.array([t, t - 5], np.int32))
+
+
+def test_decode_large_value_scales():
+    """Values scaled by 2^9: p s leaves the fp16 range under a lagging running
+    maximum, so those rounds take the exact maximum.  o scales exactly."""
+    hkv, d, g, bsz, t = 2, 128, 4, 2, 600
+    pr = Pair(hkv, d, 128, (4, 4), bsz * 40, max_batch=bsz)
+    pt = page_table(132, bsz, 40)
+    k, v = _kv(132, bsz, t, hkv, d, outl=0)
+    ramp = 1.8 * np.arange(t, dtype=np.float32) / t
+    k = torch.from_numpy(k + ramp[None, :, None, None]).to(torch.bfloat16).float().numpy()
+    v = v * 512.0
+    pr.gpu.append(0, dev_bf16(k), dev_bf16(v), dev_i32(pt), dev_i32(np.zeros(bsz, np.int32)))
+    torch.cuda.synchronize()
+    assert pr.gpu.get_status() == 0
+    q = queries(132, 0, bsz, hkv * g, d, False) + 2.0
+    q = torch.from_numpy(q).to(torch.bfloat16).float().numpy()
+    lens = np.array([t, t - 7], np.int32)
+    o = pr.gpu.decode(0, torch.from_numpy(q).cuda().to(torch.bfloat16), dev_i32(pt), dev_i32(lens))
+    torch.cuda.synchronize()
+    assert pr.gpu.get_status() == 0
+    ref = attention.decode(pr.gpu_state(), 0, q.astype(np.float64), pt, lens)
+    compare_outputs(o.cpu().numpy() / 512.0, ref / 512.0)
