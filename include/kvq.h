@@ -94,7 +94,22 @@ typedef struct kvq_cache {
                                 of a batch (e.g. a one-sequence prefill) passes a
                                 descriptor whose pointers are offset to its rows. */
   int* status_dev;           /* device int, the sticky status word (may be NULL) */
+  int launch_flags;          /* 0 or KVQ_LAUNCH_OVERLAP (decode calls only) */
 } kvq_cache;
+
+/*
+ * KVQ_LAUNCH_OVERLAP: decode launches (kvq_decode_attn, kvq_decode_attn_static,
+ * kvq_decode_step) use programmatic dependent launch.  The kernel may start
+ * while the kernel launched just before it on the stream is still running.  Before
+ * that kernel has completed, it reads only the page table, the sequence lengths
+ * and the layer's pool, and it starts the page copies.  It waits for that
+ * kernel's completion before reading q, K_new, V_new or the window, and before
+ * writing anything.  Contract: the preceding kernel does not write this layer's
+ * pool, the page table or seq_lens.  A preceding kvq_decode_step of the same layer
+ * writes that pool, for example.  A copy or memset in between orders the
+ * launches as usual.
+ */
+#define KVQ_LAUNCH_OVERLAP 0x1
 
 /* Bytes of one page of `layer` (layout above); 0 on a bad descriptor. */
 size_t kvq_page_bytes(const kvq_cache* cache, int layer);

@@ -55,6 +55,7 @@ class kvq_cache(ctypes.Structure):
         ("layer_pools", ctypes.POINTER(ctypes.c_void_p)),
         ("window_bufs", ctypes.POINTER(ctypes.c_void_p)),
         ("status_dev", ctypes.c_void_p),
+        ("launch_flags", ctypes.c_int),
     ]
 
 
@@ -169,6 +170,7 @@ def kvq_decode_step(desc: kvq_cache, layer: int, K_new, V_new, q, q_is_fp32: boo
 
 
 STATIC_WORKSPACE_BYTES = 8 * 1024 * 1024   # KVQ_STATIC_WORKSPACE_BYTES in kvq.h
+LAUNCH_OVERLAP = 0x1                        # KVQ_LAUNCH_OVERLAP in kvq.h
 
 
 def kvq_decode_attn_static(desc: kvq_cache, layer: int, q, q_is_fp32: bool, page_table,
@@ -232,7 +234,8 @@ class Cache:
     """
 
     def __init__(self, num_layers: int, num_kv_heads: int, head_dim: int, had_block: int,
-                 bits, num_pages: int, window: int = 0, max_batch: int = 0, device="cuda"):
+                 bits, num_pages: int, window: int = 0, max_batch: int = 0, device="cuda",
+                 overlap: bool = False):
         import torch
         self.bits = np.ascontiguousarray(np.asarray(bits).reshape(num_layers, num_kv_heads, 2),
                                          dtype=np.int8)
@@ -259,6 +262,9 @@ class Cache:
             d.window_bufs = self._win_ptrs
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         d.status_dev = self.status.data_ptr()
+        # decode launches may overlap the preceding kernel (programmatic dependent
+        # launch); that kernel must not write these pools, the page table or the lengths
+        d.launch_flags = LAUNCH_OVERLAP if overlap else 0
         self._ws = {}
 
     # -- calls ------------------------------------------------------------------------------
@@ -342,7 +348,7 @@ class Cache:
 
 __all__ = [
     "KVQ_OK", "KVQ_EINVAL", "KVQ_EUNSUPPORTED", "KVQ_ECUDA", "KVQ_EBUDGET", "KVQ_EDEVICE",
-    "KVQ_EWORKSPACE", "DEV_BAD_PAGE", "DEV_BAD_LENGTH", "DEV_NONFINITE", "DEV_COPY_TIMEOUT",
+    "KVQ_EWORKSPACE", "LAUNCH_OVERLAP", "DEV_BAD_PAGE", "DEV_BAD_LENGTH", "DEV_NONFINITE", "DEV_COPY_TIMEOUT",
     "KvqError", "KvqLibraryMissing", "kvq_cache", "lib", "kvq_version", "kvq_last_error",
     "kvq_page_bytes", "kvq_append", "kvq_decode_workspace_bytes", "kvq_decode_attn",
     "kvq_decode_attn_static", "kvq_decode_step", "STATIC_WORKSPACE_BYTES",

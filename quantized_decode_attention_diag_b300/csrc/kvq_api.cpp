@@ -78,6 +78,8 @@ kvq_status check_geometry(const kvq_cache* c, int layer, kvq::LayerGeom* geom) {
 kvq_status check_cache(const kvq_cache* c, int layer, kvq::LayerGeom* geom) {
   const kvq_status st = check_geometry(c, layer, geom);
   if (st != KVQ_OK) return st;
+  if (c->launch_flags & ~KVQ_LAUNCH_OVERLAP)
+    return fail(KVQ_EINVAL, "launch_flags 0x%x has unknown bits", c->launch_flags);
   if (!c->layer_pools || !c->layer_pools[layer])
     return fail(KVQ_EINVAL, "layer_pools[%d] is NULL", layer);
   if (!aligned(c->layer_pools[layer], 16))
@@ -223,6 +225,7 @@ kvq_status decode_impl(const kvq_cache* cache, int layer, const void* K_new, con
   p.S = pl.S;
   p.NS = pl.NS;
   p.pages_per_split = pl.pages_per_split;
+  p.overlap = (cache->launch_flags & KVQ_LAUNCH_OVERLAP) ? 1 : 0;
   p.cluster = pl.cluster;
   p.stage_bytes = pl.stage_bytes;
   p.scale_log2 = scale * 1.4426950408889634f;

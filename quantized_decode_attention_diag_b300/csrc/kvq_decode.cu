@@ -285,12 +285,12 @@ __device__ __forceinline__ void load_query(const DecodeParams& p, int b, int h, 
   }
 }
 
-// First chunk of this warp's page ids (pages first + 4 k, k < 32, lane k),
-// bounded by the page-table row only, so that it can be issued before the
+// First chunk of this warp's page ids (pages pg0 + warp + 4 k, k < 32, lane
+// k), bounded by the page-table row only, so that it can be issued before the
 // sequence length is known; 0 past the row.
-__device__ __forceinline__ int load_page_chunk0(const DecodeParams& p, int b, int split) {
+__device__ __forceinline__ int load_page_chunk0(const DecodeParams& p, int b, int pg0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pg = split * p.pages_per_split + warp + kDecodeWarps * lane;
+  const int pg = pg0 + warp + kDecodeWarps * lane;
   if (pg >= p.max_pages) return 0;
   return static_cast<int>(ldg_nc_u32(p.page_table + static_cast<size_t>(b) * p.max_pages + pg));
 }
@@ -410,6 +410,15 @@ __device__ __forceinline__ uint32_t movm_trans(uint32_t a) {
   return d;
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel on
+// the stream start its CTAs early; wait returns once the kernel launched before
+// this one has completed and its writes are visible (at once when this grid was
+// launched without programmatic stream serialization).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // CTA merge, warp i: the partials of query head i of the kDecodeWarps warps
 // (merge region) -> the CTA's partial of head i in `out`; `drop` empties it.
 template <int D>
@@ -476,39 +485,53 @@ __device__ __forceinline__ void store_codes(uint8_t* dst, const uint32_t (&c)[2]
 // them to the cache page (for later calls) and to `pbuf` in shared memory
 // (K codes [KB], V codes [VB], K (s, z), V (s, z)), from which this launch's
 // staged copy of the page gets patched.  Same rule and same bits as kvq_append.
+// This lane's elements of ring slot pos % R of (b, h), K (lanes 0-15) or V.
+template <int D>
+__device__ __forceinline__ uint16_t* step_ring(const DecodeParams& p, int b, int h, int pos) {
+  constexpr int F = D / 16;
+  const int lane = threadIdx.x & 31, half = lane >> 4, l = lane & 15;
+  return const_cast<uint16_t*>(p.window) +
+         ((static_cast<size_t>(b) * p.Hkv + h) * 2 + half) * p.R * D +
+         static_cast<size_t>(pos % p.R) * D + F * l;
+}
+
+// The token that leaves the ring when position pos is quantized (its bf16
+// elements of this lane, as loaded by load_new_token for the new token).
+template <int D>
+__device__ __forceinline__ void step_ring_load(const DecodeParams& p, int b, int h, int pos,
+                                               uint32_t (&leave)[D / 32]) {
+  const uint16_t* ring = step_ring<D>(p, b, h, pos);
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) leave[i] = ldg_nc_u32(ring + 2 * i);
+}
+
+// Decode step, one warp: quantizes the token at position pos of (b, h) into
+// page `pid` -- the new token, or with a window the token leaving the ring
+// (`leave`), the new token taking its ring slot -- and leaves the patch in
+// pbuf (K codes [KB], V codes [VB], K (s, z), V (s, z)), from which this
+// launch's staged copy of the page gets patched.  Same rule and same bits as
+// kvq_append.
 template <int D>
 __device__ void step_append(const DecodeParams& p, int b, int h, int pos, int bk, int bv,
-                            const uint32_t (&tok)[D / 32], uint8_t* pbuf) {
+                            const uint32_t (&tok)[D / 32], const uint32_t (&leave)[D / 32],
+                            int pid, uint8_t* pbuf) {
   constexpr int F = D / 16;
   const int lane = threadIdx.x & 31, half = lane >> 4, l = lane & 15;
   const int bits = half ? bv : bk;
   const int KB = D * bk / 8, VB = D * bv / 8;
   const int rowb = half ? VB : KB;              // code bytes of this vector's row
   const int nb = F * bits / 8;                  // code bytes of this lane
-  uint16_t* ring = nullptr;                     // this lane's elements of the ring slot
-  if (p.R > 0)
-    ring = const_cast<uint16_t*>(p.window) + ((static_cast<size_t>(b) * p.Hkv + h) * 2 + half) *
-                                                  p.R * D +
-           static_cast<size_t>(pos % p.R) * D + F * l;
+  const bool ring = p.R > 0;
   float v[F];
-  if (ring) {                                   // the token leaving the ring
 #pragma unroll
-    for (int i = 0; i < F / 2; ++i) {
-      const uint32_t x = *reinterpret_cast<const uint32_t*>(ring + 2 * i);
-      v[2 * i] = bf16lo(x);
-      v[2 * i + 1] = bf16hi(x);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < F / 2; ++i) {
-      v[2 * i] = bf16lo(tok[i]);
-      v[2 * i + 1] = bf16hi(tok[i]);
-    }
+  for (int i = 0; i < F / 2; ++i) {
+    const uint32_t x = ring ? leave[i] : tok[i];
+    v[2 * i] = bf16lo(x);
+    v[2 * i + 1] = bf16hi(x);
   }
   uint32_t codes[2];
   __half sh, zh;
   rotate_quantize_halfwarp<D>(v, p.had_block, bits, codes, sh, zh);
-  const int pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pos / kPage);
   uint8_t* seg = nullptr;
   if (pid >= 0 && pid < p.num_pages) {
     seg = const_cast<uint8_t*>(p.pool) + static_cast<size_t>(pid) * p.geom.page_bytes +
@@ -527,8 +550,9 @@ __device__ void step_append(const DecodeParams& p, int b, int h, int pos, int bk
     if (seg) *reinterpret_cast<uint32_t*>(seg + kPage * (KB + VB) + 4 * kPage * half + slot * 4) = sz;
   }
   if (ring) {                                   // the new token takes the slot
+    uint16_t* slot_ptr = step_ring<D>(p, b, h, pos);
 #pragma unroll
-    for (int i = 0; i < F / 2; ++i) *reinterpret_cast<uint32_t*>(ring + 2 * i) = tok[i];
+    for (int i = 0; i < F / 2; ++i) *reinterpret_cast<uint32_t*>(slot_ptr + 2 * i) = tok[i];
   }
   __syncwarp();
 }
@@ -559,7 +583,7 @@ __device__ __forceinline__ void patch_stage(uint32_t st, const uint8_t* pbuf, in
 // of the quantized part; warp w takes pages w, w + 4, ... two at a time.
 template <int D, int BK, int BV>
 __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h, int split,
-                            int lq, float (&qv)[D / 32], int chunk0, const uint32_t (&tok)[D / 32]) {
+                            int lq, float (&qv)[D / 32], int chunk0, uint32_t (&tok)[D / 32]) {
   constexpr int KB = D * BK / 8;                 // K code bytes per token
   constexpr int VB = D * BV / 8;
   constexpr int CHUNK = kPage * (KB + VB + 8);   // one (page, head) segment
@@ -586,9 +610,15 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   //      32 per chunk (lane i holds page k = 32 * chunk + i).  Ids outside
   //      [0, num_pages) are reported, replaced by page 0 so that every copy
   //      stays in bounds, and the whole split is dropped at the end.
+  // S splits of this sequence's pages: the host plan's split size (from the
+  // page-table width) while it still gives every split pages, else the split
+  // size of this length (and the page ids loaded for the plan's are reloaded)
   const int npages = (lq + kPage - 1) / kPage;
-  const int pg0 = split * p.pages_per_split;
-  const int pg1 = min(npages, pg0 + p.pages_per_split);
+  const int pps = npages > p.pages_per_split * (p.S - 1) ? p.pages_per_split
+                                                          : max(1, (npages + p.S - 1) / p.S);
+  const int pg0 = split * pps;
+  const int pg1 = min(npages, pg0 + pps);
+  if (pps != p.pages_per_split) chunk0 = load_page_chunk0(p, b, pg0);
   const int first = pg0 + warp;
   const int nk = pg1 > first ? (pg1 - first + kDecodeWarps - 1) / kDecodeWarps : 0;
   const int32_t* ptab = p.page_table + static_cast<size_t>(b) * p.max_pages + first;
@@ -626,22 +656,37 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     mbar_expect_tx(bar, CHUNK);
     bulk_g2s(stages + slot * stage_bytes, head_base + pid * page_bytes, CHUNK, bar);
   };
+  // decode step: the warp owning the page of the last quantized position
+  // quantizes the token there (warp-uniform)
+  const int plast = npages - 1;
+  const bool owner = p.step && lq > 0 && plast >= pg0 && plast < pg1 &&
+                     (plast - pg0) % kDecodeWarps == warp;
+  const int kpatch = owner ? (plast - pg0) / kDecodeWarps : -1;
+  uint32_t leave[D / 32];
+  if (owner && p.R > 0 && !p.overlap) step_ring_load<D>(p, b, h, lq - 1, leave);
+
   // start streaming before the query prologue
   for (int kk = 0; kk < nk && kk < NST; ++kk) {
     const int pid = pid_of(kk);
     if (lane == 0) issue(kk, pid);
   }
 
-  // decode step: the warp owning the page of the last quantized position
-  // quantizes the token there while its first copies are in flight
-  int kpatch = -1;
+  // with programmatic dependent launch, everything above may overlap the
+  // previous kernel; q and the new token are its results
+  grid_wait();
+  if (p.overlap) {
+    load_query<D>(p, b, h, qv);
+    if (p.step) load_new_token<D>(p, b, h, tok);
+    if (owner && p.R > 0) step_ring_load<D>(p, b, h, lq - 1, leave);
+  }
+
+  // the step's token goes in while the first copies are in flight; its page
+  // id is among the raw ids this warp loaded for its first 32 pages
   uint8_t* pbuf = reinterpret_cast<uint8_t*>(sm.merge);
-  if (p.step && lq > 0) {
-    const int pl = npages - 1;
-    if (pl >= pg0 && pl < pg1 && (pl - pg0) % kDecodeWarps == warp) {
-      kpatch = (pl - pg0) / kDecodeWarps;
-      step_append<D>(p, b, h, lq - 1, BK, BV, tok, pbuf);
-    }
+  if (owner) {
+    int pid = __shfl_sync(kFullMask, chunk0, kpatch & 31);
+    if (kpatch >= 32) pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + plast);
+    step_append<D>(p, b, h, lq - 1, BK, BV, tok, leave, pid, pbuf);
   }
   const int pslot = (lq - 1) % kPage;
 
@@ -1114,14 +1159,19 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5;
 
+  grid_launch_dependents();
+
   // The query, page-id and length loads go out first: the page copies issued
   // next fill the memory system for microseconds, and a load queued behind
-  // them would stall the CTA for as long.
+  // them would stall the CTA for as long.  Under programmatic dependent launch
+  // the query and the new token are loaded after the wait instead.
   float qv[D / 32];
-  load_query<D>(p, b, h, qv);
-  const int chunk0 = split < p.S ? load_page_chunk0(p, b, split) : 0;
   uint32_t tok[D / 32];                 // decode step: this lane's part of the new token
-  if (p.step && split < p.S) load_new_token<D>(p, b, h, tok);
+  if (!p.overlap) {
+    load_query<D>(p, b, h, qv);
+    if (p.step && split < p.S) load_new_token<D>(p, b, h, tok);
+  }
+  const int chunk0 = split < p.S ? load_page_chunk0(p, b, split * p.pages_per_split) : 0;
   int len = static_cast<int>(ldg_nc_u32(p.seq_lens + b));
   if (len < p.step || len > p.max_pages * kPage) {   // a step appends one token: len >= 1
     if (tid == 0) flag_status(p.status, KVQ_DEV_BAD_LENGTH);
@@ -1138,6 +1188,8 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
   __syncthreads();
 
   if (is_window) {
+    grid_wait();
+    if (p.overlap) load_query<D>(p, b, h, qv);
     query_window_prologue<D>(p, sm, qv);
     window_split<D>(p, sm, b, h, len, lq, sm.cpart);
   } else {
@@ -1223,15 +1275,22 @@ cudaError_t launch_d(const DecodeParams& p, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = bytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
   if (p.cluster) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = p.NS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = p.NS;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
   }
+  if (p.overlap) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, decode_kernel<D>, p);
 }
 

@@ -12,6 +12,7 @@ import pytest
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
+import quantized_decode_attention_diag_b300 as kvq
 from oracle import attention, cache as ocache
 from tests.parity import compare_outputs, compare_written
 from tests.test_gpu_parity import Pair, dev_bf16, dev_i32, _need_gpu  # noqa: F401
@@ -124,6 +125,72 @@ def test_step_rejects_a_zero_length():
     q = torch.zeros((1, 32, 128), dtype=torch.bfloat16, device="cuda")
     pr.gpu.decode_step(0, dev_bf16(kn), dev_bf16(kn), q, dev_i32(pt), dev_i32(np.zeros(1, np.int32)))
     torch.cuda.synchronize()
-    import quantized_decode_attention_diag_b300 as kvq
+
     assert pr.gpu.get_status() & kvq.DEV_BAD_LENGTH
     pr.gpu.reset_status()
+
+
+@pytest.mark.parametrize("window", [0, 128])
+def test_step_overlapped_layers(window):
+    """Back-to-back decode steps of several layers launched with programmatic
+    dependent launch (each may start while the previous layer's kernel runs),
+    eagerly and replayed from a CUDA graph: the same cache bytes and o as
+    ordinary launches, and o within tolerance of the oracle."""
+    L, hkv, d, g, bsz, t = 4, 8, 128, 4, 3, 700
+    mp = t // 16 + 2
+    pt = page_table(95, bsz, mp)
+    caches = []
+    for overlap in (False, True):
+        c = kvq.Cache(L, hkv, d, 128, np.full((L, hkv, 2), 4), bsz * mp, window, bsz,
+                      overlap=overlap)
+        for l in range(L):
+            k = kv_tokens(95, 2 * l, bsz, t, hkv, d, 4, 10.0, 50.0)
+            v = kv_tokens(95, 2 * l + 1, bsz, t, hkv, d, 4, 10.0, 50.0)
+            c.append(l, dev_bf16(k[:, :t - 1]), dev_bf16(v[:, :t - 1]), dev_i32(pt),
+                     dev_i32(np.zeros(bsz, np.int32)))
+        caches.append((c, k, v))
+    torch.cuda.synchronize()
+    kn = [dev_bf16(kv_tokens(95, 2 * l, bsz, t, hkv, d, 4, 10.0, 50.0)[:, t - 1]) for l in range(L)]
+    vn = [dev_bf16(kv_tokens(95, 2 * l + 1, bsz, t, hkv, d, 4, 10.0, 50.0)[:, t - 1])
+          for l in range(L)]
+    q = [torch.from_numpy(queries(96, l, bsz, hkv * g, d, False)).cuda().to(torch.bfloat16)
+         for l in range(L)]
+    ptd, lens = dev_i32(pt), dev_i32(np.full(bsz, t, np.int32))
+    outs = []
+    for c, _, _ in caches:
+        o = torch.zeros((L, bsz, hkv * g, d), dtype=torch.float32, device="cuda")
+        ws = c.workspace(bsz, hkv * g, mp)
+        for l in range(L):
+            c.decode_step(l, kn[l], vn[l], q[l], ptd, lens, o=o[l], workspace=ws)
+        torch.cuda.synchronize()
+        assert c.get_status() == 0
+        first = o.clone()
+        if window:   # a step moves the ring: repeating it is not idempotent
+            outs.append(o.cpu().numpy())
+            continue
+        # the same steps from a graph (the step re-appends the same token: idempotent)
+        o.zero_()
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=s):
+                for l in range(L):
+                    c.decode_step(l, kn[l], vn[l], q[l], ptd, lens, o=o[l], workspace=ws)
+            for _ in range(3):
+                gr.replay()
+        torch.cuda.synchronize()
+        assert c.get_status() == 0
+        assert torch.equal(first, o)
+        outs.append(o.cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
+    for l in range(L):
+        assert np.array_equal(caches[0][0].pool_host(l), caches[1][0].pool_host(l))
+        if window:
+            assert np.array_equal(caches[0][0].window_host(l), caches[1][0].window_host(l))
+    c = caches[1][0]
+    for l in (0, L - 1):
+        st = ocache.CacheState(d, 128, window, c.bits, [c.pool_host(x) for x in range(L)],
+                               None if not window else [c.window_host(x) for x in range(L)])
+        ref = attention.decode(st, l, queries(96, l, bsz, hkv * g, d, False).astype(np.float64),
+                               pt, np.full(bsz, t, np.int32))
+        compare_outputs(outs[1][l], ref)
