@@ -485,53 +485,44 @@ __device__ __forceinline__ void store_codes(uint8_t* dst, const uint32_t (&c)[2]
 // them to the cache page (for later calls) and to `pbuf` in shared memory
 // (K codes [KB], V codes [VB], K (s, z), V (s, z)), from which this launch's
 // staged copy of the page gets patched.  Same rule and same bits as kvq_append.
-// This lane's elements of ring slot pos % R of (b, h), K (lanes 0-15) or V.
-template <int D>
-__device__ __forceinline__ uint16_t* step_ring(const DecodeParams& p, int b, int h, int pos) {
-  constexpr int F = D / 16;
-  const int lane = threadIdx.x & 31, half = lane >> 4, l = lane & 15;
-  return const_cast<uint16_t*>(p.window) +
-         ((static_cast<size_t>(b) * p.Hkv + h) * 2 + half) * p.R * D +
-         static_cast<size_t>(pos % p.R) * D + F * l;
-}
-
-// The token that leaves the ring when position pos is quantized (its bf16
-// elements of this lane, as loaded by load_new_token for the new token).
-template <int D>
-__device__ __forceinline__ void step_ring_load(const DecodeParams& p, int b, int h, int pos,
-                                               uint32_t (&leave)[D / 32]) {
-  const uint16_t* ring = step_ring<D>(p, b, h, pos);
-#pragma unroll
-  for (int i = 0; i < D / 32; ++i) leave[i] = ldg_nc_u32(ring + 2 * i);
-}
-
-// Decode step, one warp: quantizes the token at position pos of (b, h) into
-// page `pid` -- the new token, or with a window the token leaving the ring
-// (`leave`), the new token taking its ring slot -- and leaves the patch in
-// pbuf (K codes [KB], V codes [VB], K (s, z), V (s, z)), from which this
-// launch's staged copy of the page gets patched.  Same rule and same bits as
-// kvq_append.
+// Decode step, one warp: quantizes the token at position pos of (b, h) -- the
+// new token, or with a window the token leaving the ring, the new token taking
+// its ring slot -- into its page, and leaves the patch in pbuf (K codes [KB],
+// V codes [VB], K (s, z), V (s, z)), from which this launch's staged copy of
+// the page gets patched.  Same rule and same bits as kvq_append.
 template <int D>
 __device__ void step_append(const DecodeParams& p, int b, int h, int pos, int bk, int bv,
-                            const uint32_t (&tok)[D / 32], const uint32_t (&leave)[D / 32],
-                            int pid, uint8_t* pbuf) {
+                            const uint32_t (&tok)[D / 32], uint8_t* pbuf) {
   constexpr int F = D / 16;
   const int lane = threadIdx.x & 31, half = lane >> 4, l = lane & 15;
   const int bits = half ? bv : bk;
   const int KB = D * bk / 8, VB = D * bv / 8;
   const int rowb = half ? VB : KB;              // code bytes of this vector's row
   const int nb = F * bits / 8;                  // code bytes of this lane
-  const bool ring = p.R > 0;
+  uint16_t* ring = nullptr;                     // this lane's elements of the ring slot
+  if (p.R > 0)
+    ring = const_cast<uint16_t*>(p.window) + ((static_cast<size_t>(b) * p.Hkv + h) * 2 + half) *
+                                                  p.R * D +
+           static_cast<size_t>(pos % p.R) * D + F * l;
   float v[F];
+  if (ring) {                                   // the token leaving the ring
 #pragma unroll
-  for (int i = 0; i < F / 2; ++i) {
-    const uint32_t x = ring ? leave[i] : tok[i];
-    v[2 * i] = bf16lo(x);
-    v[2 * i + 1] = bf16hi(x);
+    for (int i = 0; i < F / 2; ++i) {
+      const uint32_t x = *reinterpret_cast<const uint32_t*>(ring + 2 * i);
+      v[2 * i] = bf16lo(x);
+      v[2 * i + 1] = bf16hi(x);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < F / 2; ++i) {
+      v[2 * i] = bf16lo(tok[i]);
+      v[2 * i + 1] = bf16hi(tok[i]);
+    }
   }
   uint32_t codes[2];
   __half sh, zh;
   rotate_quantize_halfwarp<D>(v, p.had_block, bits, codes, sh, zh);
+  const int pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pos / kPage);
   uint8_t* seg = nullptr;
   if (pid >= 0 && pid < p.num_pages) {
     seg = const_cast<uint8_t*>(p.pool) + static_cast<size_t>(pid) * p.geom.page_bytes +
@@ -550,9 +541,8 @@ __device__ void step_append(const DecodeParams& p, int b, int h, int pos, int bk
     if (seg) *reinterpret_cast<uint32_t*>(seg + kPage * (KB + VB) + 4 * kPage * half + slot * 4) = sz;
   }
   if (ring) {                                   // the new token takes the slot
-    uint16_t* slot_ptr = step_ring<D>(p, b, h, pos);
 #pragma unroll
-    for (int i = 0; i < F / 2; ++i) *reinterpret_cast<uint32_t*>(slot_ptr + 2 * i) = tok[i];
+    for (int i = 0; i < F / 2; ++i) *reinterpret_cast<uint32_t*>(ring + 2 * i) = tok[i];
   }
   __syncwarp();
 }
@@ -656,15 +646,6 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     mbar_expect_tx(bar, CHUNK);
     bulk_g2s(stages + slot * stage_bytes, head_base + pid * page_bytes, CHUNK, bar);
   };
-  // decode step: the warp owning the page of the last quantized position
-  // quantizes the token there (warp-uniform)
-  const int plast = npages - 1;
-  const bool owner = p.step && lq > 0 && plast >= pg0 && plast < pg1 &&
-                     (plast - pg0) % kDecodeWarps == warp;
-  const int kpatch = owner ? (plast - pg0) / kDecodeWarps : -1;
-  uint32_t leave[D / 32];
-  if (owner && p.R > 0 && !p.overlap) step_ring_load<D>(p, b, h, lq - 1, leave);
-
   // start streaming before the query prologue
   for (int kk = 0; kk < nk && kk < NST; ++kk) {
     const int pid = pid_of(kk);
@@ -677,16 +658,18 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   if (p.overlap) {
     load_query<D>(p, b, h, qv);
     if (p.step) load_new_token<D>(p, b, h, tok);
-    if (owner && p.R > 0) step_ring_load<D>(p, b, h, lq - 1, leave);
   }
 
-  // the step's token goes in while the first copies are in flight; its page
-  // id is among the raw ids this warp loaded for its first 32 pages
+  // decode step: the warp owning the page of the last quantized position
+  // quantizes the token there while its first copies are in flight
+  int kpatch = -1;
   uint8_t* pbuf = reinterpret_cast<uint8_t*>(sm.merge);
-  if (owner) {
-    int pid = __shfl_sync(kFullMask, chunk0, kpatch & 31);
-    if (kpatch >= 32) pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + plast);
-    step_append<D>(p, b, h, lq - 1, BK, BV, tok, leave, pid, pbuf);
+  if (p.step && lq > 0) {
+    const int pl = npages - 1;
+    if (pl >= pg0 && pl < pg1 && (pl - pg0) % kDecodeWarps == warp) {
+      kpatch = (pl - pg0) / kDecodeWarps;
+      step_append<D>(p, b, h, lq - 1, BK, BV, tok, pbuf);
+    }
   }
   const int pslot = (lq - 1) % kPage;
 
