@@ -393,6 +393,7 @@ def run_kvq(args) -> None:
 
     # append sweep: 8 sequences x 8192 new tokens into empty caches
     append = append_sweep(kvq, torch, dev) if not args.skip_append else None
+    calib = calibration_bench(kvq, torch, dev) if not args.skip_append else None
 
     if rank != 0:
         if world > 1:
@@ -427,6 +428,7 @@ def run_kvq(args) -> None:
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
         "append": append,
+        "calibration": calib,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -472,6 +474,52 @@ def append_sweep(kvq, torch, dev) -> dict:
     return {"workload": "append-sweep 8 seqs x 8192 new tokens, 8 KV heads, head_dim 128",
             "bytes": "bf16 K/V read + packed codes + fp16 (s, z) written",
             "unit": "tokens/s", "points": points}
+
+
+def calibration_bench(kvq, torch, dev) -> dict:
+    """Distortion calibration of a 32-layer cache: per layer, K and V of 16
+    calibration sequences x 512 tokens (8 KV heads, head_dim 128), MSE at widths
+    2 .. 6 (kvq_distortion), then the host fit of (alpha, beta) per component."""
+    w = LLAMA3_8B_LAYER
+    seqs, t, hkv, d, widths = 16, 512, w.hkv, w.head_dim, [2, 3, 4, 5, 6]
+    T = seqs * t
+    xs = [torch.from_numpy(kv_tokens(w.seed + 7, kv, seqs, t, hkv, d,
+                                     w.k_outliers if kv == 0 else w.v_outliers,
+                                     w.outlier_lo, w.outlier_hi).reshape(T, hkv, d))
+          .to(dev).to(torch.bfloat16) for kv in range(2)]
+    outs = [torch.empty((hkv, len(widths)), dtype=torch.float64, device=dev)
+            for _ in range(2 * N_LAYERS)]
+
+    def run():   # 2 * N_LAYERS calls: the two sample tensors stand in for every layer's
+        for i in range(2 * N_LAYERS):
+            kvq.kvq_distortion(d, w.had_block, xs[i % 2], widths, mse=outs[i])
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    reps = 5
+    e0.record()
+    for _ in range(reps):
+        run()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    sec = e0.elapsed_time(e1) / reps * 1e-3 / (2 * N_LAYERS)
+    t0 = time.perf_counter()
+    mse = torch.stack(outs).cpu().numpy().reshape(-1, len(widths))
+    alpha, beta = kvq.kvq_fit_distortion(mse, widths)
+    fit_s = time.perf_counter() - t0
+    nbytes = T * hkv * d * 2
+    pk = peaks()
+    return {"workload": f"calibration: {N_LAYERS} layers x (K, V) x {seqs} seqs x {t} tokens, "
+                        f"{hkv} KV heads, head_dim {d}, widths 2..6",
+            "us_per_call": round(sec * 1e6, 2), "vectors_per_s": round(T * hkv / sec, 1),
+            "GB_s": round(nbytes / sec / 1e9, 1),
+            "frac_of_hbm": round(nbytes / sec / 1e9 / pk["hbm_gbs"], 4),
+            "bytes": "bf16 vectors read once per call",
+            "fit_ms": round(fit_s * 1e3, 3),
+            "beta_range": [round(float(beta.min()), 3), round(float(beta.max()), 3)]}
 
 
 def main() -> None:

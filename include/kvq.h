@@ -12,6 +12,8 @@
  *                    once-rotated query; merges the bf16 window; writes fp32 o.
  *   kvq_alloc_bits   RateQuant greedy marginal-gain allocation of per-component
  *                    bit-widths (host only).
+ *   kvq_distortion   per-head quantization MSE at several widths (calibration),
+ *   kvq_fit_distortion  and the (alpha, beta) fit of D(b) = alpha beta^-b.
  *
  * Conventions shared by every call
  *   - Every pointer marked "device" is caller-owned device memory (e.g. from
@@ -245,6 +247,50 @@ kvq_status kvq_decode_attn_static(const kvq_cache* cache, int layer, const void*
  */
 kvq_status kvq_alloc_bits(const double* w, const double* beta, int n, long long budget,
                           const uint16_t* allowed_mask, int* bits_out, long long* leftover);
+
+/*
+ * kvq_distortion -- distortion calibration: the mean-squared error of this
+ * library's quantizer (rotation, fp16 scale and zero, round-half-even codes,
+ * as stored by kvq_append) at several bit-widths, per KV head, on a sample of
+ * K or V vectors.  Follows the RateQuant technical summary, Methodology
+ * section 3 (fit the distortion model D(b) = alpha * beta^-b of the quantizer
+ * actually used, on a small calibration set, per K and V component) and
+ * section 4 (the fit takes 5 bit-widths).
+ *
+ *   head_dim, had_block  as in kvq_cache (64 | 128; 32 | 64 | 128 dividing it).
+ *   X        device bf16 [T][num_kv_heads][head_dim], 16-byte aligned: T vectors
+ *            per head (e.g. a batch of calibration sequences, flattened).
+ *   widths   host int [n_widths], each 1 .. 8; n_widths 1 .. 8.
+ *   mse      device double [num_kv_heads][n_widths], 8-byte aligned, overwritten
+ *            with sum over the T vectors of |x - deq(x)|^2 / (T * head_dim) in the
+ *            model's basis.  The orthonormal rotation keeps that norm, so it is
+ *            sum |u - deq(u)|^2 / (had_block * T * head_dim), where u is the
+ *            unnormalised rotation.
+ * A width-b code is c = round-half-even((u - z) / s) with M = 2^b - 1 levels, as
+ * for the cache's 2-, 4- and 8-bit codes.  Zeroes mse and launches one kernel on
+ * `stream`.  Per-CTA sums are added in fp64 atomically, so the last bits depend
+ * on their order.  T == 0 gives zeros.
+ */
+kvq_status kvq_distortion(int head_dim, int had_block, int num_kv_heads, const void* X,
+                          long long T, const int* widths, int n_widths, double* mse,
+                          void* stream);
+
+/*
+ * kvq_fit_distortion -- least-squares fit of ln D(b) = ln alpha - b ln beta per
+ * component (host only), the distortion model of the RateQuant technical
+ * summary, Methodology section 1, fitted as in section 3.
+ *
+ *   mse    host double [n][n_widths] (e.g. kvq_distortion's output, copied back).
+ *   widths host int [n_widths], distinct.
+ *   alpha, beta  host double [n], written.
+ * Widths whose D is not positive and finite (a lossless width) are left out.  A
+ * component with fewer than two widths left takes beta = 4: one more bit halves a
+ * uniform quantizer's step and quarters its error.  Its alpha then comes from the
+ * width left (D(b) 4^b), or is 0 when none is left.  The result feeds
+ * kvq_alloc_bits as w_i = sensitivity_i * alpha_i, beta_i.
+ */
+kvq_status kvq_fit_distortion(const double* mse, const int* widths, int n_widths, int n,
+                              double* alpha, double* beta);
 
 /* Copy the device status word into *device_status (synchronous copy; the caller
  * synchronises the streams that ran kernels first).  Returns KVQ_EDEVICE when it

@@ -72,6 +72,8 @@ _SIGS = {
     "kvq_decode_step": (_I, [ctypes.POINTER(kvq_cache), _I, _P, _P, _P, _I, _P, _I, _P, _I, _I, _F,
                              _P, _P, _SZ, _P]),
     "kvq_alloc_bits": (_I, [_P, _P, _I, _LL, _P, _P, _P]),
+    "kvq_distortion": (_I, [_I, _I, _I, _P, _LL, _P, _I, _P, _P]),
+    "kvq_fit_distortion": (_I, [_P, _P, _I, _I, _P, _P]),
     "kvq_get_status": (_I, [ctypes.POINTER(kvq_cache), ctypes.POINTER(ctypes.c_int)]),
     "kvq_reset_status": (_I, [ctypes.POINTER(kvq_cache), _P]),
     "kvq_last_error": (ctypes.c_char_p, []),
@@ -202,6 +204,37 @@ def kvq_alloc_bits(w: Sequence[float], beta: Sequence[float], budget: int,
                                 None if mask is None else mask.ctypes.data, out.ctypes.data,
                                 ctypes.addressof(left)))
     return out.tolist(), int(left.value)
+
+
+def kvq_distortion(head_dim: int, had_block: int, X, widths: Sequence[int], mse=None,
+                   stream=None):
+    """Per-head quantization MSE at each width: X bf16 [T][Hkv][head_dim] on the
+    device; returns (or fills) a float64 device tensor [Hkv][len(widths)]."""
+    import torch
+    T, hkv = int(X.shape[0]), int(X.shape[1])
+    if X.dim() != 3 or int(X.shape[2]) != head_dim or X.dtype != torch.bfloat16:
+        raise ValueError("X must be bf16 [T][Hkv][head_dim]")
+    if not X.is_contiguous():
+        raise ValueError("X must be contiguous")
+    w = np.ascontiguousarray(widths, dtype=np.int32)
+    if mse is None:
+        mse = torch.empty((hkv, int(w.shape[0])), dtype=torch.float64, device=X.device)
+    _check(lib().kvq_distortion(head_dim, had_block, hkv, _ptr(X), T, w.ctypes.data,
+                                int(w.shape[0]), _ptr(mse), _stream(stream)))
+    return mse
+
+
+def kvq_fit_distortion(mse, widths: Sequence[int]) -> tuple[np.ndarray, np.ndarray]:
+    """(alpha, beta) per row of mse [n][len(widths)] (host) for D(b) = alpha beta^-b."""
+    d = np.ascontiguousarray(mse, dtype=np.float64)
+    w = np.ascontiguousarray(widths, dtype=np.int32)
+    if d.ndim != 2 or d.shape[1] != w.shape[0]:
+        raise ValueError("mse must be [n][len(widths)]")
+    alpha = np.zeros(d.shape[0], np.float64)
+    beta = np.zeros(d.shape[0], np.float64)
+    _check(lib().kvq_fit_distortion(d.ctypes.data, w.ctypes.data, int(w.shape[0]),
+                                    int(d.shape[0]), alpha.ctypes.data, beta.ctypes.data))
+    return alpha, beta
 
 
 def kvq_get_status(desc: kvq_cache) -> int:
@@ -352,5 +385,6 @@ __all__ = [
     "KvqError", "KvqLibraryMissing", "kvq_cache", "lib", "kvq_version", "kvq_last_error",
     "kvq_page_bytes", "kvq_append", "kvq_decode_workspace_bytes", "kvq_decode_attn",
     "kvq_decode_attn_static", "kvq_decode_step", "STATIC_WORKSPACE_BYTES",
+    "kvq_distortion", "kvq_fit_distortion",
     "kvq_alloc_bits", "kvq_get_status", "kvq_reset_status", "mask_of", "Cache",
 ]

@@ -19,7 +19,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libkvq.so")
-SOURCES = ["kvq_api.cpp", "kvq_append.cu", "kvq_decode.cu", "kvq_static.cu"]
+SOURCES = ["kvq_api.cpp", "kvq_append.cu", "kvq_decode.cu", "kvq_static.cu", "kvq_calib.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -322,6 +322,51 @@ kvq_status kvq_decode_step(const kvq_cache* cache, int layer, const void* K_new,
                      Hq, softmax_scale, o, workspace, ws_bytes, stream);
 }
 
+kvq_status kvq_fit_distortion(const double* mse, const int* widths, int n_widths, int n,
+                              double* alpha, double* beta) {
+  if (n < 0 || n_widths < 1) return fail(KVQ_EINVAL, "n must be >= 0 and n_widths >= 1");
+  if (n == 0) return KVQ_OK;
+  if (!mse || !widths || !alpha || !beta)
+    return fail(KVQ_EINVAL, "mse, widths, alpha and beta must be non-NULL");
+  for (int a = 0; a < n_widths; ++a)
+    for (int b = a + 1; b < n_widths; ++b)
+      if (widths[a] == widths[b]) return fail(KVQ_EINVAL, "width %d repeated", widths[a]);
+  for (int i = 0; i < n; ++i) {
+    const double* d = mse + static_cast<size_t>(i) * n_widths;
+    // least squares of y = ln D against b over the usable widths:
+    // y = ln alpha - b ln beta
+    double sb = 0.0, sy = 0.0;
+    int k = 0, last = -1;
+    for (int w = 0; w < n_widths; ++w) {
+      if (d[w] > 0.0 && std::isfinite(d[w])) {
+        sb += widths[w];
+        sy += std::log(d[w]);
+        ++k;
+        last = w;
+      }
+    }
+    if (k >= 2) {
+      const double mb = sb / k, my = sy / k;
+      double sxx = 0.0, sxy = 0.0;
+      for (int w = 0; w < n_widths; ++w) {
+        if (d[w] > 0.0 && std::isfinite(d[w])) {
+          const double x = widths[w] - mb;
+          sxx += x * x;
+          sxy += x * (std::log(d[w]) - my);
+        }
+      }
+      const double ln_beta = -sxy / sxx;
+      beta[i] = std::exp(ln_beta);
+      alpha[i] = std::exp(my + ln_beta * mb);
+    } else {
+      // one more bit quarters a uniform quantizer's error
+      beta[i] = 4.0;
+      alpha[i] = k == 1 ? d[last] * std::pow(4.0, widths[last]) : 0.0;
+    }
+  }
+  return KVQ_OK;
+}
+
 kvq_status kvq_alloc_bits(const double* w, const double* beta, int n, long long budget,
                           const uint16_t* allowed_mask, int* bits_out, long long* leftover) {
   if (n < 1 || !w || !beta || !bits_out)

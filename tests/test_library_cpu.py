@@ -136,3 +136,41 @@ def test_host_argument_checks_run_before_any_device_call():
     assert _checked(dec, desc, 12) == kvq.KVQ_EINVAL            # Hq not a multiple of Hkv
     assert _checked(dec, desc, 64) == kvq.KVQ_EUNSUPPORTED      # GQA group of 8
     assert kvq.kvq_append(desc, 0, fake, fake, fake, 4, fake, 2, 0, 0) is None   # T_new = 0: no-op
+
+
+# ------------------------------------------------------------ distortion calibration (host)
+
+def test_fit_distortion_matches_the_oracle_fit():
+    from oracle import distortion
+    rng = np.random.default_rng(21)
+    widths = [2, 3, 4, 5, 6]
+    b = np.array(widths, np.float64)
+    mse = np.stack([rng.uniform(0.1, 3.0) * rng.uniform(3.0, 6.0) ** (-b) *
+                    np.exp(rng.normal(0.0, 0.05, size=b.shape)) for _ in range(40)])
+    alpha, beta = kvq.kvq_fit_distortion(mse, widths)
+    for i in range(40):
+        a, bt = distortion.fit(widths, mse[i])
+        assert abs(alpha[i] / a - 1) < 1e-10 and abs(beta[i] / bt - 1) < 1e-10
+
+
+def test_fit_distortion_fallbacks_and_errors():
+    alpha, beta = kvq.kvq_fit_distortion([[0.0, 0.0, 2e-3], [0.0, 0.0, 0.0]], [2, 4, 8])
+    assert beta.tolist() == [4.0, 4.0]
+    assert abs(alpha[0] - 2e-3 * 4.0 ** 8) < 1e-9 and alpha[1] == 0.0
+    with pytest.raises(kvq.KvqError):
+        kvq.kvq_fit_distortion([[1.0, 0.5]], [4, 4])
+
+
+def test_distortion_host_checks_run_before_any_device_call():
+    fake = 1 << 20                       # never dereferenced: every call fails its checks first
+    L = kvq.lib()
+    w = np.array([2, 3, 4], np.int32)
+    assert L.kvq_distortion(96, 32, 8, fake, 10, w.ctypes.data, 3, fake, 0) == kvq.KVQ_EUNSUPPORTED
+    assert L.kvq_distortion(128, 48, 8, fake, 10, w.ctypes.data, 3, fake, 0) == kvq.KVQ_EINVAL
+    assert L.kvq_distortion(128, 128, 0, fake, 10, w.ctypes.data, 3, fake, 0) == kvq.KVQ_EINVAL
+    assert L.kvq_distortion(128, 128, 8, fake, -1, w.ctypes.data, 3, fake, 0) == kvq.KVQ_EINVAL
+    assert L.kvq_distortion(128, 128, 8, fake, 10, w.ctypes.data, 0, fake, 0) == kvq.KVQ_EINVAL
+    bad = np.array([2, 9], np.int32)
+    assert L.kvq_distortion(128, 128, 8, fake, 10, bad.ctypes.data, 2, fake, 0) == kvq.KVQ_EINVAL
+    assert L.kvq_distortion(128, 128, 8, fake + 4, 10, w.ctypes.data, 3, fake, 0) == kvq.KVQ_EINVAL
+    assert L.kvq_distortion(128, 128, 8, fake, 10, w.ctypes.data, 3, fake + 4, 0) == kvq.KVQ_EINVAL
