@@ -101,6 +101,19 @@ __device__ __forceinline__ void prefetch_chunk(const AppendParams& p, const RowR
   }
 }
 
+// load_row_top from the staged row (both halves; see kvq_quant.cuh)
+template <int D>
+__device__ __forceinline__ void row_top_from_smem(const uint4* buf, int row, int u,
+                                                  float (&v)[D / 2]) {
+  const float sgn = u ? -1.f : 1.f;
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) {
+    const uint4 lo = buf[row * (D / 8) + swz<D>(row, i)];
+    const uint4 hi = buf[row * (D / 8) + swz<D>(row, D / 16 + i)];
+    top_stage8(lo, hi, sgn, v + 8 * i);
+  }
+}
+
 template <int D>
 __device__ __forceinline__ void half_row_from_smem(const uint4* buf, int row, int u,
                                                    float (&v)[D / 2]) {
@@ -170,10 +183,18 @@ __device__ __forceinline__ void append_chunk(const AppendParams& p, const RowRef
   // ---- this lane's half of the row, rotated and quantized with its partner;
   //      rows past the batch quantize whatever the buffer holds, unused
   float v[E];
-  if (from_ring == nullptr) {
-    half_row_from_smem<D>(buf, row, u, v);
+  if constexpr (NB > E) {                // the block is the whole vector: top stage first
+    if (from_ring == nullptr) {
+      row_top_from_smem<D>(buf, row, u, v);
+    } else {
+      load_row_top<D>(from_ring, u, v);  // only with a window
+    }
   } else {
-    load_half_row<D>(from_ring, u, v);   // only with a window
+    if (from_ring == nullptr) {
+      half_row_from_smem<D>(buf, row, u, v);
+    } else {
+      load_half_row<D>(from_ring, u, v); // only with a window
+    }
   }
   uint32_t words[NW];
   __half sh, zh;

@@ -16,6 +16,16 @@ namespace kvq {
 
 constexpr float kMagicRound = 12582912.0f;  // 1.5 * 2^23: x + magic rounds x to an integer
 
+// The top stage on 8 bf16 pairs: v_k = lo_k + hi_k (sgn = 1) or lo_k - hi_k.
+__device__ __forceinline__ void top_stage8(const uint4& lo, const uint4& hi, float sgn, float* v) {
+  const uint32_t a[4] = {lo.x, lo.y, lo.z, lo.w}, b[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    v[2 * j] = __fmaf_rn(sgn, bf16lo(b[j]), bf16lo(a[j]));
+    v[2 * j + 1] = __fmaf_rn(sgn, bf16hi(b[j]), bf16hi(a[j]));
+  }
+}
+
 // Lane u (0 or 1) of a pair loads half u of a bf16 head vector (dims
 // [u D/2, (u+1) D/2)) as exact fp32; zeros when row is null.
 template <int D>
@@ -39,10 +49,28 @@ __device__ __forceinline__ void load_half_row(const uint16_t* row, int u, float 
   }
 }
 
+// Lane u of a pair loads dims [u D/2, (u+1) D/2) of the top Sylvester stage of
+// a bf16 head vector x whose Hadamard block is the whole vector: x_i + x_{i+D/2}
+// (u = 0) or x_i - x_{i+D/2} (u = 1), each rounded once to fp32.  The stages
+// of the transform commute, so this one comes first.  Both halves are read,
+// and no value crosses lanes.
+template <int D>
+__device__ __forceinline__ void load_row_top(const uint16_t* row, int u, float (&v)[D / 2]) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(row);
+  const float sgn = u ? -1.f : 1.f;
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) {
+    const uint4 lo = s4[i], hi = s4[D / 16 + i];
+    top_stage8(lo, hi, sgn, v + 8 * i);
+  }
+}
+
 // Rotates the vector held by the lane pair (lane ^ 1 is the partner; every
 // lane of the warp must call this) and quantizes it: this lane's packed codes
 // (half u of the row, D * BITS / 16 bytes as 32-bit words), and the pair's
-// fp16 scale and zero.
+// fp16 scale and zero.  When the block spans both halves (NB > D / 2) the
+// caller has applied the top stage already (load_row_top); the other stages
+// then stay inside the lane.
 template <int D, int NB, int BITS>
 __device__ __forceinline__ void rotate_quantize_half(float (&v)[D / 2], int u,
                                                      uint32_t (&words)[D * BITS / 64], __half& sh,
@@ -65,14 +93,6 @@ __device__ __forceinline__ void rotate_quantize_half(float (&v)[D / 2], int u,
 #pragma unroll
     for (int e = 0; e < E; e += 2) {
       if (!(e & hs)) addsub2(v[e], v[e + 1], v[e + hs], v[e + hs + 1]);
-    }
-  }
-  if constexpr (NB > E) {  // the block spans both lanes: lane 0 holds the lower half
-    const float sgn = u ? -1.f : 1.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const float o = __shfl_xor_sync(kFullMask, v[e], 1);
-      v[e] = __fmaf_rn(sgn, v[e], o);  // u = 0: a + b, u = 1: a - b
     }
   }
 
@@ -162,6 +182,18 @@ __device__ __forceinline__ void rotate_quantize_halfwarp(float (&v)[D / 16], int
                                                          __half& zh) {
   constexpr int F = D / 16;   // elements per lane
   const int lane = threadIdx.x & 31;
+  // a block of the whole vector takes its top stage (hs = D / 2, lanes l and
+  // l ^ 8) first, the order of the pair routine's load_row_top
+  constexpr int kTopM = D / 2 / F;
+  const bool top_first = nb == D;
+  if (top_first) {
+    const float sgn = (lane & kTopM) ? -1.f : 1.f;
+#pragma unroll
+    for (int e = 0; e < F; ++e) {
+      const float o = __shfl_xor_sync(kFullMask, v[e], kTopM);
+      v[e] = __fmaf_rn(sgn, v[e], o);   // lower: a + b, upper: a - b
+    }
+  }
   // butterflies inside the lane: stages hs < F
 #pragma unroll
   for (int hs = 1; hs < F; hs <<= 1) {
@@ -176,6 +208,7 @@ __device__ __forceinline__ void rotate_quantize_halfwarp(float (&v)[D / 16], int
   }
   // across lanes: stage hs = F m pairs lanes l and l ^ m (within the half)
   for (int m = 1; m * F < nb; m <<= 1) {
+    if (top_first && m == kTopM) break;   // done first
     const float sgn = (lane & m) ? -1.f : 1.f;
 #pragma unroll
     for (int e = 0; e < F; ++e) {
