@@ -253,6 +253,31 @@ def config_dict() -> dict:
 
 # ------------------------------------------------------------------------- GPU leg
 
+def init_distributed(world: int, local: int):
+    """One process per GPU (NCCL) for N > 1; gloo on a machine without CUDA."""
+    import torch
+    import torch.distributed as dist
+    if world <= 1:
+        return
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        dist.init_process_group("gloo")
+
+
+def max_over_ranks(value: float, world: int, dev) -> float:
+    """The largest of the ranks' values (a step time): one all-reduce of a
+    scalar, nothing on the data path."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_kvq(args) -> None:
     import torch
     import torch.distributed as dist
@@ -263,9 +288,7 @@ def run_kvq(args) -> None:
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    init_distributed(world, local)
     dev = torch.device("cuda", local if world > 1 else 0)
     if rank == 0 or world == 1:
         build.build()
@@ -348,12 +371,7 @@ def run_kvq(args) -> None:
         torch.cuda.synchronize(dev)
         if world > 1:
             dist.barrier()
-        ms = t0.elapsed_time(t1) / k_steps
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(t0.elapsed_time(t1) / k_steps, world, dev)
 
     for _ in range(args.warmup):
         with torch.cuda.stream(stream):
