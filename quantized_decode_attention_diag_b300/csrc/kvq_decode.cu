@@ -641,16 +641,15 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   uint64_t* bars = sm.bars + warp * NST;
   const uint8_t* head_base = p.pool + p.geom.head_off[h];
   const long long page_bytes = p.geom.page_bytes;
-  auto issue = [&](int slot, int pid) {  // lane 0 only; pid already validated
-    uint64_t* bar = bars + slot;
-    mbar_expect_tx(bar, CHUNK);
-    bulk_g2s(stages + slot * stage_bytes, head_base + pid * page_bytes, CHUNK, bar);
+  // lane 0 issues the copy of page `pid` (already validated) into `slot` when
+  // `go` (predicated, no branch)
+  const uint32_t bars0 = smem_u32(bars);
+  auto issue = [&](bool go, int slot, int pid) {
+    bulk_g2s_if(go && lane == 0, st0 + slot * stage_bytes, head_base + pid * page_bytes, CHUNK,
+                bars0 + 8u * slot);
   };
   // start streaming before the query prologue
-  for (int kk = 0; kk < nk && kk < NST; ++kk) {
-    const int pid = pid_of(kk);
-    if (lane == 0) issue(kk, pid);
-  }
+  for (int kk = 0; kk < nk && kk < NST; ++kk) issue(true, kk, pid_of(kk));
 
   // with programmatic dependent launch, everything above may overlap the
   // previous kernel; q and the new token are its results
@@ -839,8 +838,9 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   // full rounds: RP full pages each
   constexpr int RP = kDecodeRoundPages;
   for (; k + RP <= nfull;) {
-    bool ok = mbar_wait_bounded(bars + sa, ph);
-    if constexpr (RP == 2) ok = mbar_wait_bounded(bars + sa + 1, ph) & ok;
+    bool ok;
+    if constexpr (RP == 2) ok = mbar_wait2_bounded(bars + sa, ph);
+    else ok = mbar_wait_bounded(bars + sa, ph);
     if (!__all_sync(kFullMask, ok)) {
       timed_out = true;
       break;
@@ -850,10 +850,8 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     const int pid0 = pid_of(k + NST);
     const int pid1 = RP == 2 ? pid_of(k + NST + 1) : 0;
     __syncwarp();
-    if (lane == 0) {
-      if (k + NST < nk) issue(sa, pid0);
-      if (RP == 2 && k + NST + 1 < nk) issue(sa + 1, pid1);
-    }
+    issue(k + NST < nk, sa, pid0);
+    if constexpr (RP == 2) issue(k + NST + 1 < nk, sa + 1, pid1);
     k += RP;
     sa += RP;
     if (sa == NST) {

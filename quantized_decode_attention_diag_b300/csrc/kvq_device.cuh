@@ -90,6 +90,20 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
       : "memory");
 }
 
+// mbar_expect_tx + bulk_g2s by the lanes with `pred` set, as predicated
+// instructions (no branch, no reconvergence point in the caller's loop).
+__device__ __forceinline__ void bulk_g2s_if(bool pred, uint32_t dst, const void* src,
+                                            unsigned bytes, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %0, 0;\n\t"
+      "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], %2;\n\t"
+      "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%3], [%4], %2, [%1];\n\t"
+      "}" ::"r"(static_cast<unsigned>(pred)),
+      "r"(bar), "r"(bytes), "r"(dst), "l"(src)
+      : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
   uint32_t ok;
   asm volatile(
@@ -111,6 +125,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
     if (clock64() - t0 > (1ll << 31)) return false;
   }
   return true;
+}
+
+// Both of two consecutive barriers (bar, bar + 1) at phase `parity`: one
+// combined test on the fast path, then bounded waits on each.
+__device__ __forceinline__ bool mbar_wait2_bounded(uint64_t* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q, [%1 + 8], %2;\n\t"
+      "and.pred p, p, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  if (ok) return true;
+  const bool a = mbar_wait_bounded(bar, parity);
+  return mbar_wait_bounded(bar + 1, parity) && a;
 }
 
 // ------------------------------------------------------ tensor-core MMA ----
