@@ -107,11 +107,19 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.window = None   # (start, end) of the timed region, local wall clock
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples: $KVQ_CLOCKS_CSV (a path template with {rank}) or a temporary file
+        tmpl = os.environ.get("KVQ_CLOCKS_CSV")
+        if tmpl:
+            self.path = tmpl.format(rank=gpu_index)
+        else:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix=f"kvq_clocks_rank{gpu_index}_", suffix=".csv")
+            os.close(fd)
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            if os.path.dirname(self.path):
+                os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
