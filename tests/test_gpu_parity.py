@@ -270,3 +270,37 @@ def test_decode_large_value_scales():
     assert pr.gpu.get_status() == 0
     ref = attention.decode(pr.gpu_state(), 0, q.astype(np.float64), pt, lens)
     compare_outputs(o.cpu().numpy() / 512.0, ref / 512.0)
+
+
+def test_decode_overlapped_layers_match_ordinary_launches():
+    """kvq_decode_attn over several layers back to back with
+    KVQ_LAUNCH_OVERLAP (programmatic dependent launch): the same o, bit for
+    bit, as ordinary launches, and within tolerance of the oracle."""
+    # 16 sequences x 8 KV heads: 128 units, 4 splits each, merged in clusters;
+    # the static-entry test covers the ticket merge under overlap
+    L, hkv, d, g, bsz, t = 3, 8, 128, 4, 16, 900
+    mp = t // 16 + 1
+    pt = page_table(97, bsz, mp)
+    lens = np.array([t, 450, 17, 1, 899, 640, 333, 16] * 2, np.int32)
+    outs = []
+    for overlap in (False, True):
+        c = kvq.Cache(L, hkv, d, 64, np.full((L, hkv, 2), 4), bsz * mp, overlap=overlap)
+        for l in range(L):
+            k = kv_tokens(97, 2 * l, bsz, t, hkv, d, 4, 10.0, 50.0)
+            v = kv_tokens(97, 2 * l + 1, bsz, t, hkv, d, 4, 10.0, 50.0)
+            c.append(l, dev_bf16(k), dev_bf16(v), dev_i32(pt), dev_i32(np.zeros(bsz, np.int32)))
+        torch.cuda.synchronize()
+        qs = [queries(98, l, bsz, hkv * g, d, False) for l in range(L)]
+        ptd, lensd = dev_i32(pt), dev_i32(lens)
+        o = [c.decode(l, torch.from_numpy(qs[l]).cuda().to(torch.bfloat16), ptd, lensd)
+             for l in range(L)]
+        torch.cuda.synchronize()
+        assert c.get_status() == 0
+        outs.append([x.cpu().numpy() for x in o])
+        if overlap:
+            for l in (0, L - 1):
+                st = ocache.CacheState(d, 64, 0, c.bits, [c.pool_host(x) for x in range(L)], None)
+                ref = attention.decode(st, l, qs[l].astype(np.float64), pt, lens)
+                compare_outputs(outs[1][l], ref)
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)

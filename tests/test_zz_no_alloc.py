@@ -83,3 +83,27 @@ def test_static_workspace_rejects_oversized_decodes():
     assert "fixed" in kvq.kvq_last_error()
     torch.cuda.synchronize()
     assert (o == 0).all()                # nothing was launched
+
+
+def test_static_with_overlapped_launches():
+    """With KVQ_LAUNCH_OVERLAP the static entry point (scratch cleared by a
+    memset, then the decode) gives the result of an ordinary launch, bit for
+    bit, when calls follow each other on one stream."""
+    c, pt = _cache(4, 2000, seed=94)
+    bsz, hq, d = 4, 32, 128
+    q = torch.from_numpy(queries(94, 0, bsz, hq, d, False)).cuda().to(torch.bfloat16)
+    lens = torch.from_numpy(np.array([2000, 1, 777, 1600], np.int32)).cuda()
+    outs = []
+    for flags in (0, kvq.LAUNCH_OVERLAP):
+        c.desc.launch_flags = flags
+        o = [torch.full((bsz, hq, d), float("nan"), dtype=torch.float32, device="cuda")
+             for _ in range(3)]
+        for x in o:      # back to back: each call may overlap the previous kernel
+            kvq.kvq_decode_attn_static(c.desc, 0, q, False, pt, int(pt.shape[1]), lens, bsz,
+                                       hq, 0.0, x)
+        torch.cuda.synchronize()
+        assert c.get_status() == 0
+        assert torch.equal(o[0], o[1]) and torch.equal(o[1], o[2])
+        outs.append(o[0])
+    c.desc.launch_flags = 0
+    assert torch.equal(outs[0], outs[1])
