@@ -174,3 +174,29 @@ def test_distortion_host_checks_run_before_any_device_call():
     assert L.kvq_distortion(128, 128, 8, fake, 10, bad.ctypes.data, 2, fake, 0) == kvq.KVQ_EINVAL
     assert L.kvq_distortion(128, 128, 8, fake + 4, 10, w.ctypes.data, 3, fake, 0) == kvq.KVQ_EINVAL
     assert L.kvq_distortion(128, 128, 8, fake, 10, w.ctypes.data, 3, fake + 4, 0) == kvq.KVQ_EINVAL
+
+
+def test_descriptor_layout_matches_the_header(tmp_path):
+    """The binding's kvq_cache has the C struct's size and field offsets (a C
+    program compiled against include/kvq.h prints them)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [f for f, _ in kvq.kvq_cache._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text(
+        "#include <stddef.h>\n#include <stdio.h>\n#include \"kvq.h\"\n"
+        "int main(void) {\n"
+        '  printf("%zu\\n", sizeof(kvq_cache));\n'
+        + "".join(f'  printf("%zu\\n", offsetof(kvq_cache, {f}));\n' for f in fields)
+        + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True, capture_output=True)
+    out = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(kvq.kvq_cache)
+    for f, off in zip(fields, out[1:]):
+        assert getattr(kvq.kvq_cache, f).offset == off, f
