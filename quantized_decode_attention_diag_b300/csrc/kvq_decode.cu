@@ -793,7 +793,6 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
       if (tok_b + g + 8 >= lq) sb1 = -CUDART_INF_F;
     }
     const float m_loc = fmaxf(fmaxf(sa0, sa1), fmaxf(sb0, sb1));
-    if (__any_sync(kFullMask, m_loc > thr)) rescale(m_loc);
     const float2 va0 = lds_half2(sta + VSZ + 4 * g), va1 = lds_half2(sta + VSZ + 4 * g + 32);
     float2 vb0 = make_float2(0.f, 0.f), vb1 = vb0;
     if (has_b) {
@@ -812,9 +811,11 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
       ps[3] = p[3] * vb1.x;
     };
     probs();
-    // p s must fit fp16: a very large value scale takes the exact maximum
-    // (p <= 1, p s <= s) for this round
-    if (__any_sync(kFullMask, fmaxf(fmaxf(ps[0], ps[1]), fmaxf(ps[2], ps[3])) > kMaxPS)) {
+    // one vote: a score past the slack raises the maximum, and p s must fit
+    // fp16 (a very large value scale takes the exact maximum, p <= 1, p s <= s);
+    // either way this round's p are taken again with the raised maximum
+    const bool slow = m_loc > thr || fmaxf(fmaxf(ps[0], ps[1]), fmaxf(ps[2], ps[3])) > kMaxPS;
+    if (__any_sync(kFullMask, slow)) {
       rescale(m_loc);
       probs();
     }
@@ -839,9 +840,9 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   constexpr int RP = kDecodeRoundPages;
   for (; k + RP <= nfull;) {
     bool ok;
-    if constexpr (RP == 2) ok = mbar_wait2_bounded(bars + sa, ph);
-    else ok = mbar_wait_bounded(bars + sa, ph);
-    if (!__all_sync(kFullMask, ok)) {
+    if constexpr (RP == 2) ok = mbar_wait2_warp(bars + sa, ph);
+    else ok = __all_sync(kFullMask, mbar_wait_bounded(bars + sa, ph));
+    if (!ok) {
       timed_out = true;
       break;
     }

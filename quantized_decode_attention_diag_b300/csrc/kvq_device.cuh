@@ -127,9 +127,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
   return true;
 }
 
-// Both of two consecutive barriers (bar, bar + 1) at phase `parity`: one
-// combined test on the fast path, then bounded waits on each.
-__device__ __forceinline__ bool mbar_wait2_bounded(uint64_t* bar, unsigned parity) {
+// Both of two consecutive barriers (bar, bar + 1) at phase `parity`, for the
+// whole warp (every lane calls it; the result is warp-uniform): one combined
+// test and a vote on the fast path, then bounded waits on each barrier.
+__device__ __forceinline__ bool mbar_wait2_warp(uint64_t* bar, unsigned parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
@@ -140,9 +141,10 @@ __device__ __forceinline__ bool mbar_wait2_bounded(uint64_t* bar, unsigned parit
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
-  if (ok) return true;
+  if (__all_sync(0xffffffffu, ok != 0)) return true;
   const bool a = mbar_wait_bounded(bar, parity);
-  return mbar_wait_bounded(bar + 1, parity) && a;
+  const bool b = mbar_wait_bounded(bar + 1, parity);
+  return __all_sync(0xffffffffu, a && b);
 }
 
 // ------------------------------------------------------ tensor-core MMA ----
