@@ -33,6 +33,19 @@
 // accuracy.  Codes enter the MMA as exact fp16 integers; the scale and zero are
 // folded outside the MMA: score = s (q'' . c) + z sum(q''),
 // sum_t p_t deq(v_t) = sum_t (p_t s_t) c_t + sum_t p_t z_t.
+//
+// The online softmax raises its running maximum only when a score passes it by
+// more than a slack of 8 (log2 units) -- any maximum gives the same o = acc /
+// l -- and redoes a round with the exact maximum when p s would leave fp16.
+//
+// Decode step (p.step): the warp owning the page of the new token quantizes it
+// (the append's rule, bit for bit), writes it to the cache and patches its
+// staged copy of the page, which it processes in its last round.
+//
+// Launch overlap (p.overlap, programmatic dependent launch): every CTA lets the
+// next kernel launch at once; before griddepcontrol.wait a CTA reads only the
+// page table, the lengths and the pool and starts its first copies; q, the new
+// token and the window are read, and everything is written, after it.
 #include <math_constants.h>
 
 #include "kvq_quant.cuh"
