@@ -47,7 +47,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from workloads import (APPEND_BITS, APPEND_BLOCKS, APPEND_SWEEP, LLAMA3_8B_LAYER,  # noqa: E402
-                       kv_tokens, page_table, queries)
+                       LONG_CONTEXT, MIXED_32L, TINY, kv_tokens, page_table, queries,
+                       sensitivities)
 
 METRIC = "quantized-KV decode attention GB/s (% of HBM peak); append tokens/s"
 N_LAYERS = 32
@@ -221,7 +222,7 @@ def oracle_baseline(n_seqs: int = 4, repeats: int = 5) -> dict:
     o.step()
     sec = statistics.median([o.step() for _ in range(repeats)])
     return {"value": round(o.nbytes / sec / 1e9, 4), "unit": "GB/s", "cores": o.threads,
-            "kind": "oracle", "sample": o.describe(repeats)}
+            "host_cpus": os.cpu_count(), "kind": "oracle", "sample": o.describe(repeats)}
 
 
 def run_reference(args) -> None:
@@ -241,7 +242,8 @@ def run_reference(args) -> None:
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": o.threads,
-                         "kind": "oracle", "sample": o.describe(len(times))},
+                         "host_cpus": os.cpu_count(), "kind": "oracle",
+                         "sample": o.describe(len(times))},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -450,9 +452,27 @@ def run_kvq(args) -> None:
     h2d = q_h.numel() * 2 + knew_h.numel() * 2 + vnew_h.numel() * 2
     d2h = o_h.numel() * 4
 
+    del cache, ws, knew, vnew, q_all, o_all
+    torch.cuda.synchronize(dev)
     # append sweep: 8 sequences x 8192 new tokens into empty caches
     append = append_sweep(kvq, torch, dev) if not args.skip_append else None
     calib = calibration_bench(kvq, torch, dev) if not args.skip_append else None
+    mixed = long_ctx = qerr = None
+    if not args.skip_configs:
+        # the mixed-bits allocation takes (alpha, beta) from the calibration
+        if calib is not None:
+            alpha, beta = calib["_alpha"], calib["_beta"]
+        else:
+            alpha = np.ones(N_LAYERS * hkv * 2)
+            beta = np.full(N_LAYERS * hkv * 2, 4.0)
+        if N_LAYERS == MIXED_32L.num_layers:
+            mixed = mixed_bits_bench(kvq, torch, dev, alpha, beta, min(args.steps, 10),
+                                     args.warmup)
+        long_ctx = long_context_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
+        qerr = quant_error_report(kvq, torch, dev)
+    if calib is not None:
+        calib.pop("_alpha")
+        calib.pop("_beta")
 
     if rank != 0:
         if world > 1:
@@ -488,6 +508,9 @@ def run_kvq(args) -> None:
         "cpu_baseline": cpu,
         "append": append,
         "calibration": calib,
+        "mixed_bits": mixed,
+        "long_context": long_ctx,
+        "quant_error": qerr,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -566,7 +589,10 @@ def calibration_bench(kvq, torch, dev) -> dict:
     torch.cuda.synchronize(dev)
     sec = e0.elapsed_time(e1) / reps * 1e-3 / (2 * N_LAYERS)
     t0 = time.perf_counter()
-    mse = torch.stack(outs).cpu().numpy().reshape(-1, len(widths))
+    # call i = 2 layer + kv holds [head][width]: into the allocator's component
+    # order (layer * Hkv + head) * 2 + kv
+    mse = (torch.stack(outs).cpu().numpy().reshape(N_LAYERS, 2, hkv, len(widths))
+           .transpose(0, 2, 1, 3).reshape(-1, len(widths)))
     alpha, beta = kvq.kvq_fit_distortion(mse, widths)
     fit_s = time.perf_counter() - t0
     nbytes = T * hkv * d * 2
@@ -578,7 +604,252 @@ def calibration_bench(kvq, torch, dev) -> dict:
             "frac_of_hbm": round(nbytes / sec / 1e9 / pk["hbm_gbs"], 4),
             "bytes": "bf16 vectors read once per call",
             "fit_ms": round(fit_s * 1e3, 3),
-            "beta_range": [round(float(beta.min()), 3), round(float(beta.max()), 3)]}
+            "beta_range": [round(float(beta.min()), 3), round(float(beta.max()), 3)],
+            "_alpha": alpha, "_beta": beta}
+
+
+def graph_step_bench(torch, dev, cache, n_layers, knew, vnew, q_all, pt, after, o_all, ws,
+                     steps, warmup) -> tuple:
+    """Times one step of n_layers fused decode steps (one per layer cache),
+    captured once as a CUDA graph with layer-to-layer launch overlap, and the
+    same launches with events between them.  Returns (ms per step, average
+    isolated launch in ms)."""
+    stream = torch.cuda.Stream(device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True, external=True),
+           torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n_layers)]
+
+    def step():
+        for l in range(n_layers):
+            cache.decode_step(l, knew[l], vnew[l], q_all[l], pt, after, o=o_all[l], workspace=ws)
+
+    def step_events():
+        for l in range(n_layers):
+            ev[l][0].record()
+            cache.decode_step(l, knew[l], vnew[l], q_all[l], pt, after, o=o_all[l], workspace=ws)
+            ev[l][1].record()
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    graph_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_ev, stream=stream):
+        step_events()
+    for _ in range(warmup):
+        with torch.cuda.stream(stream):
+            graph.replay()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record()
+        for _ in range(steps):
+            graph.replay()
+        t1.record()
+    torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1) / steps
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            graph_ev.replay()
+    torch.cuda.synchronize(dev)
+    iso = statistics.mean(ev[l][0].elapsed_time(ev[l][1]) for l in range(n_layers))
+    assert cache.get_status() == 0, f"device status {cache.get_status():#x}"
+    return ms, iso
+
+
+def step_bytes_layer(bits_layer, bsz, ctx, hq, d, window=0, partial_floats=0) -> int:
+    """Algorithmic bytes of one layer's decode step: the quantized tokens'
+    codes and (s, z), the bf16 window, the new token (bf16 K/V read, one
+    vector per head quantized and written), q read, o written, page-table rows,
+    and split partials (written and read once) where the merge keeps them in
+    memory."""
+    lq = ctx - window
+    cache_b = bsz * lq * sum(unit_bytes(d, int(bk), int(bv)) for bk, bv in bits_layer)
+    win_b = bsz * window * len(bits_layer) * 2 * 2 * d
+    new_tok = bsz * sum(2 * 2 * d + d * (int(bk) + int(bv)) // 8 + 8 for bk, bv in bits_layer)
+    q_o = bsz * hq * d * (2 + 4)
+    ptab = bsz * ((ctx + 15) // 16) * 4
+    return cache_b + win_b + new_tok + q_o + ptab + 2 * 4 * partial_floats
+
+
+def _roofline(step_bytes, ms, n_layers, iso_ms, bytes_per_launch) -> dict:
+    pk = peaks()
+    achieved = step_bytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 2), "peak": pk["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+            "peak_source": pk["source"], "traffic": None,
+            "algorithmic_bytes_per_launch": int(bytes_per_launch),
+            "avg_launch_us": round(ms / n_layers * 1e3, 3),
+            "isolated_launch_us": round(iso_ms * 1e3, 3)}
+
+
+def mixed_bits_bench(kvq, torch, dev, alpha, beta, steps, warmup) -> dict:
+    """The mixed per-head bits workload: 32 layers x 8 KV heads, batch 64,
+    context 2048, 32 query heads, bits from the RateQuant greedy (sensitivities
+    lognormal x U-shape over depth, times alpha; beta per component from the
+    calibration section) at the stated 3-bit average (which leaves K4V2 on
+    every head) and at 3.5 bits.  One step = one fused decode step per layer,
+    each over its own cache (3.5-4.3 GB per step: far above L2).  Layer 0's
+    K/V streams fill every layer's cache (the values do not change the work)."""
+    w = MIXED_32L
+    L, hkv, hq, d, bsz, ctx = w.num_layers, w.hkv, w.hq, w.head_dim, w.batch, w.ctx
+    mp = ctx // 16
+    sens = sensitivities(w.seed, L, hkv).reshape(-1)
+    allowed = [kvq.mask_of([4, 8]), kvq.mask_of([2, 4])] * (L * hkv)
+    k = kv_tokens(w.seed, 0, bsz, ctx, hkv, d, w.k_outliers, w.outlier_lo, w.outlier_hi)
+    v = kv_tokens(w.seed, 1, bsz, ctx, hkv, d, w.v_outliers, w.outlier_lo, w.outlier_hi)
+    kd = torch.from_numpy(k).to(dev).to(torch.bfloat16)
+    vd = torch.from_numpy(v).to(dev).to(torch.bfloat16)
+    del k, v
+    kpre, vpre = kd[:, :ctx - 1].contiguous(), vd[:, :ctx - 1].contiguous()
+    knew = kd[:, ctx - 1].contiguous().unsqueeze(0).repeat(L, 1, 1, 1).contiguous()
+    vnew = vd[:, ctx - 1].contiguous().unsqueeze(0).repeat(L, 1, 1, 1).contiguous()
+    del kd, vd
+    pt = torch.from_numpy(page_table(w.seed, bsz, mp)).to(dev)
+    q_all = torch.from_numpy(np.stack([queries(w.seed, l, bsz, hq, d, False) for l in range(L)])
+                             ).to(dev).to(torch.bfloat16)
+    o_all = torch.empty((L, bsz, hq, d), dtype=torch.float32, device=dev)
+    zero = torch.zeros(bsz, dtype=torch.int32, device=dev)
+    after = torch.full((bsz,), ctx, dtype=torch.int32, device=dev)
+    out = {"workload": f"mixed per-head bits: {L} layers x {hkv} KV heads, {hq} q heads, "
+                       f"head_dim {d}, batch {bsz}, context {ctx}, Hadamard {w.had_block}",
+           "step": "per layer: kvq_decode_step over its own cache", "variants": []}
+    a = np.asarray(alpha, np.float64)
+    b = np.asarray(beta, np.float64)
+    for avg in (3.0, 3.5):
+        budget = int(round(avg * L * hkv * 2))
+        bits, left = kvq.kvq_alloc_bits(sens * a, b, budget, allowed)
+        bits = np.array(bits).reshape(L, hkv, 2)
+        cache = kvq.Cache(L, hkv, d, w.had_block, bits, bsz * mp, device=dev, overlap=True)
+        for l in range(L):
+            cache.append(l, kpre, vpre, pt, zero)
+        ws = cache.workspace(bsz, hq, mp)
+        torch.cuda.synchronize(dev)
+        ms, iso = graph_step_bench(torch, dev, cache, L, knew, vnew, q_all, pt, after, o_all, ws,
+                                   steps, warmup)
+        per_layer = [step_bytes_layer(bits[l], bsz, ctx, hq, d) for l in range(L)]
+        sb = sum(per_layer)
+        mix = {}
+        for bk, bv in bits.reshape(-1, 2):
+            key = f"K{bk}V{bv}"
+            mix[key] = mix.get(key, 0) + 1
+        out["variants"].append({
+            "avg_bits": avg, "budget_bits": budget, "leftover_bits": left, "heads_by_bits": mix,
+            "ms_per_step": round(ms, 4), "GB_per_step": round(sb / 1e9, 4),
+            "roofline": _roofline(sb, ms, L, iso, sb / L)})
+        del cache, ws
+        torch.cuda.synchronize(dev)
+    return out
+
+
+def long_context_bench(kvq, torch, dev, n_layers, steps, warmup) -> dict:
+    """Long context: one sequence of 131072 tokens, 32 query / 8 KV heads,
+    head_dim 128, K INT4 / V INT2 with Hadamard 128, the last 128 tokens kept
+    in a bf16 window.  One step = one fused decode step per layer over
+    n_layers distinct layer caches (109.5 MB each: together far above L2)."""
+    w = LONG_CONTEXT
+    hkv, hq, d, ctx, r = w.hkv, w.hq, w.head_dim, w.ctx, w.window
+    mp = ctx // 16
+    k = kv_tokens(w.seed, 0, 1, ctx, hkv, d, w.k_outliers, w.outlier_lo, w.outlier_hi)
+    v = kv_tokens(w.seed, 1, 1, ctx, hkv, d, w.v_outliers, w.outlier_lo, w.outlier_hi)
+    kd = torch.from_numpy(k).to(dev).to(torch.bfloat16)
+    vd = torch.from_numpy(v).to(dev).to(torch.bfloat16)
+    del k, v
+    bits = np.tile(np.array([w.k_bits, w.v_bits]), (n_layers, hkv, 1))
+    cache = kvq.Cache(n_layers, hkv, d, w.had_block, bits, mp, window=r, max_batch=1,
+                      device=dev, overlap=True)
+    pt = torch.from_numpy(page_table(w.seed, 1, mp)).to(dev)
+    zero = torch.zeros(1, dtype=torch.int32, device=dev)
+    kpre, vpre = kd[:, :ctx - 1].contiguous(), vd[:, :ctx - 1].contiguous()
+    for l in range(n_layers):
+        cache.append(l, kpre, vpre, pt, zero)
+    knew = kd[:, ctx - 1].contiguous().unsqueeze(0).repeat(n_layers, 1, 1, 1).contiguous()
+    vnew = vd[:, ctx - 1].contiguous().unsqueeze(0).repeat(n_layers, 1, 1, 1).contiguous()
+    del kd, vd, kpre, vpre
+    q_all = torch.from_numpy(np.stack([queries(w.seed, l, 1, hq, d, False)
+                                       for l in range(n_layers)])).to(dev).to(torch.bfloat16)
+    o_all = torch.empty((n_layers, 1, hq, d), dtype=torch.float32, device=dev)
+    after = torch.full((1,), ctx, dtype=torch.int32, device=dev)
+    ws = cache.workspace(1, hq, mp)
+    torch.cuda.synchronize(dev)
+    ms, iso = graph_step_bench(torch, dev, cache, n_layers, knew, vnew, q_all, pt, after, o_all,
+                               ws, steps, warmup)
+    # the split-K partials of the ticket merge: (workspace - tickets) floats
+    partial_floats = (ws.numel() - (hkv * 4 + 255) // 256 * 256) // 4
+    per = step_bytes_layer(bits[0], 1, ctx, hq, d, window=r, partial_floats=partial_floats)
+    sb = per * n_layers
+    del cache
+    return {"workload": f"long context: 1 sequence x {ctx} tokens, {hq} q / {hkv} KV heads, "
+                        f"head_dim {d}, K{w.k_bits}V{w.v_bits}, Hadamard {w.had_block}, "
+                        f"{r}-token bf16 window, {n_layers} layer caches",
+            "step": "per layer: kvq_decode_step (ticket merge over the splits)",
+            "ms_per_step": round(ms, 4), "GB_per_step": round(sb / 1e9, 4),
+            "roofline": _roofline(sb, ms, n_layers, iso, per)}
+
+
+def _exact_attention_torch(torch, q, k, v, scale):
+    """softmax(q k^T scale) v in float64 on the device for one KV head:
+    q [G, d], k/v [T, d] (bf16 values)."""
+    s = (q.double() @ k.double().T) * scale
+    return torch.softmax(s, dim=-1) @ v.double()
+
+
+def quant_error_report(kvq, torch, dev) -> dict:
+    """Error of the decode output over the quantized cache against attention
+    over the original bf16 K/V (float64, computed with torch on the device),
+    with the configuration's Hadamard block and with no rotation (block 1):
+    max / mean absolute difference, relative L2 and the L1 output perturbation
+    per query row (CriticalKV technical summary, Methodology)."""
+    out = {}
+    cases = [(TINY, 1, TINY.ctx, None), (LLAMA3_8B_LAYER, 2, LLAMA3_8B_LAYER.ctx, None),
+             (LONG_CONTEXT, 1, LONG_CONTEXT.ctx, [0, 3, 6])]
+    for w, bsz, n, heads in cases:
+        k = kv_tokens(w.seed, 0, bsz, n, w.hkv, w.head_dim, w.k_outliers, w.outlier_lo,
+                      w.outlier_hi)
+        v = kv_tokens(w.seed, 1, bsz, n, w.hkv, w.head_dim, w.v_outliers, w.outlier_lo,
+                      w.outlier_hi)
+        qn = queries(w.seed, 0, bsz, w.hq, w.head_dim, w.q_fp32)
+        kd = torch.from_numpy(k).to(dev).to(torch.bfloat16)
+        vd = torch.from_numpy(v).to(dev).to(torch.bfloat16)
+        del k, v
+        q = torch.from_numpy(qn).to(dev)
+        if not w.q_fp32:
+            q = q.to(torch.bfloat16)
+        mp = n // 16
+        pt = torch.from_numpy(page_table(w.seed, bsz, mp)).to(dev)
+        lens = torch.full((bsz,), n, dtype=torch.int32, device=dev)
+        g = w.hq // w.hkv
+        scale = 1.0 / np.sqrt(w.head_dim)
+        hs = heads if heads is not None else list(range(w.hkv))
+        ref = torch.stack([torch.stack([_exact_attention_torch(
+            torch, q[b, h * g:(h + 1) * g], kd[b, :, h], vd[b, :, h], scale) for h in hs])
+            for b in range(bsz)])
+        bits = np.tile(np.array([w.k_bits, w.v_bits]), (1, w.hkv, 1))
+        res = {}
+        for block in (w.had_block, 1):
+            c = kvq.Cache(1, w.hkv, w.head_dim, block, bits, bsz * mp, window=w.window,
+                          max_batch=bsz, device=dev)
+            c.append(0, kd, vd, pt, torch.zeros(bsz, dtype=torch.int32, device=dev))
+            o = c.decode(0, q, pt, lens)
+            torch.cuda.synchronize(dev)
+            assert c.get_status() == 0
+            got = torch.stack([torch.stack([o[b, h * g:(h + 1) * g].double() for h in hs])
+                               for b in range(bsz)])
+            diff = (got - ref)
+            rows = diff.shape[0] * diff.shape[1] * diff.shape[2]
+            res[f"block_{block}"] = {
+                "max_abs": round(float(diff.abs().max()), 6),
+                "mean_abs": round(float(diff.abs().mean()), 6),
+                "rel_l2": round(float(diff.norm() / ref.norm()), 6),
+                "l1_per_row": round(float(diff.abs().sum()) / rows, 4)}
+            del c
+        out[w.name] = {"bits": f"K{w.k_bits}V{w.v_bits}", "rows": f"{bsz} seqs x heads {hs}",
+                       **res}
+        del kd, vd
+    return {"reference": "float64 attention over the original bf16 K/V (torch, on the device)",
+            "configs": out}
 
 
 def main() -> None:
@@ -589,6 +860,8 @@ def main() -> None:
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-append", action="store_true")
+    ap.add_argument("--skip-configs", action="store_true",
+                    help="leave out the mixed-bits, long-context and quantization-error sections")
     ap.add_argument("--layers", type=int, default=32,
                     help="distinct layer caches per step (profiling uses a small case)")
     args = ap.parse_args()

@@ -83,7 +83,9 @@ typedef struct kvq_cache {
   int num_kv_heads;          /* Hkv, 1 .. 64 */
   int head_dim;              /* d: 64 or 128 */
   int page_size;             /* must be 16 */
-  int had_block;             /* Hadamard block n: 32, 64 or 128, dividing head_dim */
+  int had_block;             /* Hadamard block n: 32, 64 or 128, dividing head_dim;
+                                1 = no rotation (u = x), the plain token-wise quantizer
+                                that the SAW-INT4 page contrasts with the rotated one */
   int window;                /* R: bf16 recent-token window (0 = none), 0 .. 4096 */
   int max_batch;             /* sequences addressable in each window buffer */
   int num_pages;             /* physical pages in each layer pool */
@@ -257,7 +259,7 @@ kvq_status kvq_alloc_bits(const double* w, const double* beta, int n, long long 
  * actually used, on a small calibration set, per K and V component) and
  * section 4 (the fit takes 5 bit-widths).
  *
- *   head_dim, had_block  as in kvq_cache (64 | 128; 32 | 64 | 128 dividing it).
+ *   head_dim, had_block  as in kvq_cache (64 | 128; 1 | 32 | 64 | 128 dividing it).
  *   X        device bf16 [T][num_kv_heads][head_dim], 16-byte aligned: T vectors
  *            per head (e.g. a batch of calibration sequences, flattened).
  *   widths   host int [n_widths], each 1 .. 8; n_widths 1 .. 8.

@@ -92,3 +92,42 @@ def decode(state: CacheState, layer: int, q: np.ndarray, page_table: np.ndarray,
 def l1_perturbation(o: np.ndarray, o_hat: np.ndarray) -> float:
     """CriticalKV's output perturbation || o - o_hat ||_1 (summed over all rows)."""
     return float(np.abs(np.asarray(o, np.float64) - np.asarray(o_hat, np.float64)).sum())
+
+
+def exact_decode(q: np.ndarray, k: np.ndarray, v: np.ndarray, seq_lens: np.ndarray,
+                 scale: float | None = None, pairs: list | None = None) -> np.ndarray:
+    """Unquantized attention o[B, Hq, d] over the original K/V [B, T, Hkv, d]
+    (bf16 values widened exactly), the reference the quantization error is
+    measured against.  ``pairs`` as in ``decode``."""
+    q = np.asarray(q, dtype=np.float64)
+    bsz, hq, d = q.shape
+    hkv = k.shape[2]
+    g = hq // hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    o = np.full((bsz, hq, d), np.nan)
+    todo = pairs if pairs is not None else [(b, h) for b in range(bsz) for h in range(hkv)]
+    for b, h in todo:
+        n = int(seq_lens[b])
+        o[b, h * g:(h + 1) * g] = softmax_attention(q[b, h * g:(h + 1) * g], k[b, :n, h],
+                                                    v[b, :n, h], scale)
+    return o
+
+
+def quant_error(o_hat: np.ndarray, o_ref: np.ndarray) -> dict:
+    """Error of attention over the quantized cache (o_hat) against attention
+    over the unquantized K/V (o_ref), over the rows o_ref holds (not NaN):
+    max and mean absolute difference, the relative L2 norm of the difference
+    ||o_hat - o_ref||_2 / ||o_ref||_2, and CriticalKV's L1 perturbation
+    ||o_ref - o_hat||_1 per query row (the sum divided by the rows)."""
+    o_hat = np.asarray(o_hat, np.float64)
+    o_ref = np.asarray(o_ref, np.float64)
+    rows = ~np.isnan(o_ref).any(axis=-1)
+    a, r = o_hat[rows], o_ref[rows]
+    diff = a - r
+    n = int(rows.sum())
+    return {"max_abs": float(np.abs(diff).max()) if n else 0.0,
+            "mean_abs": float(np.abs(diff).mean()) if n else 0.0,
+            "rel_l2": float(np.linalg.norm(diff) / np.linalg.norm(r)) if n else 0.0,
+            "l1_per_row": l1_perturbation(r, a) / n if n else 0.0,
+            "rows": n}

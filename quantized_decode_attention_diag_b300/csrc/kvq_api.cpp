@@ -42,9 +42,9 @@ kvq_status check_geometry(const kvq_cache* c, int layer, kvq::LayerGeom* geom) {
     return fail(KVQ_EUNSUPPORTED, "head_dim %d not built (64 or 128)", c->head_dim);
   if (c->page_size != kvq::kPage)
     return fail(KVQ_EUNSUPPORTED, "page_size %d not built (16)", c->page_size);
-  if ((c->had_block != 32 && c->had_block != 64 && c->had_block != 128) ||
+  if ((c->had_block != 1 && c->had_block != 32 && c->had_block != 64 && c->had_block != 128) ||
       c->had_block > c->head_dim)
-    return fail(KVQ_EUNSUPPORTED, "Hadamard block %d not built for head_dim %d (32/64/128)",
+    return fail(KVQ_EUNSUPPORTED, "Hadamard block %d not built for head_dim %d (1/32/64/128)",
                 c->had_block, c->head_dim);
   if (c->window < 0 || c->window > kvq::kMaxWindow)
     return fail(KVQ_EUNSUPPORTED, "window %d outside [0, %d]", c->window, kvq::kMaxWindow);

@@ -309,9 +309,11 @@ cudaError_t launch_append(const AppendParams& p, int head_dim, int had_block, cu
     if (had_block == 128) return launch<128, 128>(p, s);
     if (had_block == 64) return launch<128, 64>(p, s);
     if (had_block == 32) return launch<128, 32>(p, s);
+    if (had_block == 1) return launch<128, 1>(p, s);
   } else if (head_dim == 64) {
     if (had_block == 64) return launch<64, 64>(p, s);
     if (had_block == 32) return launch<64, 32>(p, s);
+    if (had_block == 1) return launch<64, 1>(p, s);
   }
   return cudaErrorInvalidValue;
 }

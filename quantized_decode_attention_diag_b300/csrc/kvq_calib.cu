@@ -153,8 +153,10 @@ extern "C" kvq_status kvq_distortion(int head_dim, int had_block, int num_kv_hea
     std::snprintf(msg, sizeof msg, "kvq_distortion: head_dim %d not built (64, 128)", head_dim);
     return kvq::set_last_error(KVQ_EUNSUPPORTED, msg);
   }
-  if ((had_block != 32 && had_block != 64 && had_block != 128) || head_dim % had_block) {
-    std::snprintf(msg, sizeof msg, "kvq_distortion: had_block %d must be 32, 64 or 128 and divide %d",
+  if ((had_block != 1 && had_block != 32 && had_block != 64 && had_block != 128) ||
+      head_dim % had_block) {
+    std::snprintf(msg, sizeof msg,
+                  "kvq_distortion: had_block %d must be 1, 32, 64 or 128 and divide %d",
                   had_block, head_dim);
     return kvq::set_last_error(KVQ_EINVAL, msg);
   }

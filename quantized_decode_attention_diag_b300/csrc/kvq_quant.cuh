@@ -81,12 +81,15 @@ __device__ __forceinline__ void rotate_quantize_half(float (&v)[D / 2], int u,
   constexpr int CPW = 32 / BITS;           // codes per word
 
   // ---- Sylvester butterflies, natural order: stage hs pairs (i, i + hs)
+  // (NB == 1: no rotation, u = x)
   constexpr int IN_REG = NB < E ? NB : E;
+  if constexpr (NB >= 2) {
 #pragma unroll
-  for (int e = 0; e < E; e += 2) {  // hs = 1
-    const float a = v[e], c = v[e + 1];
-    v[e] = a + c;
-    v[e + 1] = a - c;
+    for (int e = 0; e < E; e += 2) {  // hs = 1
+      const float a = v[e], c = v[e + 1];
+      v[e] = a + c;
+      v[e + 1] = a - c;
+    }
   }
 #pragma unroll
   for (int hs = 2; hs < IN_REG; hs <<= 1) {
@@ -131,7 +134,10 @@ __device__ __forceinline__ void rotate_quantize_half(float (&v)[D / 2], int u,
 
   // ---- codes: round-half-even((u - z) * inv) via the magic-number add; the
   //      result's bits are 0x4B400000 + code, so the packed word is the sum of
-  //      the bit patterns shifted into place minus the shifted constants
+  //      the bit patterns shifted into place minus the shifted constants.
+  //      There is no clamp: z rounded down and s rounded up keep (u - z) * inv
+  //      within [0, M + 1/2), so every code lies in [0, M] (a CPU test drives
+  //      the same fp32 rule through extreme spans, subnormal scales included)
   constexpr uint32_t kMagicBits = 0x4B400000u;
   uint32_t ksum = 0;
 #pragma unroll

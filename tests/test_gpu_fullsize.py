@@ -4,11 +4,16 @@
   (Hadamard block, bits) pair; block 128 / 4 bits compared on every vector,
   the others on sampled (sequence, head, K|V) groups;
 * Llama-3-8B-shaped decode layer: batch 16, 32 q / 8 KV heads, context 4096,
-  K4 V4; sampled (sequence, KV head) pairs;
-* long context: batch 1, context 131072, K4 V2, 128-token bf16 window;
-  sampled KV heads;
-* mixed per-head bits from the RateQuant allocator: two of the 32 layers of
-  the batch-64 / context-2048 workload at full size.
+  K4 V4, through the fused decode step the benchmark times (4095 tokens
+  prefilled, the 4096th appended by the step); every KV head of sequence 0
+  and more sampled pairs under the cluster merge of the full batch, and one
+  sequence alone under the ticket merge;
+* long context: batch 1, context 131072, K4 V2, 128-token bf16 window; every
+  KV head;
+* mixed per-head bits: all 32 layers of the batch-64 / context-2048 workload,
+  streamed one layer at a time, bits from the RateQuant greedy with (alpha,
+  beta) per component calibrated on the GPU (kvq_distortion, kvq_fit_distortion),
+  both the stated 3-bit average (K4V2 everywhere) and the 3.5-bit variant.
 """
 import numpy as np
 import pytest
@@ -106,18 +111,30 @@ def test_decode_llama3_8b_layer_full_size():
     pt = page_table(w.seed, bsz, mp)
     bits = np.full((1, hkv, 2), 4)
     c = kvq.Cache(1, hkv, d, w.had_block, bits, bsz * mp)
-    _prefill(c, 0, k, v, pt, 1024)
+    _prefill(c, 0, k[:, :ctx - 1], v[:, :ctx - 1], pt, 1024)
     q = queries(w.seed, 0, bsz, w.hq, d, False)
     lens = np.full(bsz, ctx, np.int32)
-    o = c.decode(0, dev_bf16(q), dev_i32(pt), dev_i32(lens))
+    # the benchmark's launch: one fused decode step (token ctx - 1 appended)
+    # for the whole batch -- 4 splits per (sequence, KV head), cluster merge
+    o = c.decode_step(0, dev_bf16(k[:, ctx - 1]), dev_bf16(v[:, ctx - 1]), dev_bf16(q),
+                      dev_i32(pt), dev_i32(lens))
     torch.cuda.synchronize()
     assert c.get_status() == 0
-    pairs = [(0, 0), (3, 5), (7, 2), (11, 7), (15, 4), (9, 1)]
-    ref = attention.decode(gpu_state(c, bits), 0, q.astype(np.float64), pt, lens, pairs=pairs)
+    pairs = [(0, h) for h in range(hkv)] + [(3, 5), (7, 2), (11, 7), (15, 4), (9, 1)]
+    st = gpu_state(c, bits)
+    ref = attention.decode(st, 0, q.astype(np.float64), pt, lens, pairs=pairs)
     compare_outputs(o.cpu().numpy(), ref)
-    # codes of sampled whole sequences against the oracle quantizer
-    compare_written(c.pool_host(0), _written(k, v, [(2, 3, 0), (13, 6, 1)], w.had_block, bits[0]),
-                    pt, d, bits[0])
+    # one sequence alone: 32 splits per KV head, ticket merge
+    o9 = c.decode(0, dev_bf16(q[9:10]), dev_i32(pt[9:10]), dev_i32(lens[9:10]))
+    torch.cuda.synchronize()
+    assert c.get_status() == 0
+    ref9 = attention.decode(st, 0, q[9:10].astype(np.float64), pt[9:10], lens[9:10],
+                            pairs=[(0, h) for h in range(hkv)])
+    compare_outputs(o9.cpu().numpy(), ref9)
+    assert np.abs(o9.cpu().numpy()[0] - o.cpu().numpy()[9]).max() < 1e-4
+    # codes of sampled whole sequences (the step's token included) against the oracle
+    compare_written(c.pool_host(0), _written(k, v, [(2, 3, 0), (13, 6, 1), (0, 0, 0)],
+                                             w.had_block, bits[0]), pt, d, bits[0])
 
 
 def test_decode_long_context_full_size():
@@ -136,7 +153,8 @@ def test_decode_long_context_full_size():
     torch.cuda.synchronize()
     assert c.get_status() == 0
     st = gpu_state(c, bits)
-    ref = attention.decode(st, 0, q.astype(np.float64), pt, lens, pairs=[(0, 0), (0, 5)])
+    ref = attention.decode(st, 0, q.astype(np.float64), pt, lens,
+                           pairs=[(0, h) for h in range(hkv)])
     compare_outputs(o.cpu().numpy(), ref)
     # the window holds the last 128 tokens exactly
     for p in (ctx - r, ctx - 1):
@@ -146,31 +164,78 @@ def test_decode_long_context_full_size():
     compare_written(c.pool_host(0), grp, pt, d, bits[0])
 
 
-def test_mixed_bits_layers_full_size():
+def _calibrated_bits(w, avg_bits):
+    """Bits [L, Hkv, 2] for the mixed-bits workload: per (layer, K|V) the GPU
+    measures each head's quantization MSE at widths 2..6 on a calibration
+    sample (2 further sequences x 4096 tokens of the layer's own K/V streams:
+    same outlier channels, tokens not in the cache), fits (alpha, beta) per
+    component, and the greedy allocates sum(bits) <= avg_bits * 2 L Hkv with
+    K in {4, 8} and V in {2, 4} (RateQuant technical summary, Methodology
+    sections 1 and 3).  Returns the bits and (alpha, beta)."""
+    L, hkv, d = w.num_layers, w.hkv, w.head_dim
+    widths = [2, 3, 4, 5, 6]
+    mse = np.zeros((L, hkv, 2, len(widths)))
+    for l in range(L):
+        for kv in range(2):
+            x = kv_tokens(w.seed, 2 * l + kv, 2, 4096, hkv, d,
+                          w.k_outliers if kv == 0 else w.v_outliers, w.outlier_lo,
+                          w.outlier_hi, seq0=w.batch)
+            X = dev_bf16(x.reshape(-1, hkv, d))
+            mse[l, :, kv] = kvq.kvq_distortion(d, w.had_block, X, widths).cpu().numpy()
+    alpha, beta = kvq.kvq_fit_distortion(mse.reshape(-1, len(widths)), widths)
+    sens = sensitivities(w.seed, L, hkv).reshape(-1)
+    allowed = [[4, 8], [2, 4]] * (L * hkv)
+    out = {}
+    for avg in avg_bits:
+        budget = int(round(avg * L * hkv * 2))
+        bits, left = kvq.kvq_alloc_bits(sens * alpha, beta, budget,
+                                        [kvq.mask_of(a) for a in allowed])
+        want, wleft = allocator.greedy(sens * alpha, beta, budget, allowed)
+        assert bits == list(want) and left == wleft
+        out[avg] = np.array(bits).reshape(L, hkv, 2)
+    return out, alpha, beta
+
+
+def test_mixed_bits_all_layers_streamed():
+    """Every layer of the mixed-bits workload, one at a time (generated,
+    appended, decoded, checked, freed): the stated 3-bit average, which the
+    greedy can only meet with K4V2 everywhere, and the 3.5-bit variant with
+    real K8/V4 upgrades.  Each layer is prefilled with 2047 tokens and takes
+    its 2048th through the fused decode step, the launch the benchmark times."""
     w = MIXED_32L
     L, hkv, d, bsz, ctx = w.num_layers, w.hkv, w.head_dim, w.batch, w.ctx
-    wsens = sensitivities(w.seed, L, hkv).reshape(-1)
-    allowed = [[4, 8], [2, 4]] * (L * hkv)
-    bits, _ = kvq.kvq_alloc_bits(wsens, [4.0] * len(wsens), int(3.5 * L * hkv * 2),
-                                 [kvq.mask_of(a) for a in allowed])
-    bits = np.array(bits).reshape(L, hkv, 2)
-    assert len({tuple(x) for x in bits.reshape(-1, 2)}) > 1          # really mixed
-    layers = [0, 17]
-    sub = bits[layers]
+    allocs, alpha, beta = _calibrated_bits(w, (3.0, 3.5))
+    assert 3.0 < beta.min() and beta.max() < 6.0   # RateQuant prints 3.6 .. 5.3
+    assert np.all(allocs[3.0] == np.array([4, 2]))          # all-minimum allocation
+    mixed = allocs[3.5]
+    assert len({tuple(x) for x in mixed.reshape(-1, 2)}) > 1
     mp = ctx // 16
-    c = kvq.Cache(len(layers), hkv, d, w.had_block, sub, bsz * mp)
     q = queries(w.seed, 0, bsz, w.hq, d, False)
     lens = np.full(bsz, ctx, np.int32)
-    for li, layer in enumerate(layers):
+    rng = np.random.default_rng(1003)
+    for layer in range(L):
         k = kv_tokens(w.seed, 2 * layer, bsz, ctx, hkv, d, w.k_outliers, w.outlier_lo,
                       w.outlier_hi)
         v = kv_tokens(w.seed, 2 * layer + 1, bsz, ctx, hkv, d, w.v_outliers, w.outlier_lo,
                       w.outlier_hi)
+        kd, vd = dev_bf16(k), dev_bf16(v)
+        kpre, vpre = kd[:, :ctx - 1].contiguous(), vd[:, :ctx - 1].contiguous()
         pt = page_table(w.seed, bsz, mp, stream=layer)
-        _prefill(c, li, k, v, pt, 2048)
-        o = c.decode(li, dev_bf16(q), dev_i32(pt), dev_i32(lens))
-        torch.cuda.synchronize()
-        assert c.get_status() == 0
-        pairs = [(1, 0), (40, 3), (63, 7)]
-        ref = attention.decode(gpu_state(c, sub), li, q.astype(np.float64), pt, lens, pairs=pairs)
-        compare_outputs(o.cpu().numpy(), ref)
+        ptd = dev_i32(pt)
+        pairs = [(int(rng.integers(bsz)), int(rng.integers(hkv))) for _ in range(2)]
+        for avg, bits in allocs.items():
+            sub = bits[layer:layer + 1]
+            c = kvq.Cache(1, hkv, d, w.had_block, sub, bsz * mp)
+            c.append(0, kpre, vpre, ptd, dev_i32(np.zeros(bsz, np.int32)))
+            o = c.decode_step(0, kd[:, ctx - 1].contiguous(), vd[:, ctx - 1].contiguous(),
+                              dev_bf16(q), ptd, dev_i32(lens))
+            torch.cuda.synchronize()
+            assert c.get_status() == 0, (layer, avg)
+            ref = attention.decode(gpu_state(c, sub), 0, q.astype(np.float64), pt, lens,
+                                   pairs=pairs)
+            compare_outputs(o.cpu().numpy(), ref)
+            b, h = pairs[0]
+            compare_written(c.pool_host(0), _written(k, v, [(b, h, 0), (b, h, 1)], w.had_block,
+                                                     sub[0]), pt, d, sub[0])
+            del c
+        del kd, vd, kpre, vpre

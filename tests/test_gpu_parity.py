@@ -304,3 +304,36 @@ def test_decode_overlapped_layers_match_ordinary_launches():
                 compare_outputs(outs[1][l], ref)
     for a, b in zip(*outs):
         assert np.array_equal(a, b)
+
+
+def test_tiny_exact_config():
+    """The tiny correctness configuration exactly as stated: 1 layer, batch 1,
+    4 q = 4 KV heads, head_dim 64, context 256, fp32 q, K and V ~ N(0, 1) with 2
+    seeded outlier channels per head scaled x20, Hadamard block 64, K INT4 /
+    V INT2, page 16.  Codes and (s, z) end to end against the oracle's own
+    append of the same inputs; o against the oracle over the GPU-written cache."""
+    from workloads import TINY as w
+    k = kv_tokens(w.seed, 0, 1, w.ctx, w.hkv, w.head_dim, w.k_outliers, w.outlier_lo,
+                  w.outlier_hi)
+    v = kv_tokens(w.seed, 1, 1, w.ctx, w.hkv, w.head_dim, w.v_outliers, w.outlier_lo,
+                  w.outlier_hi)
+    assert w.outlier_lo == w.outlier_hi == 20.0 and w.k_outliers == w.v_outliers == 2
+    pt = page_table(w.seed, 1, w.ctx // 16)
+    pr = Pair(w.hkv, w.head_dim, w.had_block, (w.k_bits, w.v_bits), w.ctx // 16)
+    stats = pr.append(0, k, v, pt, np.zeros(1, np.int32))
+    assert stats["vectors"] == w.ctx * w.hkv * 2
+    q = queries(w.seed, 0, 1, w.hq, w.head_dim, True)
+    pr.decode_check(0, q, pt, np.array([w.ctx], np.int32), q_fp32=True)
+
+
+@pytest.mark.parametrize("bits", [(4, 2), (8, 4)])
+def test_no_rotation_block_1(bits):
+    """Hadamard block 1 (no rotation, u = x): append and decode against the
+    oracle, whose block-1 'rotation' is the identity matrix."""
+    pr, pt, k, v = _filled_pair(4, 128, 1, bits, [300, 45])
+    q = queries(68, 0, 2, 16, 128, False)
+    pr.decode_check(0, q, pt, np.array([300, 45], np.int32))
+    pr2 = Pair(4, 128, 1, bits, 40)
+    pt2 = page_table(69, 2, 20)
+    kk, vv = _kv(69, 2, 70, 4, 128)
+    pr2.append(0, kk, vv, pt2, np.array([0, 3], np.int32))

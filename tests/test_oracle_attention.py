@@ -120,3 +120,53 @@ def test_empty_sequence_gives_zeros():
     st, k, v, pt = _filled(1, 16, 1, 64, 64, (4, 4), window=0)
     o = attention.decode(st, 0, queries(1, 0, 1, 1, 64, True), pt, np.array([0]))
     assert np.array_equal(o, np.zeros_like(o))
+
+
+def test_exact_decode_equals_a_window_covering_everything():
+    """exact_decode is attention over the bf16 K/V themselves: the same as the
+    cache's attention when the bf16 window holds every token."""
+    st, k, v, pt = _filled(2, 37, 2, 64, 64, (4, 2), window=64)
+    q = queries(5, 2, 2, 4, 64, True)
+    lens = np.array([37, 20])
+    st2, _, _, _ = _filled(2, 37, 2, 64, 64, (4, 2), window=64)
+    want = attention.decode(st, 0, q, pt, np.array([37, 37]))
+    got = attention.exact_decode(q, k, v, np.array([37, 37]))
+    assert np.allclose(got, want, atol=1e-13)
+    part = attention.exact_decode(q, k, v, lens, pairs=[(1, 0)])
+    assert np.isnan(part[0]).all() and np.isnan(part[1, 2:]).all()
+    ref = attention.softmax_attention(q[1, :2], k[1, :20, 0], v[1, :20, 0], 1 / 8)
+    assert np.allclose(part[1, :2], ref, atol=1e-14)
+
+
+def test_quant_error_closed_form():
+    o_ref = np.array([[[3.0, 4.0], [np.nan, np.nan]], [[0.0, 1.0], [1.0, 0.0]]])
+    o_hat = np.array([[[3.0, 5.0], [9.0, 9.0]], [[-1.0, 1.0], [1.0, 0.0]]])
+    e = attention.quant_error(o_hat, o_ref)
+    assert e["rows"] == 3
+    assert e["max_abs"] == 1.0
+    assert abs(e["mean_abs"] - 2.0 / 6) < 1e-15
+    assert abs(e["rel_l2"] - np.sqrt(2.0) / np.sqrt(27.0)) < 1e-15
+    assert abs(e["l1_per_row"] - 2.0 / 3) < 1e-15
+    zero = attention.quant_error(o_ref, o_ref)
+    assert zero["max_abs"] == 0.0 and zero["rel_l2"] == 0.0
+
+
+def test_rotation_lowers_the_error_on_outlier_channels():
+    """SAW-INT4 page, sections 1-2: naive token-wise INT4 collapses when a few
+    channels carry large outliers, and the block-diagonal Hadamard rotation
+    spreads them.  The tiny configuration's data (2 channels x20 per head),
+    4-bit keys and 2-bit values, quantized with block 64 and with no rotation
+    (block 1, the identity)."""
+    n, d, hkv = 256, 64, 4
+    k = kv_tokens(1001, 0, 1, n, hkv, d, 2, 20.0, 20.0)
+    v = kv_tokens(1001, 1, 1, n, hkv, d, 2, 20.0, 20.0)
+    q = queries(1001, 0, 1, hkv, d, True)
+    pt = page_table(1001, 1, n // 16)
+    ref = attention.exact_decode(q, k, v, np.array([n]))
+    errs = {}
+    for block in (64, 1):
+        st = cache.new_state(1, n // 16, d, block, np.array([[[4, 2]] * hkv]))
+        cache.append(st, 0, k, v, pt, np.zeros(1, np.int32))
+        errs[block] = attention.quant_error(attention.decode(st, 0, q, pt, np.array([n])), ref)
+    assert errs[64]["rel_l2"] < errs[1]["rel_l2"]
+    assert errs[64]["mean_abs"] < errs[1]["mean_abs"]

@@ -117,13 +117,15 @@ def outlier_channels(seed: int, hkv: int, d: int, count: int, lo: float, hi: flo
 
 
 def kv_tokens(seed: int, stream: int, batch: int, tokens: int, hkv: int, d: int,
-              n_outliers: int, lo: float, hi: float, start: int = 0) -> np.ndarray:
+              n_outliers: int, lo: float, hi: float, start: int = 0,
+              seq0: int = 0) -> np.ndarray:
     """bf16-exact float32 K or V tokens, shape [batch, tokens, hkv, d].
 
     ``stream`` separates K (0) from V (1) and layers (2*layer + kv).  Token
     ``start`` offsets the draw so that a long sequence can be generated in
     chunks: the values of token t of sequence b do not depend on how the
-    sequence is chunked.
+    sequence is chunked.  The rows are sequences seq0 .. seq0 + batch - 1 of
+    the stream (same outlier channels, independent tokens).
     """
     out = np.empty((batch, tokens, hkv, d), dtype=np.float32)
     idx, fac = outlier_channels(seed, hkv, d, n_outliers, lo, hi, stream)
@@ -132,9 +134,11 @@ def kv_tokens(seed: int, stream: int, batch: int, tokens: int, hkv: int, d: int,
         t0 = start
         while t0 < start + tokens:
             t1 = min(start + tokens, (t0 // chunk + 1) * chunk)
-            rng = rng_for(seed, stream, b, t0 // chunk)
-            block = rng.standard_normal((chunk, hkv, d), dtype=np.float32)
-            block = block[t0 - (t0 // chunk) * chunk: t1 - (t0 // chunk) * chunk]
+            rng = rng_for(seed, stream, seq0 + b, t0 // chunk)
+            # the generator is sequential: drawing up to t1 gives the prefix of
+            # the whole chunk's draw
+            block = rng.standard_normal((t1 - (t0 // chunk) * chunk, hkv, d), dtype=np.float32)
+            block = block[t0 - (t0 // chunk) * chunk:]
             if n_outliers:
                 for h in range(hkv):
                     block[:, h, idx[h]] *= fac[h]
