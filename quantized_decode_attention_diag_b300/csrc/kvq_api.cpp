@@ -142,7 +142,8 @@ kvq_status plan_decode(const kvq_cache* c, const kvq::LayerGeom& g, int B, int m
     cache_val[0] = bps;
   }
   const long long units = static_cast<long long>(B) * c->num_kv_heads;
-  long long s = static_cast<long long>(sms) * bps / units;
+  // with a window, each unit's window CTA takes one of the wave's slots
+  long long s = static_cast<long long>(sms) * bps / units - (c->window > 0 ? 1 : 0);
   const long long cap = (max_pages + 7) / 8;
   if (s > cap) s = cap;
   if (s > kvq::decode_max_splits()) s = kvq::decode_max_splits();

@@ -925,44 +925,103 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
 }
 
 // ------------------------------------------------------------- window split
+// The bf16 window of (b, h): tokens at positions lq .. len - 1, in ring slots
+// p % R (the decode step's newest token comes from k_new / v_new: its slot is
+// being rewritten by this launch).  Attention is order-free, so the slots are
+// read in storage order.  Lane l holds dims [E l, E l + E) of a row; each warp
+// keeps UNROLL rows in flight (the kernel start has prefetched the window into
+// L2).
+//   1. scores: warp w takes tokens w, w + 4, ...; each lane forms its dims'
+//      partial dot products with the G query heads, and one transpose-reduce
+//      (6 shuffles) leaves head (2 [l >= 16] + [l & 8]) summed in each group of
+//      8 lanes;
+//   2. warp i: maximum and sum of head i, p = 2^(s - m) in place;
+//   3. values: warp w takes the same tokens, accumulates p v for every head
+//      in registers; the warps' sums meet in shared memory.
 template <int D>
 __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h, int len, int lq,
                              float* part) {
+  constexpr int E = D / 32;
+  constexpr int RW = E / 2;     // packed bf16 words of a row per lane
+  constexpr int UNROLL = 16;    // rows in flight per warp
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nw = len - lq;
   float* sc = reinterpret_cast<float*>(sm.area);   // [kMaxGroup][R]
   const int R = p.R;
   const uint16_t* kring = p.window + ((static_cast<size_t>(b) * p.Hkv + h) * 2 + 0) * R * D;
   const uint16_t* vring = kring + static_cast<size_t>(R) * D;
-  // decode step: the newest position (len - 1) is this launch's token, read
-  // from the input (its ring slot is being rewritten by this launch)
   const int tnew = p.step ? nw - 1 : -1;
   const uint16_t* knew = p.step ? p.k_new + (static_cast<size_t>(b) * p.Hkv + h) * D : nullptr;
   const uint16_t* vnew = p.step ? p.v_new + (static_cast<size_t>(b) * p.Hkv + h) * D : nullptr;
-  for (int t = tid; t < nw; t += kThreads) {
-    const uint4* kr = reinterpret_cast<const uint4*>(
-        t == tnew ? knew : kring + static_cast<size_t>((lq + t) % R) * D);
-    float acc[kMaxGroup] = {};
-    for (int i8 = 0; i8 < D / 8; ++i8) {
-      const uint4 w = kr[i8];
-      const float x[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
-                          bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+  auto row_of = [&](const uint16_t* ring, const uint16_t* fresh, int t) -> const uint16_t* {
+    return (t == tnew ? fresh : ring + static_cast<size_t>((lq + t) % R) * D) + E * lane;
+  };
+  auto load_row = [&](const uint16_t* src, uint32_t (&w)[RW]) {
+    if constexpr (E == 4) {
+      const uint2 x = *reinterpret_cast<const uint2*>(src);
+      w[0] = x.x;
+      w[1] = x.y;
+    } else {
+      w[0] = *reinterpret_cast<const uint32_t*>(src);
+    }
+  };
+  auto unpack = [&](const uint32_t (&w)[RW], float (&x)[E]) {
 #pragma unroll
-      for (int i = 0; i < kMaxGroup; ++i)
+    for (int i = 0; i < RW; ++i) {
+      x[2 * i] = bf16lo(w[i]);
+      x[2 * i + 1] = bf16hi(w[i]);
+    }
+  };
+  float qf[kMaxGroup][E];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[i] = __fmaf_rn(sm.qtab[i * D + 8 * i8 + e], x[e], acc[i]);
+  for (int i = 0; i < kMaxGroup; ++i)
+#pragma unroll
+    for (int e = 0; e < E; ++e) qf[i][e] = sm.qtab[i * D + E * lane + e];
+  const bool up = lane & 16, u8 = lane & 8;
+  const int hsel = (up ? 2 : 0) + (u8 ? 1 : 0);
+
+  // ---- 1. scores
+  for (int t0 = warp; t0 < nw; t0 += kDecodeWarps * UNROLL) {
+    uint32_t raw[UNROLL][RW];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int t = t0 + kDecodeWarps * u;
+      if (t < nw) load_row(row_of(kring, knew, t), raw[u]);
     }
 #pragma unroll
-    for (int i = 0; i < kMaxGroup; ++i) sc[i * R + t] = acc[i];
+    for (int u = 0; u < UNROLL; ++u) {
+      const int t = t0 + kDecodeWarps * u;
+      if (t >= nw) break;                       // warp-uniform
+      float x[E];
+      unpack(raw[u], x);
+      float a[kMaxGroup];
+#pragma unroll
+      for (int i = 0; i < kMaxGroup; ++i) {
+        a[i] = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) a[i] = __fmaf_rn(qf[i][e], x[e], a[i]);
+      }
+      // lanes < 16 keep heads 0, 1 and lanes >= 16 heads 2, 3; then bit 3
+      // picks one of the two; then a sum over the 8 lanes
+      const float r0 = __shfl_xor_sync(kFullMask, up ? a[0] : a[2], 16);
+      const float r1 = __shfl_xor_sync(kFullMask, up ? a[1] : a[3], 16);
+      const float k0 = (up ? a[2] : a[0]) + r0, k1 = (up ? a[3] : a[1]) + r1;
+      float vv = (u8 ? k1 : k0) + __shfl_xor_sync(kFullMask, u8 ? k0 : k1, 8);
+      vv += __shfl_xor_sync(kFullMask, vv, 4);
+      vv += __shfl_xor_sync(kFullMask, vv, 2);
+      vv += __shfl_xor_sync(kFullMask, vv, 1);
+      if ((lane & 7) == 0) sc[hsel * R + t] = vv;
+    }
   }
   __syncthreads();
-  if (warp < p.G) {  // warp i: softmax statistics of query head i
+  // ---- 2. softmax statistics of query head i (warp i)
+  if (warp < p.G) {
     float mm = -CUDART_INF_F;
     for (int t = lane; t < nw; t += 32) mm = fmaxf(mm, sc[warp * R + t]);
     mm = warp_max(mm);
     float ll = 0.f;
     for (int t = lane; t < nw; t += 32) {
-      const float e = exp2f(sc[warp * R + t] - mm);
+      const float e = ex2(sc[warp * R + t] - mm);
       sc[warp * R + t] = e;
       ll += e;
     }
@@ -973,14 +1032,44 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
     }
   }
   __syncthreads();
-  for (int idx = tid; idx < p.G * D; idx += kThreads) {
-    const int i = idx / D, d = idx - i * D;
-    float acc = 0.f;
-    for (int t = 0; t < nw; ++t) {
-      const uint16_t raw = t == tnew ? vnew[d] : vring[static_cast<size_t>((lq + t) % R) * D + d];
-      acc = __fmaf_rn(sc[i * R + t], __uint_as_float(static_cast<uint32_t>(raw) << 16), acc);
+  // ---- 3. values
+  float acc[kMaxGroup][E];
+#pragma unroll
+  for (int i = 0; i < kMaxGroup; ++i)
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[i][e] = 0.f;
+  for (int t0 = warp; t0 < nw; t0 += kDecodeWarps * UNROLL) {
+    uint32_t raw[UNROLL][RW];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int t = t0 + kDecodeWarps * u;
+      if (t < nw) load_row(row_of(vring, vnew, t), raw[u]);
     }
-    part_acc<D>(part, i)[d] = acc;
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int t = t0 + kDecodeWarps * u;
+      if (t >= nw) break;
+      float x[E];
+      unpack(raw[u], x);
+#pragma unroll
+      for (int i = 0; i < kMaxGroup; ++i) {
+        const float pi = i < p.G ? sc[i * R + t] : 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[i][e] = __fmaf_rn(pi, x[e], acc[i][e]);
+      }
+    }
+  }
+  float* macc = sm.merge;                       // [warps][kMaxGroup][D]
+#pragma unroll
+  for (int i = 0; i < kMaxGroup; ++i)
+#pragma unroll
+    for (int e = 0; e < E; ++e) macc[(warp * kMaxGroup + i) * D + E * lane + e] = acc[i][e];
+  __syncthreads();
+  for (int idx = tid; idx < kMaxGroup * D; idx += kThreads) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) sum += macc[w * kMaxGroup * D + idx];
+    part[idx] = sum;                            // part_acc<D>(part, i)[d], idx = i D + d
   }
   // decode step on a sequence no longer than the window: no token leaves the
   // ring, so nobody else writes the new token into it
@@ -1183,6 +1272,17 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
   __syncthreads();
 
   if (is_window) {
+    // the window's valid slots are a prefix of the ring (all R of them once
+    // the sequence is longer than the window): one bulk prefetch into L2 each
+    // for K and V, before the wait (a hint; L2 is coherent with the writes
+    // of the previous kernel)
+    if (tid == 0 && len > 0) {
+      const int nw = len - lq;
+      const uint16_t* kring = p.window + (static_cast<size_t>(b) * p.Hkv + h) * 2 * p.R * D;
+      const uint32_t bytes = static_cast<uint32_t>(nw) * D * 2;
+      l2_prefetch_bulk(kring, bytes);
+      l2_prefetch_bulk(kring + static_cast<size_t>(p.R) * D, bytes);
+    }
     grid_wait();
     if (p.overlap) load_query<D>(p, b, h, qv);
     query_window_prologue<D>(p, sm, qv);

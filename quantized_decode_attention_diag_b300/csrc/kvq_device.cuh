@@ -62,6 +62,12 @@ __device__ __forceinline__ void subfma2(float x0, float x1, float z, float inv, 
       : "f"(x0), "f"(x1), "f"(z), "f"(inv), "f"(c));
 }
 
+// Prefetch of `bytes` (a multiple of 16; 16-byte aligned address) into L2 by
+// the bulk-copy engine; a hint, nothing waits for it.
+__device__ __forceinline__ void l2_prefetch_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------ mbarrier + bulk ----
 __device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
