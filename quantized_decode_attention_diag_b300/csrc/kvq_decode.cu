@@ -157,32 +157,25 @@ __device__ __forceinline__ float2 lds_half2(uint32_t a) {
 // offset off afterwards would save that instruction, but the offset inflates
 // the fp32 partial sums of the MMA by up to ~100x, which costs too much score
 // precision on keys with large outlier channels.)
-// Pairs come out in the order whose dims kpair_dims() reports.
-template <int BITS, int NWORDS>
-__device__ __forceinline__ void kconv(const uint32_t* w, uint32_t* pr) {
-#pragma unroll
-  for (int i = 0; i < NWORDS; ++i) {
-    const uint32_t x = w[i];
-    if constexpr (BITS == 4) {
-      const uint32_t y = x >> 8;
-      pr[4 * i + 0] = h2_sub1024(lop_or_magic(x, 0x000f000fu));
-      pr[4 * i + 1] = h2_unscale<4>(lop_or_magic(x, 0x00f000f0u));
-      pr[4 * i + 2] = h2_sub1024(lop_or_magic(y, 0x000f000fu));
-      pr[4 * i + 3] = h2_unscale<4>(lop_or_magic(y, 0x00f000f0u));
-    } else if constexpr (BITS == 2) {
-      const uint32_t y = x >> 8;
-      pr[8 * i + 0] = h2_sub1024(lop_or_magic(x, 0x00030003u));
-      pr[8 * i + 1] = h2_unscale<2>(lop_or_magic(x, 0x000c000cu));
-      pr[8 * i + 2] = h2_unscale<4>(lop_or_magic(x, 0x00300030u));
-      pr[8 * i + 3] = h2_unscale<6>(lop_or_magic(x, 0x00c000c0u));
-      pr[8 * i + 4] = h2_sub1024(lop_or_magic(y, 0x00030003u));
-      pr[8 * i + 5] = h2_unscale<2>(lop_or_magic(y, 0x000c000cu));
-      pr[8 * i + 6] = h2_unscale<4>(lop_or_magic(y, 0x00300030u));
-      pr[8 * i + 7] = h2_unscale<6>(lop_or_magic(y, 0x00c000c0u));
-    } else {
-      pr[2 * i + 0] = h2_sub1024(__byte_perm(x, 0x64646464u, 0x4140));
-      pr[2 * i + 1] = h2_sub1024(__byte_perm(x, 0x64646464u, 0x4342));
+// K pair i: dims kpair_dims() of one token row (w: the lane's slice of it).
+// Each pair is formed right before the MMA that takes it.
+template <int BITS>
+__device__ __forceinline__ uint32_t kpair(const uint32_t* w, int i) {
+  if constexpr (BITS == 4) {
+    const uint32_t x = (i & 2) ? (w[i >> 2] >> 8) : w[i >> 2];
+    return (i & 1) ? h2_unscale<4>(lop_or_magic(x, 0x00f000f0u))
+                   : h2_sub1024(lop_or_magic(x, 0x000f000fu));
+  } else if constexpr (BITS == 2) {
+    const int k = i & 7;
+    const uint32_t x = (k & 4) ? (w[i >> 3] >> 8) : w[i >> 3];
+    switch (k & 3) {
+      case 0: return h2_sub1024(lop_or_magic(x, 0x00030003u));
+      case 1: return h2_unscale<2>(lop_or_magic(x, 0x000c000cu));
+      case 2: return h2_unscale<4>(lop_or_magic(x, 0x00300030u));
+      default: return h2_unscale<6>(lop_or_magic(x, 0x00c000c0u));
     }
+  } else {
+    return h2_sub1024(__byte_perm(w[i >> 1], 0x64646464u, (i & 1) ? 0x4342 : 0x4140));
   }
 }
 
@@ -204,49 +197,30 @@ __device__ __forceinline__ void kpair_dims(int c, int i, int& lo, int& hi) {
 }
 
 // ------------------------------------- V codes of two tokens -> fp16 pairs --
-// Pair i = dim i of the thread's slice, (token 1 in the low half, token 2 high).
-template <int BITS, int NWORDS>
-__device__ __forceinline__ void vconv(const uint32_t* w1, const uint32_t* w2, uint32_t* pr) {
-#pragma unroll
-  for (int i = 0; i < NWORDS; ++i) {
-    const uint32_t x1 = w1[i], x2 = w2[i];
-    if constexpr (BITS == 4) {
-      const uint32_t a = __byte_perm(x1, x2, 0x5410), a8 = a >> 8;
-      const uint32_t b = __byte_perm(x1, x2, 0x7632), b8 = b >> 8;
-      pr[8 * i + 0] = h2_sub1024(lop_or_magic(a, 0x000f000fu));
-      pr[8 * i + 1] = h2_unscale<4>(lop_or_magic(a, 0x00f000f0u));
-      pr[8 * i + 2] = h2_sub1024(lop_or_magic(a8, 0x000f000fu));
-      pr[8 * i + 3] = h2_unscale<4>(lop_or_magic(a8, 0x00f000f0u));
-      pr[8 * i + 4] = h2_sub1024(lop_or_magic(b, 0x000f000fu));
-      pr[8 * i + 5] = h2_unscale<4>(lop_or_magic(b, 0x00f000f0u));
-      pr[8 * i + 6] = h2_sub1024(lop_or_magic(b8, 0x000f000fu));
-      pr[8 * i + 7] = h2_unscale<4>(lop_or_magic(b8, 0x00f000f0u));
-    } else if constexpr (BITS == 2) {
-      // a word holds 16 dims; the 2-byte slice (head_dim 64) holds 8
-      const uint32_t a = __byte_perm(x1, x2, 0x5410), a8 = a >> 8;
-      pr[16 * i + 0] = h2_sub1024(lop_or_magic(a, 0x00030003u));
-      pr[16 * i + 1] = h2_unscale<2>(lop_or_magic(a, 0x000c000cu));
-      pr[16 * i + 2] = h2_unscale<4>(lop_or_magic(a, 0x00300030u));
-      pr[16 * i + 3] = h2_unscale<6>(lop_or_magic(a, 0x00c000c0u));
-      pr[16 * i + 4] = h2_sub1024(lop_or_magic(a8, 0x00030003u));
-      pr[16 * i + 5] = h2_unscale<2>(lop_or_magic(a8, 0x000c000cu));
-      pr[16 * i + 6] = h2_unscale<4>(lop_or_magic(a8, 0x00300030u));
-      pr[16 * i + 7] = h2_unscale<6>(lop_or_magic(a8, 0x00c000c0u));
-      const uint32_t b = __byte_perm(x1, x2, 0x7632), b8 = b >> 8;
-      pr[16 * i + 8] = h2_sub1024(lop_or_magic(b, 0x00030003u));
-      pr[16 * i + 9] = h2_unscale<2>(lop_or_magic(b, 0x000c000cu));
-      pr[16 * i + 10] = h2_unscale<4>(lop_or_magic(b, 0x00300030u));
-      pr[16 * i + 11] = h2_unscale<6>(lop_or_magic(b, 0x00c000c0u));
-      pr[16 * i + 12] = h2_sub1024(lop_or_magic(b8, 0x00030003u));
-      pr[16 * i + 13] = h2_unscale<2>(lop_or_magic(b8, 0x000c000cu));
-      pr[16 * i + 14] = h2_unscale<4>(lop_or_magic(b8, 0x00300030u));
-      pr[16 * i + 15] = h2_unscale<6>(lop_or_magic(b8, 0x00c000c0u));
-    } else {
-      pr[4 * i + 0] = h2_sub1024(lop_or_magic(__byte_perm(x1, x2, 0x4400), 0x00ff00ffu));
-      pr[4 * i + 1] = h2_sub1024(lop_or_magic(__byte_perm(x1, x2, 0x5511), 0x00ff00ffu));
-      pr[4 * i + 2] = h2_sub1024(lop_or_magic(__byte_perm(x1, x2, 0x6622), 0x00ff00ffu));
-      pr[4 * i + 3] = h2_sub1024(lop_or_magic(__byte_perm(x1, x2, 0x7733), 0x00ff00ffu));
+// V pair i: dim i of the lane's slice for two tokens (w1 in the low half, w2
+// high): the rows' bytes interleaved, then the same masks as for K.
+template <int BITS>
+__device__ __forceinline__ uint32_t vpair(const uint32_t* w1, const uint32_t* w2, int i) {
+  if constexpr (BITS == 4) {
+    const int k = i & 7;
+    const uint32_t ab = __byte_perm(w1[i >> 3], w2[i >> 3], (k & 4) ? 0x7632 : 0x5410);
+    const uint32_t x = (k & 2) ? (ab >> 8) : ab;
+    return (k & 1) ? h2_unscale<4>(lop_or_magic(x, 0x00f000f0u))
+                   : h2_sub1024(lop_or_magic(x, 0x000f000fu));
+  } else if constexpr (BITS == 2) {
+    // a word holds 16 dims; the 2-byte slice (head_dim 64) holds 8
+    const int k = i & 15;
+    const uint32_t ab = __byte_perm(w1[i >> 4], w2[i >> 4], (k & 8) ? 0x7632 : 0x5410);
+    const uint32_t x = (k & 4) ? (ab >> 8) : ab;
+    switch (k & 3) {
+      case 0: return h2_sub1024(lop_or_magic(x, 0x00030003u));
+      case 1: return h2_unscale<2>(lop_or_magic(x, 0x000c000cu));
+      case 2: return h2_unscale<4>(lop_or_magic(x, 0x00300030u));
+      default: return h2_unscale<6>(lop_or_magic(x, 0x00c000c0u));
     }
+  } else {
+    const uint32_t sel = 0x4400u + 0x1111u * static_cast<uint32_t>(i & 3);
+    return h2_sub1024(lop_or_magic(__byte_perm(w1[i >> 2], w2[i >> 2], sel), 0x00ff00ffu));
   }
 }
 
@@ -595,10 +569,9 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   constexpr int VSLICE = VB / 8;                 // bytes of a token row per dim group
   constexpr int KWORDS = KSLICE >= 4 ? KSLICE / 4 : 1;
   constexpr int VWORDS = VSLICE >= 4 ? VSLICE / 4 : 1;
-  // pairs vconv produces (>= 2 * NJ; only head_dim 64 with 2-bit values makes
-  // more than are used, from the zero upper half of a 2-byte slice)
-  constexpr int VPAIRS = (BV == 2 ? 16 : BV == 4 ? 8 : 4) * VWORDS;
-  static_assert(VPAIRS >= 2 * NJ, "value slice too small");
+  // pairs of the lane's V slice (>= 2 * NJ; only head_dim 64 with 2-bit values
+  // has more, from the zero upper half of a 2-byte slice)
+  static_assert((BV == 2 ? 16 : BV == 4 ? 8 : 4) * VWORDS >= 2 * NJ, "value slice too small");
   constexpr int NST = kDecodeStages;
   static_assert(NST % 2 == 0, "stages are consumed in pairs");
   constexpr uint32_t KSZ = kPage * (KB + VB);    // offset of the K (s, z) pairs
@@ -724,13 +697,11 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     lds_u32<KSLICE>(st + koff + 8 * KB, w1);
     const float2 k0 = lds_half2(st + KSZ + 4 * g);
     const float2 k1 = lds_half2(st + KSZ + 4 * g + 32);
-    uint32_t p0[2 * NJ], p1[2 * NJ];
-    kconv<BK, KWORDS>(w0, p0);
-    kconv<BK, KWORDS>(w1, p1);
     float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-      const uint32_t x[4] = {p0[2 * j], p1[2 * j], p0[2 * j + 1], p1[2 * j + 1]};
+      const uint32_t x[4] = {kpair<BK>(w0, 2 * j), kpair<BK>(w1, 2 * j),
+                             kpair<BK>(w0, 2 * j + 1), kpair<BK>(w1, 2 * j + 1)};
       mma_16816(a, x, bq[j][0], bq[j][1]);
     }
     sc0 = __fmaf_rn(k0.x, a[0] + a[1], k0.y * qs);
@@ -759,12 +730,10 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     lds_u32<VSLICE>(st + voff + VB, a1);
     lds_u32<VSLICE>(st + voff + 8 * VB, b0);
     lds_u32<VSLICE>(st + voff + 9 * VB, b1);
-    uint32_t pa[VPAIRS], pb[VPAIRS];
-    vconv<BV, VWORDS>(a0, a1, pa);
-    vconv<BV, VWORDS>(b0, b1, pb);
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-      const uint32_t x[4] = {pa[2 * j], pa[2 * j + 1], pb[2 * j], pb[2 * j + 1]};
+      const uint32_t x[4] = {vpair<BV>(a0, a1, 2 * j), vpair<BV>(a0, a1, 2 * j + 1),
+                             vpair<BV>(b0, b1, 2 * j), vpair<BV>(b0, b1, 2 * j + 1)};
       mma_16816(oacc[j], x, pb0, pb1);
     }
   };
