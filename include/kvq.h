@@ -211,13 +211,17 @@ kvq_status kvq_decode_step(const kvq_cache* cache, int layer, const void* K_new,
  * workspace and ws_bytes) with its scratch in a fixed device array of
  * KVQ_STATIC_WORKSPACE_BYTES owned by the library, which every GPU that loads
  * the library holds until the process exits.  It calls no allocating routine.
- *   - Its first call on a device looks up the array's device address (once per
- *     device, with that device current); make that first call before any
- *     stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress; the first such query on a device loads the
+ *     module there), so make the first call on a device before any stream
+ *     capture.  Looking it up each time keeps the call correct after a device
+ *     reset.
  *   - Every call shares the array and it keeps the last call's contents; the
  *     call clears the part that must start at zero (an async memset on
- *     `stream`) itself.  Calls whose work overlaps on the GPU (other streams,
- *     other host threads) race on the array: serialise them.
+ *     `stream`) itself.  That memset also orders the decode after the previous
+ *     kernel on the stream, so KVQ_LAUNCH_OVERLAP has no effect here.  Calls
+ *     whose work overlaps on the GPU (other streams, other host threads) race
+ *     on the array: serialise them.
  *   - Returns KVQ_EWORKSPACE, launching nothing, when the decode needs more
  *     scratch than KVQ_STATIC_WORKSPACE_BYTES (kvq_decode_workspace_bytes tells
  *     how much); use kvq_decode_attn with a workspace then.

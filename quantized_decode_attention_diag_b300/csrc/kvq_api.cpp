@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 
@@ -92,6 +93,21 @@ kvq_status check_cache(const kvq_cache* c, int layer, kvq::LayerGeom* geom) {
       return fail(KVQ_EINVAL, "window_bufs[%d] is not 16-byte aligned", layer);
   }
   return KVQ_OK;
+}
+
+// log2 of the cycles a decode's main loop waits for a page copy before it
+// reports KVQ_DEV_COPY_TIMEOUT: 31 (about a second), or the value of the
+// environment variable KVQ_DEBUG_COPY_WAIT_LOG2 (0 .. 31; read once), which
+// lets a test make the wait run out on copies that do complete.  A warp that
+// gives up still waits, with the full limit, for every copy it issued.
+int copy_wait_log2() {
+  static const int v = [] {
+    const char* e = std::getenv("KVQ_DEBUG_COPY_WAIT_LOG2");
+    if (!e || !*e) return 31;
+    const long x = std::strtol(e, nullptr, 10);
+    return x < 0 ? 0 : x > 31 ? 31 : static_cast<int>(x);
+  }();
+  return v;
 }
 
 int sm_count() {
@@ -230,6 +246,7 @@ kvq_status decode_impl(const kvq_cache* cache, int layer, const void* K_new, con
   p.cluster = pl.cluster;
   p.stage_bytes = pl.stage_bytes;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_log2 = copy_wait_log2();
   p.step = step ? 1 : 0;
   p.k_new = static_cast<const uint16_t*>(K_new);
   p.v_new = static_cast<const uint16_t*>(V_new);

@@ -634,8 +634,12 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     bulk_g2s_if(go && lane == 0, st0 + slot * stage_bytes, head_base + pid * page_bytes, CHUNK,
                 bars0 + 8u * slot);
   };
-  // start streaming before the query prologue
-  for (int kk = 0; kk < nk && kk < NST; ++kk) issue(true, kk, pid_of(kk));
+  // start streaming before the query prologue (with a shortened copy wait, a
+  // debugging aid, only right before the loop: the first waits then come
+  // sooner than any copy can land)
+  const bool debug_wait = p.wait_log2 < kWaitLimitLog2;
+  if (!debug_wait)
+    for (int kk = 0; kk < nk && kk < NST; ++kk) issue(true, kk, pid_of(kk));
 
   // with programmatic dependent launch, everything above may overlap the
   // previous kernel; q and the new token are its results
@@ -815,6 +819,8 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   // is this warp's last page); the final round takes the rest
   const int nfull = nk - ((last_partial || kpatch >= 0) ? 1 : 0);
 
+  if (debug_wait)
+    for (int kk = 0; kk < nk && kk < NST; ++kk) issue(true, kk, pid_of(kk));
   bool timed_out = false;
   int k = 0, sa = 0;
   unsigned ph = 0;
@@ -822,8 +828,8 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   constexpr int RP = kDecodeRoundPages;
   for (; k + RP <= nfull;) {
     bool ok;
-    if constexpr (RP == 2) ok = mbar_wait2_warp(bars + sa, ph);
-    else ok = __all_sync(kFullMask, mbar_wait_bounded(bars + sa, ph));
+    if constexpr (RP == 2) ok = mbar_wait2_warp(bars + sa, ph, p.wait_log2);
+    else ok = __all_sync(kFullMask, mbar_wait_bounded(bars + sa, ph, p.wait_log2));
     if (!ok) {
       timed_out = true;
       break;
@@ -850,8 +856,8 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   // the rest: at most RP pages, the last maybe partial
   if (!timed_out && k < nk) {
     const bool has_b = RP == 2 && k + 1 < nk;
-    bool ok = mbar_wait_bounded(bars + sa, ph);
-    if (has_b) ok = mbar_wait_bounded(bars + sa + 1, ph) && ok;
+    bool ok = mbar_wait_bounded(bars + sa, ph, p.wait_log2);
+    if (has_b) ok = mbar_wait_bounded(bars + sa + 1, ph, p.wait_log2) && ok;
     if (!__all_sync(kFullMask, ok)) {
       timed_out = true;
     } else {
@@ -862,7 +868,8 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   }
   if (timed_out) {
     if (lane == 0) flag_status(p.status, KVQ_DEV_COPY_TIMEOUT);
-    // drain the copies still in flight (pages k .. k + NST - 1)
+    // drain the copies still in flight (pages k .. k + NST - 1), with the full
+    // limit: none of them may land after the CTA has exited
     int s = sa;
     unsigned q = ph;
     for (int kk = k; kk < nk && kk < k + NST; ++kk) {

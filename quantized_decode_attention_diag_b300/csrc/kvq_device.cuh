@@ -122,13 +122,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar`, giving up after ~2^31 SM cycles (about a
-// second).  Returns false on timeout; the caller records it and drains.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
+// Wait for phase `parity` of `bar`, giving up after ~2^limit_log2 SM cycles
+// (2^31: about a second).  Returns false on timeout; the caller records it and
+// drains its copies with the full limit.
+// A shorter limit (a debugging aid) also polls with test_wait, which never
+// suspends the thread: try_wait may sleep until the phase completes, so a short
+// limit could never run out.
+constexpr int kWaitLimitLog2 = 31;
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity,
+                                                  int limit_log2 = kWaitLimitLog2) {
+  if (limit_log2 < kWaitLimitLog2) {
+    const long long t0 = clock64();
+    while (!mbar_test_wait(bar, parity)) {
+      if (clock64() - t0 > (1ll << limit_log2)) return false;
+    }
+    return true;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > (1ll << 31)) return false;
+    if (clock64() - t0 > (1ll << limit_log2)) return false;
   }
   return true;
 }
@@ -136,7 +160,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
 // Both of two consecutive barriers (bar, bar + 1) at phase `parity`, for the
 // whole warp (every lane calls it; the result is warp-uniform): one combined
 // test and a vote on the fast path, then bounded waits on each barrier.
-__device__ __forceinline__ bool mbar_wait2_warp(uint64_t* bar, unsigned parity) {
+__device__ __forceinline__ bool mbar_wait2_warp(uint64_t* bar, unsigned parity, int limit_log2) {
+  if (limit_log2 < kWaitLimitLog2) {   // debugging: polling only (see mbar_wait_bounded)
+    const bool a = mbar_wait_bounded(bar, parity, limit_log2);
+    const bool b = mbar_wait_bounded(bar + 1, parity, limit_log2);
+    return __all_sync(0xffffffffu, a && b);
+  }
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
@@ -148,8 +177,8 @@ __device__ __forceinline__ bool mbar_wait2_warp(uint64_t* bar, unsigned parity) 
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   if (__all_sync(0xffffffffu, ok != 0)) return true;
-  const bool a = mbar_wait_bounded(bar, parity);
-  const bool b = mbar_wait_bounded(bar + 1, parity);
+  const bool a = mbar_wait_bounded(bar, parity, limit_log2);
+  const bool b = mbar_wait_bounded(bar + 1, parity, limit_log2);
   return __all_sync(0xffffffffu, a && b);
 }
 

@@ -59,6 +59,8 @@ struct DecodeParams {
   const uint16_t* v_new;
   int stage_bytes;               // bytes of one pipeline stage buffer
   float scale_log2;              // softmax_scale * log2(e)
+  int wait_log2;                 // the main loop gives up on a page copy after
+                                 // ~2^wait_log2 cycles (31 unless debugging)
   LayerGeom geom;
 };
 

@@ -13,7 +13,6 @@
 #include <cuda_runtime_api.h>
 
 #include <cstdio>
-#include <mutex>
 
 #include "kvq.h"
 #include "kvq_internal.h"
@@ -25,27 +24,17 @@ namespace {
 // process exits.  All calls share them and they keep the last call's contents.
 static __device__ __align__(256) unsigned char kvq_static_workspace[KVQ_STATIC_WORKSPACE_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-void* g_workspace[kMaxDevices] = {nullptr};
-
 // Device address of kvq_static_workspace on the current device.  In host code
 // the array's name is only a stand-in for the symbol, not a device address; the
-// address comes from cudaGetSymbolAddress, once per device, with that device
-// current.
+// address comes from cudaGetSymbolAddress with the device current.  It is
+// looked up on every call (a host-side query once the module is loaded), so a
+// device reset or a re-created primary context, which may move the array,
+// cannot leave a stale pointer behind.
 cudaError_t workspace_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, kvq_static_workspace);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_workspace[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, kvq_static_workspace);
-    if (e != cudaSuccess) return e;
-    g_workspace[dev] = p;
-  }
-  *out = g_workspace[dev];
+  *out = p;
   return cudaSuccess;
 }
 
