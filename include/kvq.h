@@ -93,13 +93,47 @@ typedef struct kvq_cache {
   void* const* layer_pools;  /* host array [num_layers] of device pointers, each
                                 num_pages * kvq_page_bytes(layer) bytes, 16-byte aligned */
   void* const* window_bufs;  /* host array [num_layers] of device pointers to bf16
-                                [max_batch][Hkv][2][R][head_dim], or NULL when R == 0.
-                                Sequence b of a call uses row b; a call for a subset
-                                of a batch (e.g. a one-sequence prefill) passes a
-                                descriptor whose pointers are offset to its rows. */
+                                [max_batch][Hkv][2][R][head_dim] (window R > 0), or to the
+                                LogQuant reserve [max_batch][Hkv][2][kvq_logquant_rows(W)]
+                                [head_dim] (logquant_w = W > 0), kvq_window_bytes() bytes
+                                each; NULL when neither is used.  Sequence b of a call
+                                uses row b; a call for a subset of a batch (e.g. a
+                                one-sequence prefill) passes a descriptor whose pointers
+                                are offset to its rows. */
   int* status_dev;           /* device int, the sticky status word (may be NULL) */
   int launch_flags;          /* 0 or KVQ_LAUNCH_OVERLAP (decode calls only) */
+  int logquant_w;            /* 0, or W: LogQuant log-spaced full-precision tokens with
+                                base window W, a power of two in [2, 256]; needs window 0 */
 } kvq_cache;
+
+/*
+ * LogQuant mode (logquant_w = W > 0).  Follows "LogQuant: Log-Distributed
+ * 2-Bit Quantization of KV Cache with Superior Accuracy Preservation",
+ * Methodology section 2 (base window W, the newest tokens at full precision,
+ * older ones selected ever more sparsely, a 3W full-precision reserve whose
+ * older selections are halved as it fills) and section 4 (A V = A_P V_P).
+ * Every token is quantized into its page on arrival, as without a window.
+ * Besides, a set B of positions keeps its bf16 K and V in the reserve: every
+ * new token joins B; when |B| reaches 3W, of the oldest 2W members (by
+ * position) every other one stays, the first of each pair.  Decode attention
+ * uses the bf16 values for the members of B and the quantized ones for every
+ * other token.  B depends on the length alone (kvq_logquant_members lists it).
+ */
+
+/* Rows of one (sequence, KV head, K|V) plane of the LogQuant reserve for base
+ * window W: 3W ring rows and log2(W) + 1 level buffers of W / 2 rows; 0 when W
+ * is not a power of two in [2, 256]. */
+int kvq_logquant_rows(int w);
+
+/* The positions of B after n appends with base window W (host only), ascending,
+ * into positions[0 .. max) when positions is not NULL; returns |B|, or -1 when
+ * W is not a power of two in [2, 256] or n < 0. */
+long long kvq_logquant_members(long long n, int w, long long* positions, long long max);
+
+/* Bytes of window_bufs[layer] this descriptor needs (the bf16 window or the
+ * LogQuant reserve, for max_batch sequences); 0 when it needs none or on a bad
+ * descriptor. */
+size_t kvq_window_bytes(const kvq_cache* cache);
 
 /*
  * KVQ_LAUNCH_OVERLAP: decode launches (kvq_decode_attn, kvq_decode_attn_static,
@@ -137,8 +171,11 @@ size_t kvq_page_bytes(const kvq_cache* cache, int layer);
  * it is quantized into its page slot.  With R > 0, positions p < L - R (L the new
  * length) are quantized -- tokens leaving the window are read from the ring slot
  * p % R of window_bufs[layer] before it is overwritten -- and the last min(L, R)
- * positions are copied to the ring.  Two appends to one sequence must be
- * stream-ordered.  Returns KVQ_OK once the kernel is enqueued.
+ * positions are copied to the ring.  In LogQuant mode every token is quantized,
+ * and the members of B after the append get their bf16 rows in the reserve
+ * (one more launch first moves the older members that this append's halvings
+ * thin out of the reserve's ring).  Two appends to one sequence must be
+ * stream-ordered.  Returns KVQ_OK once the kernels are enqueued.
  */
 kvq_status kvq_append(const kvq_cache* cache, int layer, const void* K, const void* V,
                       const int32_t* page_table, int max_pages, const int32_t* seq_lens,
@@ -167,6 +204,8 @@ size_t kvq_decode_workspace_bytes(const kvq_cache* cache, int B, int Hq, int max
  *                gets o = 0.
  *   workspace    device, ws_bytes >= kvq_decode_workspace_bytes(cache, B, Hq,
  *                max_pages), 16-byte aligned, zero-filled before its first use.
+ * In LogQuant mode the quantized splits leave out the members of B and one more
+ * CTA per (sequence, KV head) attends over their bf16 rows in the reserve.
  * One kernel launch.  Returns KVQ_OK once enqueued.
  */
 kvq_status kvq_decode_attn(const kvq_cache* cache, int layer, const void* q, int q_is_fp32,
@@ -192,7 +231,9 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, int layer, const void* q, int
  * Position len - 1 of sequence b takes the new token.  Without a window it is
  * quantized into its page slot; with R > 0 it enters ring slot (len - 1) % R,
  * and the token it replaces (position len - 1 - R, if any) is quantized into
- * its page slot.  Two steps on one cache must be stream-ordered.  One kernel
+ * its page slot.  In LogQuant mode it is quantized into its page slot and its
+ * bf16 rows enter the reserve; when this token fills B to 3W, the halving's
+ * block moves from the reserve's ring to its level buffer in the same launch.  Two steps on one cache must be stream-ordered.  One kernel
  * launch.  Returns KVQ_OK once enqueued.
  */
 kvq_status kvq_decode_step(const kvq_cache* cache, int layer, const void* K_new,

@@ -56,6 +56,7 @@ class kvq_cache(ctypes.Structure):
         ("window_bufs", ctypes.POINTER(ctypes.c_void_p)),
         ("status_dev", ctypes.c_void_p),
         ("launch_flags", ctypes.c_int),
+        ("logquant_w", ctypes.c_int),
     ]
 
 
@@ -74,6 +75,9 @@ _SIGS = {
     "kvq_alloc_bits": (_I, [_P, _P, _I, _LL, _P, _P, _P]),
     "kvq_distortion": (_I, [_I, _I, _I, _P, _LL, _P, _I, _P, _P]),
     "kvq_fit_distortion": (_I, [_P, _P, _I, _I, _P, _P]),
+    "kvq_logquant_rows": (_I, [_I]),
+    "kvq_logquant_members": (_LL, [_LL, _I, _P, _LL]),
+    "kvq_window_bytes": (_SZ, [ctypes.POINTER(kvq_cache)]),
     "kvq_get_status": (_I, [ctypes.POINTER(kvq_cache), ctypes.POINTER(ctypes.c_int)]),
     "kvq_reset_status": (_I, [ctypes.POINTER(kvq_cache), _P]),
     "kvq_last_error": (ctypes.c_char_p, []),
@@ -237,6 +241,25 @@ def kvq_fit_distortion(mse, widths: Sequence[int]) -> tuple[np.ndarray, np.ndarr
     return alpha, beta
 
 
+def kvq_logquant_rows(w: int) -> int:
+    """Rows of one plane of the LogQuant reserve for base window w (0 if unsupported)."""
+    return int(lib().kvq_logquant_rows(int(w)))
+
+
+def kvq_logquant_members(n: int, w: int) -> np.ndarray:
+    """Positions kept at full precision after n appends with base window w."""
+    count = lib().kvq_logquant_members(int(n), int(w), None, 0)
+    if count < 0:
+        raise KvqError(KVQ_EINVAL, kvq_last_error())
+    out = np.zeros(max(count, 1), dtype=np.int64)
+    lib().kvq_logquant_members(int(n), int(w), out.ctypes.data, count)
+    return out[:count]
+
+
+def kvq_window_bytes(desc: kvq_cache) -> int:
+    return int(lib().kvq_window_bytes(ctypes.byref(desc)))
+
+
 def kvq_get_status(desc: kvq_cache) -> int:
     v = ctypes.c_int(0)
     st = lib().kvq_get_status(ctypes.byref(desc), ctypes.byref(v))
@@ -268,7 +291,7 @@ class Cache:
 
     def __init__(self, num_layers: int, num_kv_heads: int, head_dim: int, had_block: int,
                  bits, num_pages: int, window: int = 0, max_batch: int = 0, device="cuda",
-                 overlap: bool = False):
+                 overlap: bool = False, logquant_w: int = 0):
         import torch
         self.bits = np.ascontiguousarray(np.asarray(bits).reshape(num_layers, num_kv_heads, 2),
                                          dtype=np.int8)
@@ -279,6 +302,8 @@ class Cache:
         d = self.desc
         d.num_layers, d.num_kv_heads, d.head_dim, d.page_size = num_layers, num_kv_heads, head_dim, 16
         d.had_block, d.window, d.max_batch, d.num_pages = had_block, window, max_batch, num_pages
+        d.logquant_w = logquant_w
+        self.logquant_w = logquant_w
         d.bits_host = self.bits.ctypes.data_as(ctypes.POINTER(ctypes.c_int8))
         self.page_bytes = [kvq_page_bytes(d, l) for l in range(num_layers)]
         self.pools = [torch.zeros(num_pages * pb, dtype=torch.uint8, device=device)
@@ -287,8 +312,9 @@ class Cache:
         d.layer_pools = self._pool_ptrs
         self.windows = None
         self._win_ptrs = None
-        if window:
-            self.windows = [torch.zeros((max_batch, num_kv_heads, 2, window, head_dim),
+        if window or logquant_w:
+            rows = window if window else kvq_logquant_rows(logquant_w)
+            self.windows = [torch.zeros((max_batch, num_kv_heads, 2, rows, head_dim),
                                         dtype=torch.bfloat16, device=device)
                             for _ in range(num_layers)]
             self._win_ptrs = (ctypes.c_void_p * num_layers)(*[w.data_ptr() for w in self.windows])
@@ -318,7 +344,8 @@ class Cache:
     def _shifted(self, row: int) -> kvq_cache:
         """A copy of the descriptor whose window buffers start at window row `row`."""
         d = kvq_cache.from_buffer_copy(self.desc)
-        step = self.num_kv_heads * 2 * self.window * self.head_dim * 2
+        rows = self.window if self.window else kvq_logquant_rows(self.logquant_w)
+        step = self.num_kv_heads * 2 * rows * self.head_dim * 2
         self._tmp_win = (ctypes.c_void_p * self.num_layers)(
             *[w.data_ptr() + row * step for w in self.windows])
         d.window_bufs = self._tmp_win
@@ -385,6 +412,7 @@ __all__ = [
     "KvqError", "KvqLibraryMissing", "kvq_cache", "lib", "kvq_version", "kvq_last_error",
     "kvq_page_bytes", "kvq_append", "kvq_decode_workspace_bytes", "kvq_decode_attn",
     "kvq_decode_attn_static", "kvq_decode_step", "STATIC_WORKSPACE_BYTES",
-    "kvq_distortion", "kvq_fit_distortion",
+    "kvq_distortion", "kvq_fit_distortion", "kvq_logquant_rows", "kvq_logquant_members",
+    "kvq_window_bytes",
     "kvq_alloc_bits", "kvq_get_status", "kvq_reset_status", "mask_of", "Cache",
 ]

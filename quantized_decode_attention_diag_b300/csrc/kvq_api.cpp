@@ -12,6 +12,7 @@
 
 #include "kvq.h"
 #include "kvq_internal.h"
+#include "kvq_logquant.h"
 
 namespace {
 
@@ -49,6 +50,14 @@ kvq_status check_geometry(const kvq_cache* c, int layer, kvq::LayerGeom* geom) {
                 c->had_block, c->head_dim);
   if (c->window < 0 || c->window > kvq::kMaxWindow)
     return fail(KVQ_EUNSUPPORTED, "window %d outside [0, %d]", c->window, kvq::kMaxWindow);
+  if (c->logquant_w != 0) {
+    const int a = kvq::lq_log2(c->logquant_w);
+    if (a < 1 || c->logquant_w > 256)
+      return fail(KVQ_EUNSUPPORTED, "logquant_w %d is not a power of two in [2, 256]",
+                  c->logquant_w);
+    if (c->window != 0)
+      return fail(KVQ_EINVAL, "logquant_w %d needs window 0 (got %d)", c->logquant_w, c->window);
+  }
   if (c->num_pages < 1) return fail(KVQ_EINVAL, "num_pages must be >= 1");
   if (!c->bits_host) return fail(KVQ_EINVAL, "bits_host is NULL");
   kvq::LayerGeom local;
@@ -85,10 +94,12 @@ kvq_status check_cache(const kvq_cache* c, int layer, kvq::LayerGeom* geom) {
     return fail(KVQ_EINVAL, "layer_pools[%d] is NULL", layer);
   if (!aligned(c->layer_pools[layer], 16))
     return fail(KVQ_EINVAL, "layer_pools[%d] is not 16-byte aligned", layer);
-  if (c->window > 0) {
-    if (c->max_batch < 1) return fail(KVQ_EINVAL, "max_batch must be >= 1 with a window");
+  if (c->window > 0 || c->logquant_w > 0) {
+    if (c->max_batch < 1)
+      return fail(KVQ_EINVAL, "max_batch must be >= 1 with a window or a LogQuant reserve");
     if (!c->window_bufs || !c->window_bufs[layer])
-      return fail(KVQ_EINVAL, "window_bufs[%d] is NULL but window = %d", layer, c->window);
+      return fail(KVQ_EINVAL, "window_bufs[%d] is NULL but window = %d, logquant_w = %d", layer,
+                  c->window, c->logquant_w);
     if (!aligned(c->window_bufs[layer], 16))
       return fail(KVQ_EINVAL, "window_bufs[%d] is not 16-byte aligned", layer);
   }
@@ -139,14 +150,15 @@ kvq_status plan_decode(const kvq_cache* c, const kvq::LayerGeom& g, int B, int m
   std::memset(&probe, 0, sizeof probe);
   probe.stage_bytes = (g.max_head_bytes + 127) / 128 * 128;
   probe.R = c->window;
+  probe.lq_w = c->logquant_w;
   const size_t smem = kvq::decode_smem_bytes(probe, c->head_dim);
   static thread_local int cache_key[4] = {0, 0, 0, 0}, cache_val[4] = {0, 0, 0, 0};
-  const int key = static_cast<int>(smem) * 2 + (c->head_dim == 128);
+  const int key = (static_cast<int>(smem) * 2 + (c->head_dim == 128)) * 2 + (c->logquant_w > 0);
   int bps = 0;
   for (int i = 0; i < 4; ++i)
     if (cache_key[i] == key) bps = cache_val[i];
   if (!bps) {
-    bps = kvq::decode_blocks_per_sm(c->head_dim, smem);
+    bps = kvq::decode_blocks_per_sm(c->head_dim, smem, c->logquant_w > 0);
     if (bps <= 0)
       return fail(KVQ_ECUDA, "decode kernel cannot be resident with %zu bytes of shared memory",
                   smem);
@@ -158,8 +170,10 @@ kvq_status plan_decode(const kvq_cache* c, const kvq::LayerGeom& g, int B, int m
     cache_val[0] = bps;
   }
   const long long units = static_cast<long long>(B) * c->num_kv_heads;
-  // with a window, each unit's window CTA takes one of the wave's slots
-  long long s = static_cast<long long>(sms) * bps / units - (c->window > 0 ? 1 : 0);
+  // with a window (or a LogQuant reserve), each unit's window CTA takes one of
+  // the wave's slots
+  const int extra = (c->window > 0 || c->logquant_w > 0) ? 1 : 0;
+  long long s = static_cast<long long>(sms) * bps / units - extra;
   const long long cap = (max_pages + 7) / 8;
   if (s > cap) s = cap;
   if (s > kvq::decode_max_splits()) s = kvq::decode_max_splits();
@@ -168,7 +182,7 @@ kvq_status plan_decode(const kvq_cache* c, const kvq::LayerGeom& g, int B, int m
   pl->S = (max_pages + pps - 1) / pps;
   pl->pages_per_split = pps;
   pl->stage_bytes = probe.stage_bytes;
-  pl->NS = pl->S + (c->window > 0 ? 1 : 0);
+  pl->NS = pl->S + extra;
   pl->cluster = pl->NS <= kvq::decode_max_cluster() ? 1 : 0;
   pl->counter_bytes = (static_cast<size_t>(units) * 4 + 255) / 256 * 256;
   pl->bytes = pl->counter_bytes + static_cast<size_t>(units) * pl->NS * kvq::kMaxGroup *
@@ -210,7 +224,7 @@ kvq_status decode_impl(const kvq_cache* cache, int layer, const void* K_new, con
   const int G = Hq / hkv;
   if (G != 1 && G != 2 && G != 4)
     return fail(KVQ_EUNSUPPORTED, "GQA group %d not built (1, 2, 4)", G);
-  if (cache->window > 0 && B > cache->max_batch)
+  if ((cache->window > 0 || cache->logquant_w > 0) && B > cache->max_batch)
     return fail(KVQ_EINVAL, "B %d exceeds the window buffers' max_batch %d", B, cache->max_batch);
   if (!std::isfinite(softmax_scale) || softmax_scale < 0.f)
     return fail(KVQ_EINVAL, "softmax_scale must be finite and >= 0");
@@ -222,7 +236,9 @@ kvq_status decode_impl(const kvq_cache* cache, int layer, const void* K_new, con
   const float scale =
       softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cache->head_dim));
   p.pool = static_cast<const uint8_t*>(cache->layer_pools[layer]);
-  p.window = cache->window > 0 ? static_cast<const uint16_t*>(cache->window_bufs[layer]) : nullptr;
+  p.window = (cache->window > 0 || cache->logquant_w > 0)
+                 ? static_cast<const uint16_t*>(cache->window_bufs[layer])
+                 : nullptr;
   p.q = q;
   p.page_table = page_table;
   p.seq_lens = seq_lens;
@@ -237,6 +253,9 @@ kvq_status decode_impl(const kvq_cache* cache, int layer, const void* K_new, con
   p.Hkv = hkv;
   p.G = G;
   p.R = cache->window;
+  p.lq_w = cache->logquant_w;
+  p.lq_a = cache->logquant_w ? kvq::lq_log2(cache->logquant_w) : 0;
+  p.lq_rows = cache->logquant_w ? kvq::lq_rows(cache->logquant_w, p.lq_a) : 0;
   p.num_pages = cache->num_pages;
   p.had_block = cache->had_block;
   p.S = pl.S;
@@ -284,12 +303,14 @@ kvq_status kvq_append(const kvq_cache* cache, int layer, const void* K, const vo
   if (max_pages < 1) return fail(KVQ_EINVAL, "max_pages must be >= 1");
   if (static_cast<long long>(B) * T_new > (1ll << 28))
     return fail(KVQ_EINVAL, "B * T_new too large");
-  if (cache->window > 0 && B > cache->max_batch)
+  if ((cache->window > 0 || cache->logquant_w > 0) && B > cache->max_batch)
     return fail(KVQ_EINVAL, "B %d exceeds the window buffers' max_batch %d", B, cache->max_batch);
   p.K = static_cast<const uint16_t*>(K);
   p.V = static_cast<const uint16_t*>(V);
   p.pool = static_cast<uint8_t*>(cache->layer_pools[layer]);
-  p.window = cache->window > 0 ? static_cast<uint16_t*>(cache->window_bufs[layer]) : nullptr;
+  p.window = (cache->window > 0 || cache->logquant_w > 0)
+                 ? static_cast<uint16_t*>(cache->window_bufs[layer])
+                 : nullptr;
   p.page_table = page_table;
   p.seq_lens = seq_lens;
   p.status = cache->status_dev;
@@ -300,10 +321,47 @@ kvq_status kvq_append(const kvq_cache* cache, int layer, const void* K, const vo
   p.R = cache->window;
   p.num_pages = cache->num_pages;
   p.warps_per_group = static_cast<int>((static_cast<long long>(B) * T_new + 15) / 16);
-  const cudaError_t e = kvq::launch_append(p, cache->head_dim, cache->had_block,
-                                           static_cast<cudaStream_t>(stream));
+  p.lq_w = cache->logquant_w;
+  p.lq_a = cache->logquant_w ? kvq::lq_log2(cache->logquant_w) : 0;
+  p.lq_rows = cache->logquant_w ? kvq::lq_rows(cache->logquant_w, p.lq_a) : 0;
+  cudaError_t e = cudaSuccess;
+  if (p.lq_w) e = kvq::launch_lq_carry(p, cache->head_dim, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "LogQuant carry launch: %s", cudaGetErrorString(e));
+  e = kvq::launch_append(p, cache->head_dim, cache->had_block, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "append launch: %s", cudaGetErrorString(e));
   return KVQ_OK;
+}
+
+int kvq_logquant_rows(int w) {
+  const int a = kvq::lq_log2(w);
+  if (a < 1 || w > 256) return 0;
+  return kvq::lq_rows(w, a);
+}
+
+long long kvq_logquant_members(long long n, int w, long long* positions, long long max) {
+  const int a = kvq::lq_log2(w);
+  if (a < 1 || w > 256 || n < 0) {
+    fail(KVQ_EINVAL, "kvq_logquant_members: w %d must be a power of two in [2, 256], n >= 0", w);
+    return -1;
+  }
+  long long count = 0;
+  for (long long p = 0; p < n; ++p) {
+    if (!kvq::lq_member(p, n, w, a)) continue;
+    if (positions && count < max) positions[count] = p;
+    ++count;
+  }
+  return count;
+}
+
+size_t kvq_window_bytes(const kvq_cache* cache) {
+  if (check_geometry(cache, 0, nullptr) != KVQ_OK) return 0;
+  if (cache->max_batch < 1) return 0;
+  const size_t per_row = static_cast<size_t>(cache->head_dim) * 2;   // bf16
+  const size_t planes = static_cast<size_t>(cache->max_batch) * cache->num_kv_heads * 2;
+  if (cache->logquant_w > 0)
+    return planes * static_cast<size_t>(kvq_logquant_rows(cache->logquant_w)) * per_row;
+  if (cache->window > 0) return planes * static_cast<size_t>(cache->window) * per_row;
+  return 0;
 }
 
 size_t kvq_decode_workspace_bytes(const kvq_cache* cache, int B, int Hq, int max_pages) {

@@ -21,6 +21,7 @@
 // 16-byte stores.
 #include <climits>
 
+#include "kvq_logquant.h"
 #include "kvq_quant.cuh"
 
 namespace kvq {
@@ -169,6 +170,13 @@ __device__ __forceinline__ void append_chunk(const AppendParams& p, const RowRef
       }
     }
   }
+  // LogQuant mode (R = 0 here, every token quantized): a member of B after the
+  // append keeps its bf16 row in the reserve (`window`)
+  uint16_t* lq_dst = nullptr;
+  if (active && p.lq_w && lq_member(pos, len, p.lq_w, p.lq_a)) {
+    lq_dst = p.window + ((static_cast<size_t>(b) * p.Hkv + h) * 2 + kv) * p.lq_rows * D +
+             static_cast<size_t>(lq_row(pos, len, p.lq_w, p.lq_a)) * D;
+  }
   uint8_t* seg = nullptr;
   if (dst >= 0) {
     if (pid < 0 || pid >= p.num_pages) {
@@ -214,9 +222,11 @@ __device__ __forceinline__ void append_chunk(const AppendParams& p, const RowRef
       flag_status(p.status, KVQ_DEV_NONFINITE);
   }
 
-  // ---- copy the new token into its ring slot (after the old one was read)
-  if (ring_slot != nullptr) {
-    uint4* d4 = reinterpret_cast<uint4*>(ring_slot) + u * (D / 16);
+  // ---- copy the new token into its ring slot (after the old one was read),
+  //      or into its LogQuant reserve row
+  uint16_t* row_dst = ring_slot != nullptr ? ring_slot : lq_dst;
+  if (row_dst != nullptr) {
+    uint4* d4 = reinterpret_cast<uint4*>(row_dst) + u * (D / 16);
 #pragma unroll
     for (int i = 0; i < D / 16; ++i) d4[i] = buf[row * (D / 8) + swz<D>(row, u * (D / 16) + i)];
   }
@@ -268,6 +278,44 @@ __global__ void __launch_bounds__(kAppendWarps * 32, 2)
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// LogQuant carry, one CTA per (sequence, KV head): the halvings this append
+// performs (k0 .. k1 - 1, from the lengths before and after) each thin a block
+// for the first time; that block's even positions still in the reserve's ring
+// -- those older than this append -- move to the block's level buffer (the
+// append itself writes the rows of its own tokens where they end up).  Blocks
+// halved away again before the end are skipped; the first halving also moves
+// block 0.  Copying a few positions the later halvings drop is harmless.
+template <int D>
+__global__ void __launch_bounds__(128) lq_carry_kernel(const __grid_constant__ AppendParams p) {
+  const int b = blockIdx.x, h = blockIdx.y;
+  const int l0 = __ldg(p.seq_lens + b);
+  if (l0 < 0 || static_cast<long long>(l0) + p.T > static_cast<long long>(p.max_pages) * kPage)
+    return;                                    // the append reports the bad length
+  const int w = p.lq_w, a = p.lq_a, half = w / 2;
+  const long long n = static_cast<long long>(l0) + p.T;
+  const int k0 = lq_halvings(l0, w), k1 = lq_halvings(n, w);
+  if (k1 == k0) return;
+  constexpr int C = D / 8;                     // uint4 chunks per row
+  for (int kv = 0; kv < 2; ++kv) {
+    uint16_t* plane = p.window + ((static_cast<size_t>(b) * p.Hkv + h) * 2 + kv) * p.lq_rows * D;
+    for (int i = max(k0, k1 - a); i < k1; ++i) {
+      const int blk = 1 + i;                   // alive at the end: blk > k1 - a
+      for (int pass = 0; pass < (i == 0 ? 2 : 1); ++pass) {
+        const int bb = pass ? 0 : blk;         // the first halving moves block 0 too
+        const int level = bb == 0 ? a : bb % a;
+        for (int idx = threadIdx.x; idx < half * C; idx += blockDim.x) {
+          const int v = idx / C, ci = idx - v * C;
+          const long long q = static_cast<long long>(bb) * w + 2 * v;
+          if (q >= l0) continue;               // a token of this append
+          const uint4* src = reinterpret_cast<const uint4*>(plane + (q % (3ll * w)) * D) + ci;
+          uint4* dst = reinterpret_cast<uint4*>(plane + (3 * w + level * half + v) * D) + ci;
+          *dst = *src;
+        }
+      }
+    }
+  }
+}
+
 int sm_count_cached() {
   static int cached[64] = {0};
   int dev = 0;
@@ -303,6 +351,14 @@ cudaError_t launch(const AppendParams& p, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_lq_carry(const AppendParams& p, int head_dim, cudaStream_t s) {
+  const dim3 grid(p.B, p.Hkv);
+  if (head_dim == 128) lq_carry_kernel<128><<<grid, 128, 0, s>>>(p);
+  else if (head_dim == 64) lq_carry_kernel<64><<<grid, 128, 0, s>>>(p);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_append(const AppendParams& p, int head_dim, int had_block, cudaStream_t s) {
   if (head_dim == 128) {

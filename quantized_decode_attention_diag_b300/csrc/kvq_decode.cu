@@ -48,6 +48,7 @@
 // token and the window are read, and everything is written, after it.
 #include <math_constants.h>
 
+#include "kvq_logquant.h"
 #include "kvq_quant.cuh"
 
 namespace kvq {
@@ -558,7 +559,9 @@ __device__ __forceinline__ void patch_stage(uint32_t st, const uint8_t* pbuf, in
 
 // One split of one (sequence, KV head): pages [split * pps, (split + 1) * pps)
 // of the quantized part; warp w takes pages w, w + 4, ... two at a time.
-template <int D, int BK, int BV>
+// LQ: LogQuant mode -- the members of B (full precision, attended by the
+// reserve split) are left out here, on the rounds whose pages can hold one.
+template <int D, int BK, int BV, bool LQ>
 __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h, int split,
                             int lq, float (&qv)[D / 32], int chunk0, uint32_t (&tok)[D / 32]) {
   constexpr int KB = D * BK / 8;                 // K code bytes per token
@@ -764,8 +767,14 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
       thr = mnew + slack;
     }
   };
+  // tokens a masked round leaves out: at or beyond lq (only the last page of a
+  // sequence has any) and, in LogQuant mode, the members of B (lq = len then)
+  const int lq_w = LQ ? p.lq_w : 0, lq_a = LQ ? p.lq_a : 0;
+  auto excluded = [&](int t) -> bool {
+    return t >= lq || (LQ && lq_member(t, lq, lq_w, lq_a));
+  };
   // one round: pages A (stage at sta) and, if has_b, B (the next stage); mask
-  // hides the tokens at or beyond lq (only the last page of a sequence has any)
+  // applies excluded() to its tokens
   auto round = [&](uint32_t sta, bool has_b, bool mask, int tok_a) {
     const uint32_t stb = sta + stage_bytes;
     float sa0, sa1, sb0 = -CUDART_INF_F, sb1 = -CUDART_INF_F;
@@ -773,10 +782,10 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     if (has_b) scores(stb, sb0, sb1);
     if (mask) {
       const int tok_b = tok_a + kDecodeWarps * kPage;
-      if (tok_a + g >= lq) sa0 = -CUDART_INF_F;
-      if (tok_a + g + 8 >= lq) sa1 = -CUDART_INF_F;
-      if (tok_b + g >= lq) sb0 = -CUDART_INF_F;
-      if (tok_b + g + 8 >= lq) sb1 = -CUDART_INF_F;
+      if (excluded(tok_a + g)) sa0 = -CUDART_INF_F;
+      if (excluded(tok_a + g + 8)) sa1 = -CUDART_INF_F;
+      if (excluded(tok_b + g)) sb0 = -CUDART_INF_F;
+      if (excluded(tok_b + g + 8)) sb1 = -CUDART_INF_F;
     }
     const float m_loc = fmaxf(fmaxf(sa0, sa1), fmaxf(sb0, sb1));
     const float2 va0 = lds_half2(sta + VSZ + 4 * g), va1 = lds_half2(sta + VSZ + 4 * g + 32);
@@ -812,6 +821,7 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     if (has_b) pv(stb, pb0, pb1);
   };
 
+  const int lq_from = LQ ? lq_lo(lq, lq_w, lq_a) : 0;
   // the last page of the sequence is partial unless lq is a multiple of 16
   const bool last_partial = (lq % kPage) != 0 && nk > 0 &&
                             first + kDecodeWarps * (nk - 1) == npages - 1;
@@ -834,7 +844,15 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
       timed_out = true;
       break;
     }
-    round(st0 + sa * stage_bytes, RP == 2, false, 0);
+    if constexpr (LQ) {
+      // pages first + 4k (, first + 4k + 4): members lie in block 0 and from
+      // lq_lo() on
+      const int t0 = (first + kDecodeWarps * k) * kPage;
+      const int t1 = t0 + (RP == 2 ? kDecodeWarps * kPage : 0) + kPage;
+      round(st0 + sa * stage_bytes, RP == 2, t0 < lq_w || t1 > lq_from, t0);
+    } else {
+      round(st0 + sa * stage_bytes, RP == 2, false, 0);
+    }
     // refill the round's stages with pages k + NST (, k + NST + 1)
     const int pid0 = pid_of(k + NST);
     const int pid1 = RP == 2 ? pid_of(k + NST + 1) : 0;
@@ -863,7 +881,8 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     } else {
       if (kpatch >= 0 && (kpatch - k) >= 0 && (kpatch - k) < (has_b ? 2 : 1))
         patch_stage<D, BK, BV>(st0 + (sa + kpatch - k) * stage_bytes, pbuf, pslot);
-      round(st0 + sa * stage_bytes, has_b, last_partial, (first + kDecodeWarps * k) * kPage);
+      round(st0 + sa * stage_bytes, has_b, last_partial || LQ,
+            (first + kDecodeWarps * k) * kPage);
     }
   }
   if (timed_out) {
@@ -900,39 +919,28 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   }
 }
 
-// ------------------------------------------------------------- window split
-// The bf16 window of (b, h): tokens at positions lq .. len - 1, in ring slots
-// p % R (the decode step's newest token comes from k_new / v_new: its slot is
-// being rewritten by this launch).  Attention is order-free, so the slots are
-// read in storage order.  Lane l holds dims [E l, E l + E) of a row; each warp
-// keeps UNROLL rows in flight (the kernel start has prefetched the window into
-// L2).
-//   1. scores: warp w takes tokens w, w + 4, ...; each lane forms its dims'
+// ---------------------------------------------- bf16 rows: window, reserve
+// Attention of the G query heads over nw bf16 rows (K row t at krow(t), V row
+// t at vrow(t)), written as an unrotated partial (m, l, acc) into `part`.  The
+// rows may come in any order (attention is order-free).  Lane l holds dims
+// [E l, E l + E) of a row; each warp keeps UNROLL rows in flight.
+//   1. scores: warp w takes rows w, w + 4, ...; each lane forms its dims'
 //      partial dot products with the G query heads, and one transpose-reduce
 //      (6 shuffles) leaves head (2 [l >= 16] + [l & 8]) summed in each group of
 //      8 lanes;
 //   2. warp i: maximum and sum of head i, p = 2^(s - m) in place;
-//   3. values: warp w takes the same tokens, accumulates p v for every head
+//   3. values: warp w takes the same rows, accumulates p v for every head
 //      in registers; the warps' sums meet in shared memory.
-template <int D>
-__device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h, int len, int lq,
-                             float* part) {
+// sc: [kMaxGroup][ldsc] floats of shared memory (ldsc >= nw).
+template <int D, typename KRow, typename VRow>
+__device__ void attend_rows(const DecodeParams& p, const Smem& sm, int nw, float* sc, int ldsc,
+                            KRow krow, VRow vrow, float* part) {
   constexpr int E = D / 32;
   constexpr int RW = E / 2;     // packed bf16 words of a row per lane
   constexpr int UNROLL = 16;    // rows in flight per warp
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nw = len - lq;
-  float* sc = reinterpret_cast<float*>(sm.area);   // [kMaxGroup][R]
-  const int R = p.R;
-  const uint16_t* kring = p.window + ((static_cast<size_t>(b) * p.Hkv + h) * 2 + 0) * R * D;
-  const uint16_t* vring = kring + static_cast<size_t>(R) * D;
-  const int tnew = p.step ? nw - 1 : -1;
-  const uint16_t* knew = p.step ? p.k_new + (static_cast<size_t>(b) * p.Hkv + h) * D : nullptr;
-  const uint16_t* vnew = p.step ? p.v_new + (static_cast<size_t>(b) * p.Hkv + h) * D : nullptr;
-  auto row_of = [&](const uint16_t* ring, const uint16_t* fresh, int t) -> const uint16_t* {
-    return (t == tnew ? fresh : ring + static_cast<size_t>((lq + t) % R) * D) + E * lane;
-  };
-  auto load_row = [&](const uint16_t* src, uint32_t (&w)[RW]) {
+  auto load_row = [&](const uint16_t* row, uint32_t (&w)[RW]) {
+    const uint16_t* src = row + E * lane;
     if constexpr (E == 4) {
       const uint2 x = *reinterpret_cast<const uint2*>(src);
       w[0] = x.x;
@@ -962,7 +970,7 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int t = t0 + kDecodeWarps * u;
-      if (t < nw) load_row(row_of(kring, knew, t), raw[u]);
+      if (t < nw) load_row(krow(t), raw[u]);
     }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
@@ -986,19 +994,19 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
       vv += __shfl_xor_sync(kFullMask, vv, 4);
       vv += __shfl_xor_sync(kFullMask, vv, 2);
       vv += __shfl_xor_sync(kFullMask, vv, 1);
-      if ((lane & 7) == 0) sc[hsel * R + t] = vv;
+      if ((lane & 7) == 0) sc[hsel * ldsc + t] = vv;
     }
   }
   __syncthreads();
   // ---- 2. softmax statistics of query head i (warp i)
   if (warp < p.G) {
     float mm = -CUDART_INF_F;
-    for (int t = lane; t < nw; t += 32) mm = fmaxf(mm, sc[warp * R + t]);
+    for (int t = lane; t < nw; t += 32) mm = fmaxf(mm, sc[warp * ldsc + t]);
     mm = warp_max(mm);
     float ll = 0.f;
     for (int t = lane; t < nw; t += 32) {
-      const float e = ex2(sc[warp * R + t] - mm);
-      sc[warp * R + t] = e;
+      const float e = ex2(sc[warp * ldsc + t] - mm);
+      sc[warp * ldsc + t] = e;
       ll += e;
     }
     ll = warp_sum(ll);
@@ -1019,7 +1027,7 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int t = t0 + kDecodeWarps * u;
-      if (t < nw) load_row(row_of(vring, vnew, t), raw[u]);
+      if (t < nw) load_row(vrow(t), raw[u]);
     }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
@@ -1029,7 +1037,7 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
       unpack(raw[u], x);
 #pragma unroll
       for (int i = 0; i < kMaxGroup; ++i) {
-        const float pi = i < p.G ? sc[i * R + t] : 0.f;
+        const float pi = i < p.G ? sc[i * ldsc + t] : 0.f;
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[i][e] = __fmaf_rn(pi, x[e], acc[i][e]);
       }
@@ -1047,6 +1055,28 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
     for (int w = 0; w < kDecodeWarps; ++w) sum += macc[w * kMaxGroup * D + idx];
     part[idx] = sum;                            // part_acc<D>(part, i)[d], idx = i D + d
   }
+}
+
+// The bf16 window of (b, h): tokens at positions lq .. len - 1, in ring slots
+// p % R (the decode step's newest token comes from k_new / v_new: its slot is
+// being rewritten by this launch).  The kernel start has prefetched the
+// window into L2.
+template <int D>
+__device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h, int len, int lq,
+                             float* part) {
+  const int tid = threadIdx.x;
+  const int nw = len - lq;
+  const int R = p.R;
+  const uint16_t* kring = p.window + ((static_cast<size_t>(b) * p.Hkv + h) * 2 + 0) * R * D;
+  const uint16_t* vring = kring + static_cast<size_t>(R) * D;
+  const int tnew = p.step ? nw - 1 : -1;
+  const uint16_t* knew = p.step ? p.k_new + (static_cast<size_t>(b) * p.Hkv + h) * D : nullptr;
+  const uint16_t* vnew = p.step ? p.v_new + (static_cast<size_t>(b) * p.Hkv + h) * D : nullptr;
+  attend_rows<D>(
+      p, sm, nw, reinterpret_cast<float*>(sm.area), R,
+      [&](int t) { return t == tnew ? knew : kring + static_cast<size_t>((lq + t) % R) * D; },
+      [&](int t) { return t == tnew ? vnew : vring + static_cast<size_t>((lq + t) % R) * D; },
+      part);
   // decode step on a sequence no longer than the window: no token leaves the
   // ring, so nobody else writes the new token into it
   if (p.step && lq == 0 && nw > 0) {
@@ -1057,6 +1087,68 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
       vslot[d] = vnew[d];
     }
   }
+}
+
+// Reserve split (LogQuant mode) of (b, h) at length len.  A decode step first
+// carries out its halving, if its token fills B to 3W (the block thinned for
+// the first time moves from the ring to its level buffer; the first halving
+// moves block 0 too), and writes its token's bf16 rows into the ring.  Then
+// the rows of every member of B are listed in shared memory (any order) and
+// attended over.
+template <int D>
+__device__ void reserve_split(const DecodeParams& p, const Smem& sm, int b, int h, int len,
+                              float* part) {
+  const int tid = threadIdx.x;
+  const int w = p.lq_w, a = p.lq_a, half = w / 2;
+  const int ldsc = 3 * w;                       // |B| <= 3W
+  float* sc = reinterpret_cast<float*>(sm.area);           // [kMaxGroup][3W]
+  int* list = reinterpret_cast<int*>(sc + kMaxGroup * ldsc); // [3W] row numbers
+  int* count = reinterpret_cast<int*>(sm.flag);
+  uint16_t* kplane = const_cast<uint16_t*>(p.window) +
+                     ((static_cast<size_t>(b) * p.Hkv + h) * 2) * p.lq_rows * D;
+  uint16_t* vplane = kplane + static_cast<size_t>(p.lq_rows) * D;
+  constexpr int C = D / 8;                      // uint4 chunks per row
+  if (p.step && len > 0) {
+    const int k0 = lq_halvings(len - 1, w), k1 = lq_halvings(len, w);
+    if (k1 > k0) {                              // one halving: block 1 + k0 (and block 0)
+      for (int pass = 0; pass < (k0 == 0 ? 2 : 1); ++pass) {
+        const int bb = pass ? 0 : 1 + k0;
+        const int level = bb == 0 ? a : bb % a;
+        for (int idx = tid; idx < 2 * half * C; idx += kThreads) {
+          const int kv = idx / (half * C), r = idx - kv * half * C;
+          const int v = r / C, ci = r - v * C;
+          const int q = bb * w + 2 * v;         // older than this step's token
+          uint16_t* plane = kv ? vplane : kplane;
+          const uint4 x = reinterpret_cast<const uint4*>(plane + static_cast<size_t>(q % (3 * w)) * D)[ci];
+          reinterpret_cast<uint4*>(plane + static_cast<size_t>(3 * w + level * half + v) * D)[ci] = x;
+        }
+      }
+    }
+    // the new token: a member, newer than (k + 1) W: its ring row
+    const int rnew = (len - 1) % (3 * w);
+    const uint16_t* knew = p.k_new + (static_cast<size_t>(b) * p.Hkv + h) * D;
+    const uint16_t* vnew = p.v_new + (static_cast<size_t>(b) * p.Hkv + h) * D;
+    for (int idx = tid; idx < 2 * C; idx += kThreads) {
+      const int kv = idx / C, ci = idx - kv * C;
+      reinterpret_cast<uint4*>((kv ? vplane : kplane) + static_cast<size_t>(rnew) * D)[ci] =
+          reinterpret_cast<const uint4*>(kv ? vnew : knew)[ci];
+    }
+  }
+  if (tid == 0) *count = 0;
+  __syncthreads();
+  // member list: block 0 and the positions from lq_lo on
+  const int lo = lq_lo(len, w, a);
+  const int nb0 = min(w, len);
+  const int ncand = nb0 + max(0, len - max(lo, nb0));
+  for (int t = tid; t < ncand; t += kThreads) {
+    const int pos = t < nb0 ? t : max(lo, nb0) + (t - nb0);
+    if (lq_member(pos, len, w, a)) list[atomicAdd(count, 1)] = lq_row(pos, len, w, a);
+  }
+  __syncthreads();
+  const int nm = *count;
+  attend_rows<D>(
+      p, sm, nm, sc, ldsc, [&](int t) { return kplane + static_cast<size_t>(list[t]) * D; },
+      [&](int t) { return vplane + static_cast<size_t>(list[t]) * D; }, part);
 }
 
 // E consecutive floats (E = 4 or 2; 16- or 8-byte aligned) bypassing L1.
@@ -1212,7 +1304,9 @@ __device__ __forceinline__ void push_partial(const Smem& sm, uint32_t rank) {
 }
 
 // -------------------------------------------------------------- the kernel --
-template <int D>
+// LQ: LogQuant mode (its own instantiation, so that the ordinary kernel's
+// code is untouched by the masking and the reserve split).
+template <int D, bool LQ>
 __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const Smem sm = carve<D>(smem_raw);
@@ -1247,7 +1341,12 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
   }
   __syncthreads();
 
-  if (is_window) {
+  if (LQ && is_window) {
+    grid_wait();
+    if (p.overlap) load_query<D>(p, b, h, qv);
+    query_window_prologue<D>(p, sm, qv);
+    reserve_split<D>(p, sm, b, h, len, sm.cpart);
+  } else if (is_window) {
     // the window's valid slots are a prefix of the ring (all R of them once
     // the sequence is longer than the window): one bulk prefetch into L2 each
     // for K and V, before the wait (a hint; L2 is coherent with the writes
@@ -1266,15 +1365,15 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
   } else {
     const int bk = p.geom.bits[h][0], bv = p.geom.bits[h][1];
     switch (bk * 16 + bv) {
-      case 0x22: quant_split<D, 2, 2>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x24: quant_split<D, 2, 4>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x28: quant_split<D, 2, 8>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x42: quant_split<D, 4, 2>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x44: quant_split<D, 4, 4>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x48: quant_split<D, 4, 8>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x82: quant_split<D, 8, 2>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x84: quant_split<D, 8, 4>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x88: quant_split<D, 8, 8>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x22: quant_split<D, 2, 2, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x24: quant_split<D, 2, 4, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x28: quant_split<D, 2, 8, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x42: quant_split<D, 4, 2, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x44: quant_split<D, 4, 4, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x48: quant_split<D, 4, 8, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x82: quant_split<D, 8, 2, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x84: quant_split<D, 8, 4, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x88: quant_split<D, 8, 8, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
       default: break;
     }
     __syncthreads();   // the warps' partials are in the merge region
@@ -1313,13 +1412,16 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
 template <int D>
 size_t smem_bytes(const DecodeParams& p) {
   const size_t stages = static_cast<size_t>(kDecodeWarps) * kDecodeStages * p.stage_bytes;
-  const size_t win = static_cast<size_t>(kMaxGroup) * p.R * 4;
+  // window scores [kMaxGroup][R], or the reserve's scores [kMaxGroup][3W] and
+  // member list [3W]
+  const size_t win = p.lq_w ? static_cast<size_t>(kMaxGroup + 1) * 3 * p.lq_w * 4
+                            : static_cast<size_t>(kMaxGroup) * p.R * 4;
   return header_bytes(D) + (stages > win ? stages : win);
 }
 
-// Lets decode_kernel<D> use up to the device's opt-in shared memory (set once
-// per device; never lowered, so any smaller size launches too).
-template <int D>
+// Lets decode_kernel<D, LQ> use up to the device's opt-in shared memory (set
+// once per device; never lowered, so any smaller size launches too).
+template <int D, bool LQ>
 cudaError_t allow_smem() {
   static int done[64] = {0};
   int dev = 0;
@@ -1329,16 +1431,17 @@ cudaError_t allow_smem() {
   int optin = 0;
   e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  e = cudaFuncSetAttribute(decode_kernel<D, LQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           optin);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
   return e;
 }
 
-template <int D>
+template <int D, bool LQ>
 cudaError_t launch_d(const DecodeParams& p, cudaStream_t s) {
   const size_t bytes = smem_bytes<D>(p);
   if (bytes > 48 * 1024) {
-    const cudaError_t e = allow_smem<D>();
+    const cudaError_t e = allow_smem<D, LQ>();
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -1362,7 +1465,16 @@ cudaError_t launch_d(const DecodeParams& p, cudaStream_t s) {
   }
   cfg.attrs = n ? attr : nullptr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<D>, p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, LQ>, p);
+}
+
+template <int D, bool LQ>
+int blocks_per_sm(size_t smem) {
+  int n = 0;
+  cudaError_t e = allow_smem<D, LQ>();
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, LQ>, kThreads, smem);
+  return e == cudaSuccess ? n : -1;
 }
 
 }  // namespace
@@ -1370,19 +1482,9 @@ cudaError_t launch_d(const DecodeParams& p, cudaStream_t s) {
 int decode_max_splits() { return kMaxSplits; }
 int decode_max_cluster() { return kMaxCluster; }
 
-int decode_blocks_per_sm(int head_dim, size_t smem) {
-  int n = 0;
-  cudaError_t e;
-  if (head_dim == 128) {
-    e = allow_smem<128>();
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<128>, kThreads, smem);
-  } else {
-    e = allow_smem<64>();
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<64>, kThreads, smem);
-  }
-  return e == cudaSuccess ? n : -1;
+int decode_blocks_per_sm(int head_dim, size_t smem, bool logquant) {
+  if (head_dim == 128) return logquant ? blocks_per_sm<128, true>(smem) : blocks_per_sm<128, false>(smem);
+  return logquant ? blocks_per_sm<64, true>(smem) : blocks_per_sm<64, false>(smem);
 }
 
 size_t decode_smem_bytes(const DecodeParams& p, int head_dim) {
@@ -1390,8 +1492,8 @@ size_t decode_smem_bytes(const DecodeParams& p, int head_dim) {
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, cudaStream_t s) {
-  if (head_dim == 128) return launch_d<128>(p, s);
-  if (head_dim == 64) return launch_d<64>(p, s);
+  if (head_dim == 128) return p.lq_w ? launch_d<128, true>(p, s) : launch_d<128, false>(p, s);
+  if (head_dim == 64) return p.lq_w ? launch_d<64, true>(p, s) : launch_d<64, false>(p, s);
   return cudaErrorInvalidValue;
 }
 

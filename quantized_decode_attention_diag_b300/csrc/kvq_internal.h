@@ -33,6 +33,8 @@ struct AppendParams {
   int* status;
   int max_pages, B, T, Hkv, R, num_pages;
   int warps_per_group;           // ceil(B * T / 16)
+  int lq_w, lq_a, lq_rows;       // LogQuant base window W (0: off), log2 W, reserve rows
+                                 // per plane; `window` is then the reserve
   LayerGeom geom;
 };
 
@@ -59,6 +61,8 @@ struct DecodeParams {
   const uint16_t* v_new;
   int stage_bytes;               // bytes of one pipeline stage buffer
   float scale_log2;              // softmax_scale * log2(e)
+  int lq_w, lq_a, lq_rows;       // LogQuant (as in AppendParams); R is 0 then, and the
+                                 // split after the S quantized ones is the reserve's
   int wait_log2;                 // the main loop gives up on a page copy after
                                  // ~2^wait_log2 cycles (31 unless debugging)
   LayerGeom geom;
@@ -90,9 +94,13 @@ constexpr int kAppendWarps = 8;
 
 // Launchers (defined in the .cu files).  Return cudaSuccess or the launch error.
 cudaError_t launch_append(const AppendParams& p, int head_dim, int had_block, cudaStream_t s);
+// LogQuant mode, before the append: the reserve's older members that the
+// append's halvings thin move from the ring to their level buffers.
+cudaError_t launch_lq_carry(const AppendParams& p, int head_dim, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, cudaStream_t s);
 size_t decode_smem_bytes(const DecodeParams& p, int head_dim);
-int decode_blocks_per_sm(int head_dim, size_t smem);   // resident CTAs per SM, -1 on error
+int decode_blocks_per_sm(int head_dim, size_t smem, bool logquant);   // resident CTAs per SM,
+                                                                     // -1 on error
 int decode_max_splits();
 int decode_max_cluster();                               // largest cluster the merge uses
 
