@@ -457,7 +457,7 @@ def run_kvq(args) -> None:
     # append sweep: 8 sequences x 8192 new tokens into empty caches
     append = append_sweep(kvq, torch, dev) if not args.skip_append else None
     calib = calibration_bench(kvq, torch, dev) if not args.skip_append else None
-    mixed = long_ctx = qerr = None
+    mixed = long_ctx = qerr = lq = None
     if not args.skip_configs:
         # the mixed-bits allocation takes (alpha, beta) from the calibration
         if calib is not None:
@@ -469,6 +469,7 @@ def run_kvq(args) -> None:
             mixed = mixed_bits_bench(kvq, torch, dev, alpha, beta, min(args.steps, 10),
                                      args.warmup)
         long_ctx = long_context_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
+        lq = logquant_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
         qerr = quant_error_report(kvq, torch, dev)
     if calib is not None:
         calib.pop("_alpha")
@@ -510,6 +511,7 @@ def run_kvq(args) -> None:
         "calibration": calib,
         "mixed_bits": mixed,
         "long_context": long_ctx,
+        "logquant": lq,
         "quant_error": qerr,
     }
     print(json.dumps(line), flush=True)
@@ -785,6 +787,54 @@ def long_context_bench(kvq, torch, dev, n_layers, steps, warmup) -> dict:
                         f"head_dim {d}, K{w.k_bits}V{w.v_bits}, Hadamard {w.had_block}, "
                         f"{r}-token bf16 window, {n_layers} layer caches",
             "step": "per layer: kvq_decode_step (ticket merge over the splits)",
+            "ms_per_step": round(ms, 4), "GB_per_step": round(sb / 1e9, 4),
+            "roofline": _roofline(sb, ms, n_layers, iso, per)}
+
+
+def logquant_bench(kvq, torch, dev, n_layers, steps, warmup, w=128) -> dict:
+    """LogQuant mode on the long-context shape: one sequence of 131072 tokens,
+    32 query / 8 KV heads, head_dim 128, K and V INT2 (the method's 2-bit
+    setting) with Hadamard 128, base window W = 128: every token quantized,
+    the log-spaced set B (< 3W positions) kept in bf16 in the reserve.  One
+    step = one fused decode step per layer over n_layers layer caches."""
+    L = LONG_CONTEXT
+    hkv, hq, d, ctx = L.hkv, L.hq, L.head_dim, L.ctx
+    mp = ctx // 16
+    k = kv_tokens(L.seed, 0, 1, ctx, hkv, d, L.k_outliers, L.outlier_lo, L.outlier_hi)
+    v = kv_tokens(L.seed, 1, 1, ctx, hkv, d, L.v_outliers, L.outlier_lo, L.outlier_hi)
+    kd = torch.from_numpy(k).to(dev).to(torch.bfloat16)
+    vd = torch.from_numpy(v).to(dev).to(torch.bfloat16)
+    del k, v
+    bits = np.full((n_layers, hkv, 2), 2)
+    cache = kvq.Cache(n_layers, hkv, d, L.had_block, bits, mp, max_batch=1, device=dev,
+                      overlap=True, logquant_w=w)
+    pt = torch.from_numpy(page_table(L.seed, 1, mp)).to(dev)
+    zero = torch.zeros(1, dtype=torch.int32, device=dev)
+    kpre, vpre = kd[:, :ctx - 1].contiguous(), vd[:, :ctx - 1].contiguous()
+    for l in range(n_layers):
+        cache.append(l, kpre, vpre, pt, zero)
+    knew = kd[:, ctx - 1].contiguous().unsqueeze(0).repeat(n_layers, 1, 1, 1).contiguous()
+    vnew = vd[:, ctx - 1].contiguous().unsqueeze(0).repeat(n_layers, 1, 1, 1).contiguous()
+    del kd, vd, kpre, vpre
+    q_all = torch.from_numpy(np.stack([queries(L.seed, l, 1, hq, d, False)
+                                       for l in range(n_layers)])).to(dev).to(torch.bfloat16)
+    o_all = torch.empty((n_layers, 1, hq, d), dtype=torch.float32, device=dev)
+    after = torch.full((1,), ctx, dtype=torch.int32, device=dev)
+    ws = cache.workspace(1, hq, mp)
+    torch.cuda.synchronize(dev)
+    ms, iso = graph_step_bench(torch, dev, cache, n_layers, knew, vnew, q_all, pt, after, o_all,
+                               ws, steps, warmup)
+    members = len(kvq.kvq_logquant_members(ctx, w))
+    partial_floats = (ws.numel() - (hkv * 4 + 255) // 256 * 256) // 4
+    per = (step_bytes_layer(bits[0], 1, ctx, hq, d, partial_floats=partial_floats)
+           + hkv * members * 2 * 2 * d)            # the members' bf16 K and V rows
+    sb = per * n_layers
+    del cache
+    return {"workload": f"LogQuant: 1 sequence x {ctx} tokens, {hq} q / {hkv} KV heads, "
+                        f"head_dim {d}, K2V2, Hadamard {L.had_block}, base window W = {w} "
+                        f"({members} full-precision positions), {n_layers} layer caches",
+            "step": "per layer: kvq_decode_step (members masked in the quantized splits, "
+                    "a reserve CTA attends over their bf16 rows)",
             "ms_per_step": round(ms, 4), "GB_per_step": round(sb / 1e9, 4),
             "roofline": _roofline(sb, ms, n_layers, iso, per)}
 

@@ -66,6 +66,7 @@ struct Smem {
   float* qsum;        // [kMaxGroup]
   int* flag;          // last-arriver flag of the ticket
   int* bad;           // a page id of this split was out of range
+  int* wait_log2;     // the page-copy wait limit (a copy of p.wait_log2)
   float* qscl;        // [kMaxGroup] power-of-two scale of the query fragments
   uint64_t* bars;     // [warps][stages]
   float* merge;       // [warps][kMaxGroup][D + 2] warp partials
@@ -89,6 +90,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base) {
   s.qsum = reinterpret_cast<float*>(misc);
   s.flag = reinterpret_cast<int*>(misc + 16);
   s.bad = reinterpret_cast<int*>(misc + 20);
+  s.wait_log2 = reinterpret_cast<int*>(misc + 24);
   s.qscl = reinterpret_cast<float*>(misc + 32);
   s.bars = reinterpret_cast<uint64_t*>(misc + 64);
   s.merge = reinterpret_cast<float*>(misc + 64 + kDecodeWarps * kDecodeStages * 8);
@@ -640,8 +642,7 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   // start streaming before the query prologue (with a shortened copy wait, a
   // debugging aid, only right before the loop: the first waits then come
   // sooner than any copy can land)
-  const bool debug_wait = p.wait_log2 < kWaitLimitLog2;
-  if (!debug_wait)
+  if (p.wait_log2 >= kWaitLimitLog2)
     for (int kk = 0; kk < nk && kk < NST; ++kk) issue(true, kk, pid_of(kk));
 
   // with programmatic dependent launch, everything above may overlap the
@@ -829,7 +830,7 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   // is this warp's last page); the final round takes the rest
   const int nfull = nk - ((last_partial || kpatch >= 0) ? 1 : 0);
 
-  if (debug_wait)
+  if (p.wait_log2 < kWaitLimitLog2)
     for (int kk = 0; kk < nk && kk < NST; ++kk) issue(true, kk, pid_of(kk));
   bool timed_out = false;
   int k = 0, sa = 0;
@@ -838,8 +839,13 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   constexpr int RP = kDecodeRoundPages;
   for (; k + RP <= nfull;) {
     bool ok;
-    if constexpr (RP == 2) ok = mbar_wait2_warp(bars + sa, ph, p.wait_log2);
-    else ok = __all_sync(kFullMask, mbar_wait_bounded(bars + sa, ph, p.wait_log2));
+    if constexpr (RP == 2) {
+      ok = mbar_wait2_warp(bars + sa, ph, sm.wait_log2);
+    } else {
+      int lim;
+      asm volatile("ld.volatile.shared.s32 %0, [%1];" : "=r"(lim) : "r"(smem_u32(sm.wait_log2)));
+      ok = __all_sync(kFullMask, mbar_wait_bounded(bars + sa, ph, lim));
+    }
     if (!ok) {
       timed_out = true;
       break;
@@ -874,8 +880,8 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   // the rest: at most RP pages, the last maybe partial
   if (!timed_out && k < nk) {
     const bool has_b = RP == 2 && k + 1 < nk;
-    bool ok = mbar_wait_bounded(bars + sa, ph, p.wait_log2);
-    if (has_b) ok = mbar_wait_bounded(bars + sa + 1, ph, p.wait_log2) && ok;
+    bool ok = mbar_wait_bounded(bars + sa, ph, *sm.wait_log2);
+    if (has_b) ok = mbar_wait_bounded(bars + sa + 1, ph, *sm.wait_log2) && ok;
     if (!__all_sync(kFullMask, ok)) {
       timed_out = true;
     } else {
@@ -1057,26 +1063,161 @@ __device__ void attend_rows(const DecodeParams& p, const Smem& sm, int nw, float
   }
 }
 
+// Shared memory of the window split: scores [kMaxGroup][R] (128-byte
+// aligned), then up to kWinChunk rows of the ring [rows][D] bf16.
+constexpr int kWinChunk = 128;
+__host__ __device__ constexpr size_t win_score_bytes(int R) {
+  return (static_cast<size_t>(kMaxGroup) * R * 4 + 127) / 128 * 128;
+}
+__host__ __device__ constexpr size_t win_bytes(int R, int d) {
+  return win_score_bytes(R) + static_cast<size_t>(R < kWinChunk ? R : kWinChunk) * d * 2;
+}
+
 // The bf16 window of (b, h): tokens at positions lq .. len - 1, in ring slots
-// p % R (the decode step's newest token comes from k_new / v_new: its slot is
-// being rewritten by this launch).  The kernel start has prefetched the
-// window into L2.
+// p % R.  The valid slots are always the prefix [0, len - lq) of the ring (all
+// R of them once the sequence is longer than the window), and attention is
+// order-free, so the slots are taken in storage order: chunks of up to
+// kWinChunk rows are staged in shared memory by one bulk copy each (the kernel
+// start has prefetched the window into L2), K for the scores, then V.  The
+// decode step's newest token comes from k_new / v_new: its slot is being
+// rewritten by this launch.  Lane l holds dims [E l, E l + E) of a row; warp w
+// takes rows w, w + 4, ... of each chunk.
 template <int D>
 __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h, int len, int lq,
                              float* part) {
-  const int tid = threadIdx.x;
+  constexpr int E = D / 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nw = len - lq;
   const int R = p.R;
   const uint16_t* kring = p.window + ((static_cast<size_t>(b) * p.Hkv + h) * 2 + 0) * R * D;
   const uint16_t* vring = kring + static_cast<size_t>(R) * D;
-  const int tnew = p.step ? nw - 1 : -1;
+  const int snew = (p.step && nw > 0) ? (len - 1) % R : -1;
   const uint16_t* knew = p.step ? p.k_new + (static_cast<size_t>(b) * p.Hkv + h) * D : nullptr;
   const uint16_t* vnew = p.step ? p.v_new + (static_cast<size_t>(b) * p.Hkv + h) * D : nullptr;
-  attend_rows<D>(
-      p, sm, nw, reinterpret_cast<float*>(sm.area), R,
-      [&](int t) { return t == tnew ? knew : kring + static_cast<size_t>((lq + t) % R) * D; },
-      [&](int t) { return t == tnew ? vnew : vring + static_cast<size_t>((lq + t) % R) * D; },
-      part);
+  float* sc = reinterpret_cast<float*>(sm.area);                       // [kMaxGroup][R]
+  uint16_t* buf = reinterpret_cast<uint16_t*>(sm.area + win_score_bytes(R));  // [chunk][D]
+  uint64_t* bar = sm.bars;              // this CTA has no page ring: its first barrier
+  unsigned ph = 0;
+  // rows [c0, c0 + n) of a ring plane into buf (every thread waits)
+  auto stage = [&](const uint16_t* plane, int c0, int n) {
+    __syncthreads();                    // everyone is done with buf
+    if (tid == 0) {
+      mbar_expect_tx(bar, static_cast<unsigned>(n) * D * 2);
+      bulk_g2s(buf, plane + static_cast<size_t>(c0) * D, static_cast<unsigned>(n) * D * 2, bar);
+    }
+    if (!mbar_wait_bounded(bar, ph)) {
+      if (tid == 0) flag_status(p.status, KVQ_DEV_COPY_TIMEOUT);
+      (void)mbar_wait_bounded(bar, ph); // the copy must land before buf is reused
+    }
+    ph ^= 1u;
+  };
+  // this lane's E values of slot t (chunk base c0), as floats
+  auto row = [&](const uint16_t* fresh, int t, int c0, float (&x)[E]) {
+    uint32_t w[E / 2];
+    if (t == snew) {
+      const uint16_t* src = fresh + E * lane;
+#pragma unroll
+      for (int i = 0; i < E / 2; ++i) w[i] = *reinterpret_cast<const uint32_t*>(src + 2 * i);
+    } else {
+      const uint32_t a = smem_u32(buf + static_cast<size_t>(t - c0) * D + E * lane);
+      if constexpr (E == 4) {
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(a));
+      } else {
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[0]) : "r"(a));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+      x[2 * i] = bf16lo(w[i]);
+      x[2 * i + 1] = bf16hi(w[i]);
+    }
+  };
+  float qf[kMaxGroup][E];
+#pragma unroll
+  for (int i = 0; i < kMaxGroup; ++i)
+#pragma unroll
+    for (int e = 0; e < E; ++e) qf[i][e] = sm.qtab[i * D + E * lane + e];
+  const bool up = lane & 16, u8 = lane & 8;
+  const int hsel = (up ? 2 : 0) + (u8 ? 1 : 0);
+
+  // ---- 1. scores: each lane forms its dims' partial dot products with the G
+  //      query heads; one transpose-reduce (6 shuffles) leaves head (2 [l >=
+  //      16] + [l & 8]) summed in each group of 8 lanes
+  for (int c0 = 0; c0 < nw; c0 += kWinChunk) {
+    const int n = min(kWinChunk, nw - c0);
+    stage(kring, c0, n);
+    for (int t = c0 + warp; t < c0 + n; t += kDecodeWarps) {
+      float x[E];
+      row(knew, t, c0, x);
+      float a[kMaxGroup];
+#pragma unroll
+      for (int i = 0; i < kMaxGroup; ++i) {
+        a[i] = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) a[i] = __fmaf_rn(qf[i][e], x[e], a[i]);
+      }
+      const float r0 = __shfl_xor_sync(kFullMask, up ? a[0] : a[2], 16);
+      const float r1 = __shfl_xor_sync(kFullMask, up ? a[1] : a[3], 16);
+      const float k0 = (up ? a[2] : a[0]) + r0, k1 = (up ? a[3] : a[1]) + r1;
+      float vv = (u8 ? k1 : k0) + __shfl_xor_sync(kFullMask, u8 ? k0 : k1, 8);
+      vv += __shfl_xor_sync(kFullMask, vv, 4);
+      vv += __shfl_xor_sync(kFullMask, vv, 2);
+      vv += __shfl_xor_sync(kFullMask, vv, 1);
+      if ((lane & 7) == 0) sc[hsel * R + t] = vv;
+    }
+  }
+  __syncthreads();
+  // ---- 2. softmax statistics of query head i (warp i)
+  if (warp < p.G) {
+    float mm = -CUDART_INF_F;
+    for (int t = lane; t < nw; t += 32) mm = fmaxf(mm, sc[warp * R + t]);
+    mm = warp_max(mm);
+    float ll = 0.f;
+    for (int t = lane; t < nw; t += 32) {
+      const float e = ex2(sc[warp * R + t] - mm);
+      sc[warp * R + t] = e;
+      ll += e;
+    }
+    ll = warp_sum(ll);
+    if (lane == 0) {
+      part_m<D>(part)[warp] = nw > 0 ? mm : -CUDART_INF_F;
+      part_l<D>(part)[warp] = ll;
+    }
+  }
+  // ---- 3. values: p v for every head in registers; the warps' sums meet in
+  //      shared memory (stage() begins with the barrier that orders phase 2)
+  float acc[kMaxGroup][E];
+#pragma unroll
+  for (int i = 0; i < kMaxGroup; ++i)
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[i][e] = 0.f;
+  for (int c0 = 0; c0 < nw; c0 += kWinChunk) {
+    const int n = min(kWinChunk, nw - c0);
+    stage(vring, c0, n);
+    for (int t = c0 + warp; t < c0 + n; t += kDecodeWarps) {
+      float x[E];
+      row(vnew, t, c0, x);
+#pragma unroll
+      for (int i = 0; i < kMaxGroup; ++i) {
+        const float pi = i < p.G ? sc[i * R + t] : 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[i][e] = __fmaf_rn(pi, x[e], acc[i][e]);
+      }
+    }
+  }
+  __syncthreads();
+  float* macc = sm.merge;                       // [warps][kMaxGroup][D]
+#pragma unroll
+  for (int i = 0; i < kMaxGroup; ++i)
+#pragma unroll
+    for (int e = 0; e < E; ++e) macc[(warp * kMaxGroup + i) * D + E * lane + e] = acc[i][e];
+  __syncthreads();
+  for (int idx = tid; idx < kMaxGroup * D; idx += kThreads) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) sum += macc[w * kMaxGroup * D + idx];
+    part[idx] = sum;                            // part_acc<D>(part, i)[d], idx = i D + d
+  }
   // decode step on a sequence no longer than the window: no token leaves the
   // ring, so nobody else writes the new token into it
   if (p.step && lq == 0 && nw > 0) {
@@ -1337,6 +1478,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
   if (tid == 0) {
     for (int i = 0; i < kDecodeWarps * kDecodeStages; ++i) mbar_init(sm.bars + i, 1);
     *sm.bad = 0;
+    *sm.wait_log2 = p.wait_log2;
     mbar_init_fence();
   }
   __syncthreads();
@@ -1415,7 +1557,7 @@ size_t smem_bytes(const DecodeParams& p) {
   // window scores [kMaxGroup][R], or the reserve's scores [kMaxGroup][3W] and
   // member list [3W]
   const size_t win = p.lq_w ? static_cast<size_t>(kMaxGroup + 1) * 3 * p.lq_w * 4
-                            : static_cast<size_t>(kMaxGroup) * p.R * 4;
+                            : (p.R > 0 ? win_bytes(p.R, D) : 0);
   return header_bytes(D) + (stages > win ? stages : win);
 }
 

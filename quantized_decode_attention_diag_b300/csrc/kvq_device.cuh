@@ -159,26 +159,26 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
 
 // Both of two consecutive barriers (bar, bar + 1) at phase `parity`, for the
 // whole warp (every lane calls it; the result is warp-uniform): one combined
-// test and a vote on the fast path, then bounded waits on each barrier.
-__device__ __forceinline__ bool mbar_wait2_warp(uint64_t* bar, unsigned parity, int limit_log2) {
-  if (limit_log2 < kWaitLimitLog2) {   // debugging: polling only (see mbar_wait_bounded)
-    const bool a = mbar_wait_bounded(bar, parity, limit_log2);
-    const bool b = mbar_wait_bounded(bar + 1, parity, limit_log2);
-    return __all_sync(0xffffffffu, a && b);
-  }
+// non-blocking test and a vote on the fast path; when a copy is late, bounded
+// waits on each barrier with the limit read from shared memory (*limit_log2, a
+// volatile load, so that no register holds it across the caller's loop).
+__device__ __forceinline__ bool mbar_wait2_warp(uint64_t* bar, unsigned parity,
+                                                const int* limit_log2) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 q, [%1 + 8], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q, [%1 + 8], %2;\n\t"
       "and.pred p, p, q;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   if (__all_sync(0xffffffffu, ok != 0)) return true;
-  const bool a = mbar_wait_bounded(bar, parity, limit_log2);
-  const bool b = mbar_wait_bounded(bar + 1, parity, limit_log2);
+  int lim;
+  asm volatile("ld.volatile.shared.s32 %0, [%1];" : "=r"(lim) : "r"(smem_u32(limit_log2)));
+  const bool a = mbar_wait_bounded(bar, parity, lim);
+  const bool b = mbar_wait_bounded(bar + 1, parity, lim);
   return __all_sync(0xffffffffu, a && b);
 }
 
