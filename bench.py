@@ -28,6 +28,16 @@ the replayed step.  "append" adds the quantize-on-append sweep (8 sequences x
 8192 new tokens, every Hadamard block and bit width) in tokens/s.
 "cpu_baseline" times the CPU oracle on a bounded sample.
 
+Further sections of the same line, each with its own roofline object:
+"mixed_bits" (32 layers x 8 KV heads, batch 64, context 2048, per-head bits
+from kvq_alloc_bits fed by kvq_distortion + kvq_fit_distortion, at 3.0 and
+3.5 average bits), "long_context" (1 sequence x 131072 tokens, K4V2, a
+128-token bf16 window), "logquant" (the same shape at K2V2 with LogQuant's
+log-spaced bf16 tokens, W = 128) and "quant_error" (error of the cache's
+attention against float64 attention over the original bf16 K/V, with and
+without the rotation, computed with torch on the device).  --only
+{mixed,long,logquant} runs one of them alone over --layers layer caches.
+
 --impl reference times the CPU oracle itself as the reference arm (this
 library has no third-party reference implementation to install).
 """
@@ -687,7 +697,7 @@ def _roofline(step_bytes, ms, n_layers, iso_ms, bytes_per_launch) -> dict:
             "isolated_launch_us": round(iso_ms * 1e3, 3)}
 
 
-def mixed_bits_bench(kvq, torch, dev, alpha, beta, steps, warmup) -> dict:
+def mixed_bits_bench(kvq, torch, dev, alpha, beta, steps, warmup, n_layers=None) -> dict:
     """The mixed per-head bits workload: 32 layers x 8 KV heads, batch 64,
     context 2048, 32 query heads, bits from the RateQuant greedy (sensitivities
     lognormal x U-shape over depth, times alpha; beta per component from the
@@ -697,6 +707,8 @@ def mixed_bits_bench(kvq, torch, dev, alpha, beta, steps, warmup) -> dict:
     K/V streams fill every layer's cache (the values do not change the work)."""
     w = MIXED_32L
     L, hkv, hq, d, bsz, ctx = w.num_layers, w.hkv, w.hq, w.head_dim, w.batch, w.ctx
+    if n_layers is not None:
+        L = n_layers                  # a smaller case for profiling
     mp = ctx // 16
     sens = sensitivities(w.seed, L, hkv).reshape(-1)
     allowed = [kvq.mask_of([4, 8]), kvq.mask_of([2, 4])] * (L * hkv)
@@ -902,6 +914,24 @@ def quant_error_report(kvq, torch, dev) -> dict:
             "configs": out}
 
 
+def run_section(args) -> None:
+    """One configuration section alone on one GPU, over --layers layer caches."""
+    import torch
+    import quantized_decode_attention_diag_b300 as kvq
+    from quantized_decode_attention_diag_b300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    if args.only == "mixed":
+        n = N_LAYERS * MIXED_32L.hkv * 2
+        out = mixed_bits_bench(kvq, torch, dev, np.ones(n), np.full(n, 4.0), args.steps,
+                               args.warmup, n_layers=N_LAYERS)
+    elif args.only == "long":
+        out = long_context_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
+    else:
+        out = logquant_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
+    print(json.dumps({"section": args.only, **out}), flush=True)
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -912,6 +942,8 @@ def main() -> None:
     ap.add_argument("--skip-append", action="store_true")
     ap.add_argument("--skip-configs", action="store_true",
                     help="leave out the mixed-bits, long-context and quantization-error sections")
+    ap.add_argument("--only", default="all", choices=["all", "mixed", "long", "logquant"],
+                    help="run one section alone and print it (profiling a small case)")
     ap.add_argument("--layers", type=int, default=32,
                     help="distinct layer caches per step (profiling uses a small case)")
     args = ap.parse_args()
@@ -921,6 +953,8 @@ def main() -> None:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.only != "all":
+        run_section(args)
     else:
         run_kvq(args)
 
