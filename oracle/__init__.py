@@ -13,10 +13,12 @@ the kernel's precision, see ``quantizer``):
                     rotation by matrix multiply.
 * ``fp16``       -- directed rounding to IEEE binary16.
 * ``quantizer``  -- token-wise asymmetric INT-b quantization with one fp16
-                    scale and one fp16 zero per vector.
+                    scale and one fp16 zero per vector; the symmetric
+                    per-channel key quantizer of the key-per-channel mode.
 * ``layout``     -- the paged-cache byte layout (pack / unpack).
 * ``cache``      -- quantize-on-append into the paged cache plus the bf16
-                    recent-token window.
+                    recent-token window (and the key-per-channel mode's
+                    page-at-a-time rule).
 * ``attention``  -- decode attention over the dequantized cache.
 * ``allocator``  -- RateQuant greedy marginal-gain bit allocation, the
                     closed-form reverse-waterfilling optimum, brute force.

@@ -9,6 +9,8 @@ Sources:
   attention output does not depend on the order of the (key, value) pairs,
   A V = A_P V_P, so full-precision window tokens and quantized tokens may be
   combined in any order.
+* RateQuant technical summary, Methodology section 3: in the key-per-channel
+  mode a page's keys are dequantized with one scale per channel.
 * CriticalKV technical summary, Methodology (perturbation definition): the L1
   distance between two attention outputs, used here to report quantization
   error.
@@ -23,9 +25,9 @@ from __future__ import annotations
 import numpy as np
 
 from . import layout
-from .cache import CacheState
+from .cache import CacheState, quantized_prefix
 from .hadamard import unrotate
-from .quantizer import dequantize
+from .quantizer import dequantize, dequantize_channels
 
 
 def softmax_attention(q: np.ndarray, keys: np.ndarray, values: np.ndarray,
@@ -44,8 +46,9 @@ def softmax_attention(q: np.ndarray, keys: np.ndarray, values: np.ndarray,
 def cached_kv(state: CacheState, layer: int, b: int, h: int, length: int,
               page_table: np.ndarray):
     """Reconstructed (keys, values) float64 [length, d] of (sequence b, KV head h)."""
-    r = state.window
-    lq = max(0, length - r) if r else length
+    kpc = state.key_per_channel
+    lq = quantized_prefix(length, state.window, kpc)
+    rows = state.ring_rows
     d = state.head_dim
     view = state.view(layer)
     pos = np.arange(lq)
@@ -53,13 +56,18 @@ def cached_kv(state: CacheState, layer: int, b: int, h: int, length: int,
     slots = pos % layout.PAGE_SIZE
     out = []
     for kv in (0, 1):
-        if lq:
+        if lq and kpc and kv == 0:
+            # key-per-channel: each page's codes times its channel scales
+            deq = [dequantize_channels(*view.read_key_channels(int(pg), h))
+                   for pg in pages[::layout.PAGE_SIZE]]
+            rec = unrotate(np.concatenate(deq, axis=0), state.had_block)
+        elif lq:
             codes, s, z = view.read(pages, slots, h, kv)
             rec = unrotate(dequantize(codes, s, z), state.had_block)
         else:
             rec = np.zeros((0, d))
         if length > lq:
-            wpos = np.arange(lq, length) % r
+            wpos = np.arange(lq, length) % rows
             win = state.windows[layer][b, h, kv, wpos].astype(np.float64)
             rec = np.concatenate([rec, win], axis=0)
         out.append(rec)

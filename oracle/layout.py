@@ -17,6 +17,15 @@ contiguous segment of
 Codes are packed with element j at bit offset (j * b) mod 8 of byte
 (j * b) // 8, i.e. for 4-bit codes element 2i is the low nibble of byte i.
 Every segment is a multiple of 16 bytes.
+
+In the key-per-channel mode the K (s, z) pairs give way to one fp16 scale per
+channel of the page's keys, and the K codes are stored in offset binary
+(c + 2^(b-1)):
+
+    K codes   [16][d * bK / 8]
+    V codes   [16][d * bV / 8]
+    K scales  [d] x fp16         channel j's scale for the page's 16 keys
+    V (s, z)  [16] x 2 x fp16
 """
 from __future__ import annotations
 
@@ -25,18 +34,20 @@ import numpy as np
 PAGE_SIZE = 16
 
 
-def head_bytes(d: int, bk: int, bv: int) -> int:
+def head_bytes(d: int, bk: int, bv: int, kpc: bool = False) -> int:
+    if kpc:
+        return PAGE_SIZE * (d * bk // 8 + d * bv // 8) + 2 * d + PAGE_SIZE * 4
     return PAGE_SIZE * (d * bk // 8 + d * bv // 8 + 8)
 
 
-def head_offsets(d: int, bits: np.ndarray) -> np.ndarray:
+def head_offsets(d: int, bits: np.ndarray, kpc: bool = False) -> np.ndarray:
     """Byte offset of each head's segment in a page; bits: int[Hkv, 2]."""
-    sizes = [head_bytes(d, int(b[0]), int(b[1])) for b in bits]
+    sizes = [head_bytes(d, int(b[0]), int(b[1]), kpc) for b in bits]
     return np.concatenate([[0], np.cumsum(sizes)[:-1]]).astype(np.int64)
 
 
-def page_bytes(d: int, bits: np.ndarray) -> int:
-    return int(sum(head_bytes(d, int(b[0]), int(b[1])) for b in bits))
+def page_bytes(d: int, bits: np.ndarray, kpc: bool = False) -> int:
+    return int(sum(head_bytes(d, int(b[0]), int(b[1]), kpc) for b in bits))
 
 
 def pack(codes: np.ndarray, bits: int) -> np.ndarray:
@@ -62,26 +73,50 @@ def unpack(packed: np.ndarray, bits: int, d: int) -> np.ndarray:
 class PageView:
     """Field accessors for one layer's pool: uint8[num_pages, page_bytes]."""
 
-    def __init__(self, pool: np.ndarray, d: int, bits: np.ndarray):
+    def __init__(self, pool: np.ndarray, d: int, bits: np.ndarray, kpc: bool = False):
         self.pool = pool
         self.d = d
         self.bits = np.asarray(bits, dtype=np.int64)
-        self.off = head_offsets(d, self.bits)
+        self.kpc = kpc
+        self.off = head_offsets(d, self.bits, kpc)
 
     def _seg(self, h: int):
+        """(bK, bV, K codes, V codes, K (s, z) or K scales, V (s, z)) offsets."""
         d = self.d
         bk, bv = int(self.bits[h, 0]), int(self.bits[h, 1])
         o = int(self.off[h])
         kc = o
         vc = kc + PAGE_SIZE * d * bk // 8
         ksz = vc + PAGE_SIZE * d * bv // 8
-        vsz = ksz + PAGE_SIZE * 4
+        vsz = ksz + (2 * d if self.kpc else PAGE_SIZE * 4)
         return bk, bv, kc, vc, ksz, vsz
+
+    def read_key_channels(self, page: int, h: int):
+        """Key-per-channel mode: (signed codes int64[16, d], scales fp16[d]) of
+        one page of head h."""
+        d = self.d
+        bk, _, kc, _, ksc, _ = self._seg(h)
+        nb = d * bk // 8
+        packed = self.pool[page, kc:kc + PAGE_SIZE * nb].reshape(PAGE_SIZE, nb)
+        codes = unpack(packed, bk, d).astype(np.int64) - (1 << (bk - 1))
+        s = self.pool[page, ksc:ksc + 2 * d].copy().view(np.float16)
+        return codes, s
+
+    def write_key_channels(self, page: int, h: int, codes: np.ndarray, s: np.ndarray) -> None:
+        """Key-per-channel mode: store signed codes[16, d] and scales s[d]."""
+        d = self.d
+        bk, _, kc, _, ksc, _ = self._seg(h)
+        nb = d * bk // 8
+        stored = np.asarray(codes, np.int64) + (1 << (bk - 1))
+        self.pool[page, kc:kc + PAGE_SIZE * nb] = pack(stored, bk).reshape(-1)
+        self.pool[page, ksc:ksc + 2 * d] = np.asarray(s, np.float16).view(np.uint8)
 
     def read(self, page: np.ndarray, slot: np.ndarray, h: int, kv: int):
         """(codes uint8[n, d], s fp16[n], z fp16[n]) for arrays of pages/slots."""
         d = self.d
         bk, bv, kc, vc, ksz, vsz = self._seg(h)
+        if self.kpc and kv == 0:
+            raise ValueError("key-per-channel pages: use read/write_key_channels for K")
         b, cbase, sbase = (bk, kc, ksz) if kv == 0 else (bv, vc, vsz)
         nb = d * b // 8
         page = np.asarray(page, dtype=np.int64)
@@ -97,6 +132,8 @@ class PageView:
               s: np.float16, z: np.float16) -> None:
         d = self.d
         bk, bv, kc, vc, ksz, vsz = self._seg(h)
+        if self.kpc and kv == 0:
+            raise ValueError("key-per-channel pages: use read/write_key_channels for K")
         b, cbase, sbase = (bk, kc, ksz) if kv == 0 else (bv, vc, vsz)
         nb = d * b // 8
         self.pool[page, cbase + slot * nb: cbase + (slot + 1) * nb] = pack(codes, b)
@@ -108,6 +145,8 @@ class PageView:
         """Vectorised ``write`` for arrays of pages/slots and codes[n, d]."""
         d = self.d
         bk, bv, kc, vc, ksz, vsz = self._seg(h)
+        if self.kpc and kv == 0:
+            raise ValueError("key-per-channel pages: use read/write_key_channels for K")
         b, cbase, sbase = (bk, kc, ksz) if kv == 0 else (bv, vc, vsz)
         nb = d * b // 8
         pages = np.asarray(pages, dtype=np.int64)

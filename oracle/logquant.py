@@ -48,8 +48,9 @@ def decode(state: CacheState, layer: int, q: np.ndarray, page_table: np.ndarray,
     """o[B, Hq, d] float64: attention over the quantized cache (window 0) in
     which the positions of B use the bf16 keys and values k_bf16, v_bf16
     [B][T][Hkv][d] (the appended tokens, bf16-exact floats)."""
-    if state.window:
-        raise ValueError("the LogQuant reserve replaces the bf16 window: window must be 0")
+    if state.window or state.key_per_channel:
+        raise ValueError("the LogQuant reserve replaces the bf16 window: window must be 0, "
+                         "keys token-wise")
     q = np.asarray(q, dtype=np.float64)
     bsz, hq, d = q.shape
     hkv = state.num_kv_heads

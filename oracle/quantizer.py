@@ -1,4 +1,5 @@
-"""Token-wise asymmetric INT-b quantization with one fp16 scale and zero.
+"""Token-wise asymmetric INT-b quantization with one fp16 scale and zero, and
+the per-channel symmetric key quantizer of the key-per-channel mode.
 
 Sources:
 * "SAW-INT4: System-Aware 4-Bit KV-Cache Quantization for Real-World LLM
@@ -100,3 +101,78 @@ def rotate_and_quantize(x: np.ndarray, block: int, bits: int):
     u32 = rotate(x, block).astype(np.float32)
     c, s, z = quantize(u32, bits)
     return c, s, z, u32
+
+
+# ------------------------------------------------------------------------
+# Per-channel symmetric keys (the key-per-channel mode).
+#
+# Sources:
+# * RateQuant technical summary, Methodology section 3 (K/V decoupling): KIVI
+#   quantizes keys symmetrically per channel and values asymmetrically per
+#   token, so K and V are separate components.
+# * "LogQuant ...", section 5 (implementation): 2-bit quantization with a
+#   key-per-channel strategy.
+#
+# Definition (per group u[n, d] -- the n = 16 tokens of one page of one KV
+# head's keys, after rotation; Q = 2^(b-1) - 1):
+#
+#     s_j = fp16 round-up( max_t |u_tj| / Q )       one scale per channel j
+#     c_tj = round-half-even( u_tj / s_j ),  -Q <= c_tj <= Q
+#     deq_tj = c_tj * s_j
+#
+# Readings of steps the pages leave open:
+# * The group is one page (16 tokens): the pages give no group size, and the
+#   page is the cache's unit of storage.
+# * "Symmetric" means no zero point and the level range [-Q, Q] (2^b - 1
+#   levels; code -2^(b-1) is unused), so 2-bit keys take -1, 0, 1.
+# * The scale is rounded up to fp16, which keeps |u_tj / s_j| <= Q for the
+#   stored scale, hence |u_tj - deq_tj| <= s_j / 2 and no clamp fires.
+# * As for the token-wise rule, the integer decision is taken in float32:
+#   max |u| / Q is a float32 division, and the code is round-half-even of the
+#   exact product u_tj * (1 / s_j) with a float32-rounded reciprocal.
+# * A channel with max |u| = 0 gets s = 0 and codes 0.
+# * In the page a code is stored as c + 2^(b-1) (offset binary, 1 .. 2^b - 1),
+#   packed like the token-wise codes.
+# ------------------------------------------------------------------------
+
+def channel_levels(bits: int) -> int:
+    """Q = 2^(b-1) - 1, the largest code magnitude of the symmetric quantizer."""
+    if bits not in (2, 4, 8):
+        raise ValueError(f"unsupported bit-width {bits}")
+    return (1 << (bits - 1)) - 1
+
+
+def channel_scales(u32: np.ndarray, bits: int) -> np.ndarray:
+    """fp16 s[..., d] per channel for groups u32[..., n, d] (n tokens each)."""
+    u32 = np.asarray(u32, dtype=np.float32)
+    amax = np.abs(u32).max(axis=-2)                              # exact
+    return fp16.round_up((amax / np.float32(channel_levels(bits))).astype(np.float32))
+
+
+def channel_codes_given(u32: np.ndarray, s: np.ndarray, bits: int,
+                        clip: bool = True) -> np.ndarray:
+    """Signed codes int64[..., n, d] of groups u32[..., n, d] for channel scales
+    s[..., d] (``clip=False``: the raw rounded values, for the clamp test)."""
+    u32 = np.asarray(u32, dtype=np.float32)
+    sf = np.asarray(s, dtype=np.float16).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        inv = np.where(sf > 0, (np.float32(1.0) / sf).astype(np.float32), np.float32(0.0))
+    prod = u32.astype(np.float64) * inv.astype(np.float64)[..., None, :]   # exact product
+    c = np.rint(prod).astype(np.int64)                                      # half to even
+    c = np.where((sf > 0)[..., None, :], c, 0)
+    if clip:
+        q = channel_levels(bits)
+        c = np.clip(c, -q, q)
+    return c
+
+
+def quantize_channels(u32: np.ndarray, bits: int):
+    """(signed codes int64[..., n, d], s fp16[..., d]) for float32 groups."""
+    s = channel_scales(u32, bits)
+    return channel_codes_given(u32, s, bits), s
+
+
+def dequantize_channels(codes: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """deq = c * s (per channel) in float64, codes[..., n, d], s[..., d]."""
+    sf = np.asarray(s, dtype=np.float16).astype(np.float64)
+    return np.asarray(codes, dtype=np.float64) * sf[..., None, :]
