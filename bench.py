@@ -35,8 +35,10 @@ from kvq_alloc_bits fed by kvq_distortion + kvq_fit_distortion, at 3.0 and
 128-token bf16 window), "logquant" (the same shape at K2V2 with LogQuant's
 log-spaced bf16 tokens, W = 128) and "quant_error" (error of the cache's
 attention against float64 attention over the original bf16 K/V, with and
-without the rotation, computed with torch on the device).  --only
-{mixed,long,logquant} runs one of them alone over --layers layer caches.
+without the rotation, computed with torch on the device), "key_per_channel"
+(the Llama-3-8B-shaped layer with keys quantized per channel, decode attention
+alone).  --only {mixed,long,logquant,key_channel} runs one of them alone over
+--layers layer caches.
 
 --impl reference times the CPU oracle itself as the reference arm (this
 library has no third-party reference implementation to install).
@@ -467,7 +469,7 @@ def run_kvq(args) -> None:
     # append sweep: 8 sequences x 8192 new tokens into empty caches
     append = append_sweep(kvq, torch, dev) if not args.skip_append else None
     calib = calibration_bench(kvq, torch, dev) if not args.skip_append else None
-    mixed = long_ctx = qerr = lq = None
+    mixed = long_ctx = qerr = lq = kpc = None
     if not args.skip_configs:
         # the mixed-bits allocation takes (alpha, beta) from the calibration
         if calib is not None:
@@ -480,6 +482,7 @@ def run_kvq(args) -> None:
                                      args.warmup)
         long_ctx = long_context_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
         lq = logquant_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
+        kpc = key_channel_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
         qerr = quant_error_report(kvq, torch, dev)
     if calib is not None:
         calib.pop("_alpha")
@@ -522,6 +525,7 @@ def run_kvq(args) -> None:
         "mixed_bits": mixed,
         "long_context": long_ctx,
         "logquant": lq,
+        "key_per_channel": kpc,
         "quant_error": qerr,
     }
     print(json.dumps(line), flush=True)
@@ -621,23 +625,29 @@ def calibration_bench(kvq, torch, dev) -> dict:
 
 
 def graph_step_bench(torch, dev, cache, n_layers, knew, vnew, q_all, pt, after, o_all, ws,
-                     steps, warmup) -> tuple:
-    """Times one step of n_layers fused decode steps (one per layer cache),
-    captured once as a CUDA graph with layer-to-layer launch overlap, and the
-    same launches with events between them.  Returns (ms per step, average
-    isolated launch in ms)."""
+                     steps, warmup, decode_only=False) -> tuple:
+    """Times one step of n_layers fused decode steps (one per layer cache;
+    with decode_only, decode attention alone), captured once as a CUDA graph
+    with layer-to-layer launch overlap, and the same launches with events
+    between them.  Returns (ms per step, average isolated launch in ms)."""
     stream = torch.cuda.Stream(device=dev)
     ev = [(torch.cuda.Event(enable_timing=True, external=True),
            torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n_layers)]
 
+    def layer(l):
+        if decode_only:
+            cache.decode(l, q_all[l], pt, after, o=o_all[l], workspace=ws)
+        else:
+            cache.decode_step(l, knew[l], vnew[l], q_all[l], pt, after, o=o_all[l], workspace=ws)
+
     def step():
         for l in range(n_layers):
-            cache.decode_step(l, knew[l], vnew[l], q_all[l], pt, after, o=o_all[l], workspace=ws)
+            layer(l)
 
     def step_events():
         for l in range(n_layers):
             ev[l][0].record()
-            cache.decode_step(l, knew[l], vnew[l], q_all[l], pt, after, o=o_all[l], workspace=ws)
+            layer(l)
             ev[l][1].record()
 
     with torch.cuda.stream(stream):
@@ -851,6 +861,53 @@ def logquant_bench(kvq, torch, dev, n_layers, steps, warmup, w=128) -> dict:
             "roofline": _roofline(sb, ms, n_layers, iso, per)}
 
 
+def key_channel_bench(kvq, torch, dev, n_layers, steps, warmup) -> dict:
+    """Key-per-channel mode on the Llama-3-8B-shaped decode layer: batch 16,
+    32 query / 8 KV heads, head_dim 128, context 4096, K and V INT4 with
+    Hadamard 128, keys quantized per channel (one fp16 scale per page, head
+    and channel), values token-wise, no window.  One step = decode attention
+    over n_layers distinct layer caches (the append of a step's token is a
+    separate launch in this mode; the decode is the kernel measured)."""
+    w = LLAMA3_8B_LAYER
+    hkv, hq, d, bsz, ctx = w.hkv, w.hq, w.head_dim, w.batch, w.ctx
+    mp = ctx // 16
+    bits = np.full((n_layers, hkv, 2), 4)
+    cache = kvq.Cache(n_layers, hkv, d, w.had_block, bits, bsz * mp, max_batch=bsz, device=dev,
+                      overlap=True, key_per_channel=True)
+    pt = torch.from_numpy(page_table(w.seed, bsz, mp)).to(dev)
+    zero = torch.zeros(bsz, dtype=torch.int32, device=dev)
+    for half in range(2):          # the inputs for 8 sequences at a time, shared by the layers
+        rows = slice(8 * half, 8 * half + 8)
+        k = kv_tokens(w.seed, 0, 8, ctx, hkv, d, w.k_outliers, w.outlier_lo, w.outlier_hi, seq0=8 * half)
+        v = kv_tokens(w.seed, 1, 8, ctx, hkv, d, w.v_outliers, w.outlier_lo, w.outlier_hi, seq0=8 * half)
+        kd = torch.from_numpy(k).to(dev).to(torch.bfloat16)
+        vd = torch.from_numpy(v).to(dev).to(torch.bfloat16)
+        del k, v
+        for l in range(n_layers):
+            cache.append(l, kd, vd, pt[rows].contiguous(), zero[rows].contiguous(), window_row=8 * half)
+        del kd, vd
+    q_all = torch.from_numpy(np.stack([queries(w.seed, l, bsz, hq, d, False)
+                                       for l in range(n_layers)])).to(dev).to(torch.bfloat16)
+    o_all = torch.empty((n_layers, bsz, hq, d), dtype=torch.float32, device=dev)
+    lens = torch.full((bsz,), ctx, dtype=torch.int32, device=dev)
+    ws = cache.workspace(bsz, hq, mp)
+    torch.cuda.synchronize(dev)
+    ms, iso = graph_step_bench(torch, dev, cache, n_layers, None, None, q_all, pt, lens, o_all,
+                               ws, steps, warmup, decode_only=True)
+    seg = cache.page_bytes[0] // hkv                     # one (page, head) segment
+    per = bsz * mp * hkv * seg + bsz * hq * d * (2 + 4) + bsz * mp * 4
+    sb = per * n_layers
+    del cache
+    return {"workload": f"key-per-channel: batch {bsz} x {ctx} tokens, {hq} q / {hkv} KV heads, "
+                        f"head_dim {d}, K4 per channel / V4 per token, Hadamard {w.had_block}, "
+                        f"{n_layers} layer caches",
+            "step": "per layer: kvq_decode_attn (cluster merge; the window CTA covers the "
+                    "open page)",
+            "bytes_per_token_head": seg // 16,
+            "ms_per_step": round(ms, 4), "GB_per_step": round(sb / 1e9, 4),
+            "roofline": _roofline(sb, ms, n_layers, iso, per)}
+
+
 def _exact_attention_torch(torch, q, k, v, scale):
     """softmax(q k^T scale) v in float64 on the device for one KV head:
     q [G, d], k/v [T, d] (bf16 values)."""
@@ -927,8 +984,10 @@ def run_section(args) -> None:
                                args.warmup, n_layers=N_LAYERS)
     elif args.only == "long":
         out = long_context_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
-    else:
+    elif args.only == "logquant":
         out = logquant_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
+    else:
+        out = key_channel_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
     print(json.dumps({"section": args.only, **out}), flush=True)
 
 
@@ -942,7 +1001,8 @@ def main() -> None:
     ap.add_argument("--skip-append", action="store_true")
     ap.add_argument("--skip-configs", action="store_true",
                     help="leave out the mixed-bits, long-context and quantization-error sections")
-    ap.add_argument("--only", default="all", choices=["all", "mixed", "long", "logquant"],
+    ap.add_argument("--only", default="all",
+                    choices=["all", "mixed", "long", "logquant", "key_channel"],
                     help="run one section alone and print it (profiling a small case)")
     ap.add_argument("--layers", type=int, default=32,
                     help="distinct layer caches per step (profiling uses a small case)")

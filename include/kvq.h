@@ -86,17 +86,19 @@ typedef struct kvq_cache {
   int had_block;             /* Hadamard block n: 32, 64 or 128, dividing head_dim;
                                 1 = no rotation (u = x), the plain token-wise quantizer
                                 that the SAW-INT4 page contrasts with the rotated one */
-  int window;                /* R: bf16 recent-token window (0 = none), 0 .. 4096 */
+  int window;                /* R: bf16 recent-token window (0 = none), 0 .. 1024 */
   int max_batch;             /* sequences addressable in each window buffer */
   int num_pages;             /* physical pages in each layer pool */
   const int8_t* bits_host;   /* host [num_layers][num_kv_heads][2] (bK, bV), each 2, 4 or 8 */
   void* const* layer_pools;  /* host array [num_layers] of device pointers, each
                                 num_pages * kvq_page_bytes(layer) bytes, 16-byte aligned */
   void* const* window_bufs;  /* host array [num_layers] of device pointers to bf16
-                                [max_batch][Hkv][2][R][head_dim] (window R > 0), or to the
+                                [max_batch][Hkv][2][R][head_dim] (window R > 0), to the
                                 LogQuant reserve [max_batch][Hkv][2][kvq_logquant_rows(W)]
-                                [head_dim] (logquant_w = W > 0), kvq_window_bytes() bytes
-                                each; NULL when neither is used.  Sequence b of a call
+                                [head_dim] (logquant_w = W > 0), or to the key-per-channel
+                                ring [max_batch][Hkv][2][R + 16][head_dim] (key_per_channel,
+                                any R), kvq_window_bytes() bytes each; NULL when none of
+                                them is used.  Sequence b of a call
                                 uses row b; a call for a subset of a batch (e.g. a
                                 one-sequence prefill) passes a descriptor whose pointers
                                 are offset to its rows. */
@@ -104,7 +106,34 @@ typedef struct kvq_cache {
   int launch_flags;          /* 0 or KVQ_LAUNCH_OVERLAP (decode calls only) */
   int logquant_w;            /* 0, or W: LogQuant log-spaced full-precision tokens with
                                 base window W, a power of two in [2, 256]; needs window 0 */
+  int key_per_channel;       /* 0, or 1: keys quantized symmetrically per channel, one fp16
+                                scale per (page, KV head, channel) (see below); not with
+                                logquant_w */
 } kvq_cache;
+
+/*
+ * Key-per-channel mode (key_per_channel = 1).  Follows the RateQuant technical
+ * summary, Methodology section 3 (KIVI quantizes keys symmetrically per channel
+ * and values asymmetrically per token) and "LogQuant ...", section 5 (2-bit
+ * quantization with a key-per-channel strategy).  The 16 keys of a page form a
+ * group (a reading: the pages give no group size): after the rotation,
+ *   s_j = fp16_round_up(max_t |u_tj| / Q),  Q = 2^(bK-1) - 1,
+ *   c_tj = round_half_even(u_tj * (1 / s_j))  in [-Q, Q],   deq_tj = c_tj * s_j,
+ * with max |u| / Q and 1 / s rounded to fp32; s_j = 0 gives c = 0.  Values keep
+ * the token-wise rule.  A page is quantized once all of its positions have left
+ * the window: with length L, positions 0 .. Q(L) - 1 are quantized, Q(L) =
+ * 16 floor(max(L - R, 0) / 16), and positions Q(L) .. L - 1 (at most R + 15)
+ * keep bf16 K and V in a ring of R + 16 rows, slot p % (R + 16), so the mode
+ * needs window_bufs even with R = 0.  Page segment of head h:
+ *   K codes  [16][head_dim * bK / 8]   stored c + 2^(bK-1), packed as above
+ *   V codes  [16][head_dim * bV / 8]
+ *   K scales [head_dim] x fp16
+ *   V (s, z) [16] x {fp16 s, fp16 z}
+ * page_bytes(l) = sum_h (16 * head_dim * (bK_h + bV_h) / 8 + 2 * head_dim + 64).
+ * kvq_append quantizes the pages the append completes, then writes the new bf16
+ * rows (two launches); kvq_decode_step runs the append of its token and then
+ * the decode (two launches).
+ */
 
 /*
  * LogQuant mode (logquant_w = W > 0).  Follows "LogQuant: Log-Distributed
@@ -130,9 +159,9 @@ int kvq_logquant_rows(int w);
  * W is not a power of two in [2, 256] or n < 0. */
 long long kvq_logquant_members(long long n, int w, long long* positions, long long max);
 
-/* Bytes of window_bufs[layer] this descriptor needs (the bf16 window or the
- * LogQuant reserve, for max_batch sequences); 0 when it needs none or on a bad
- * descriptor. */
+/* Bytes of window_bufs[layer] this descriptor needs (the bf16 window, the
+ * LogQuant reserve or the key-per-channel ring, for max_batch sequences); 0 when
+ * it needs none or on a bad descriptor. */
 size_t kvq_window_bytes(const kvq_cache* cache);
 
 /*
@@ -174,8 +203,12 @@ size_t kvq_page_bytes(const kvq_cache* cache, int layer);
  * positions are copied to the ring.  In LogQuant mode every token is quantized,
  * and the members of B after the append get their bf16 rows in the reserve
  * (one more launch first moves the older members that this append's halvings
- * thin out of the reserve's ring).  Two appends to one sequence must be
- * stream-ordered.  Returns KVQ_OK once the kernels are enqueued.
+ * thin out of the reserve's ring).  In the key-per-channel mode a page is
+ * quantized when the append completes it and all of its positions have left
+ * the window (rows of older positions come from the ring), and the appended
+ * positions from max(seq_lens[b], Q(L)) on are copied to the ring (a second
+ * launch).  Two appends to one sequence must be stream-ordered.  Returns
+ * KVQ_OK once the kernels are enqueued.
  */
 kvq_status kvq_append(const kvq_cache* cache, int layer, const void* K, const void* V,
                       const int32_t* page_table, int max_pages, const int32_t* seq_lens,
@@ -205,7 +238,9 @@ size_t kvq_decode_workspace_bytes(const kvq_cache* cache, int B, int Hq, int max
  *   workspace    device, ws_bytes >= kvq_decode_workspace_bytes(cache, B, Hq,
  *                max_pages), 16-byte aligned, zero-filled before its first use.
  * In LogQuant mode the quantized splits leave out the members of B and one more
- * CTA per (sequence, KV head) attends over their bf16 rows in the reserve.
+ * CTA per (sequence, KV head) attends over their bf16 rows in the reserve.  In
+ * the key-per-channel mode the splits read each page's channel scales and one
+ * more CTA attends over the ring's positions Q(L) .. L - 1.
  * One kernel launch.  Returns KVQ_OK once enqueued.
  */
 kvq_status kvq_decode_attn(const kvq_cache* cache, int layer, const void* q, int q_is_fp32,
@@ -233,8 +268,11 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, int layer, const void* q, int
  * and the token it replaces (position len - 1 - R, if any) is quantized into
  * its page slot.  In LogQuant mode it is quantized into its page slot and its
  * bf16 rows enter the reserve; when this token fills B to 3W, the halving's
- * block moves from the reserve's ring to its level buffer in the same launch.  Two steps on one cache must be stream-ordered.  One kernel
- * launch.  Returns KVQ_OK once enqueued.
+ * block moves from the reserve's ring to its level buffer in the same launch.
+ * In the key-per-channel mode the step is kvq_append of the token (whose page,
+ * once complete and out of the window, is quantized) followed by the decode:
+ * three launches.  Two steps on one cache must be stream-ordered.  Otherwise
+ * one kernel launch.  Returns KVQ_OK once enqueued.
  */
 kvq_status kvq_decode_step(const kvq_cache* cache, int layer, const void* K_new,
                            const void* V_new, const void* q, int q_is_fp32,

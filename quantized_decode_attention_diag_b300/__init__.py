@@ -57,6 +57,7 @@ class kvq_cache(ctypes.Structure):
         ("status_dev", ctypes.c_void_p),
         ("launch_flags", ctypes.c_int),
         ("logquant_w", ctypes.c_int),
+        ("key_per_channel", ctypes.c_int),
     ]
 
 
@@ -286,12 +287,13 @@ class Cache:
 
     ``bits`` is an int array [num_layers][num_kv_heads][2] of (bK, bV).
     Pools are uint8 [num_pages * page_bytes(layer)]; window buffers are bf16
-    [max_batch][Hkv][2][window][head_dim]; the status word is one int32.
+    [max_batch][Hkv][2][rows][head_dim] with rows the window R, the LogQuant
+    reserve's rows, or R + 16 with per-channel keys; the status word is one int32.
     """
 
     def __init__(self, num_layers: int, num_kv_heads: int, head_dim: int, had_block: int,
                  bits, num_pages: int, window: int = 0, max_batch: int = 0, device="cuda",
-                 overlap: bool = False, logquant_w: int = 0):
+                 overlap: bool = False, logquant_w: int = 0, key_per_channel: bool = False):
         import torch
         self.bits = np.ascontiguousarray(np.asarray(bits).reshape(num_layers, num_kv_heads, 2),
                                          dtype=np.int8)
@@ -303,7 +305,9 @@ class Cache:
         d.num_layers, d.num_kv_heads, d.head_dim, d.page_size = num_layers, num_kv_heads, head_dim, 16
         d.had_block, d.window, d.max_batch, d.num_pages = had_block, window, max_batch, num_pages
         d.logquant_w = logquant_w
+        d.key_per_channel = 1 if key_per_channel else 0
         self.logquant_w = logquant_w
+        self.key_per_channel = bool(key_per_channel)
         d.bits_host = self.bits.ctypes.data_as(ctypes.POINTER(ctypes.c_int8))
         self.page_bytes = [kvq_page_bytes(d, l) for l in range(num_layers)]
         self.pools = [torch.zeros(num_pages * pb, dtype=torch.uint8, device=device)
@@ -312,8 +316,8 @@ class Cache:
         d.layer_pools = self._pool_ptrs
         self.windows = None
         self._win_ptrs = None
-        if window or logquant_w:
-            rows = window if window else kvq_logquant_rows(logquant_w)
+        if window or logquant_w or key_per_channel:
+            rows = self.ring_rows
             self.windows = [torch.zeros((max_batch, num_kv_heads, 2, rows, head_dim),
                                         dtype=torch.bfloat16, device=device)
                             for _ in range(num_layers)]
@@ -341,10 +345,17 @@ class Cache:
         kvq_append(desc, layer, K, V, page_table, int(page_table.shape[1]), seq_lens, B, T,
                    stream)
 
+    @property
+    def ring_rows(self) -> int:
+        """Rows per (sequence, KV head, K|V) of the window buffers."""
+        if self.logquant_w:
+            return kvq_logquant_rows(self.logquant_w)
+        return self.window + 16 if self.key_per_channel else self.window
+
     def _shifted(self, row: int) -> kvq_cache:
         """A copy of the descriptor whose window buffers start at window row `row`."""
         d = kvq_cache.from_buffer_copy(self.desc)
-        rows = self.window if self.window else kvq_logquant_rows(self.logquant_w)
+        rows = self.ring_rows
         step = self.num_kv_heads * 2 * rows * self.head_dim * 2
         self._tmp_win = (ctypes.c_void_p * self.num_layers)(
             *[w.data_ptr() + row * step for w in self.windows])

@@ -58,6 +58,10 @@ kvq_status check_geometry(const kvq_cache* c, int layer, kvq::LayerGeom* geom) {
     if (c->window != 0)
       return fail(KVQ_EINVAL, "logquant_w %d needs window 0 (got %d)", c->logquant_w, c->window);
   }
+  if (c->key_per_channel != 0 && c->key_per_channel != 1)
+    return fail(KVQ_EINVAL, "key_per_channel must be 0 or 1 (got %d)", c->key_per_channel);
+  if (c->key_per_channel && c->logquant_w)
+    return fail(KVQ_EUNSUPPORTED, "key_per_channel is not built together with logquant_w");
   if (c->num_pages < 1) return fail(KVQ_EINVAL, "num_pages must be >= 1");
   if (!c->bits_host) return fail(KVQ_EINVAL, "bits_host is NULL");
   kvq::LayerGeom local;
@@ -72,7 +76,9 @@ kvq_status check_geometry(const kvq_cache* c, int layer, kvq::LayerGeom* geom) {
       if (b != 2 && b != 4 && b != 8)
         return fail(KVQ_EUNSUPPORTED, "bits %d of layer %d head %d not built (2, 4, 8)", b,
                     layer, h);
-    const int hb = kvq::kPage * (c->head_dim * (bk + bv) / 8 + 8);
+    const int hb = c->key_per_channel
+                       ? kvq::kPage * (c->head_dim * (bk + bv) / 8) + 2 * c->head_dim + 4 * kvq::kPage
+                       : kvq::kPage * (c->head_dim * (bk + bv) / 8 + 8);
     g->head_off[h] = static_cast<int>(off);
     g->bits[h][0] = static_cast<int8_t>(bk);
     g->bits[h][1] = static_cast<int8_t>(bv);
@@ -84,6 +90,19 @@ kvq_status check_geometry(const kvq_cache* c, int layer, kvq::LayerGeom* geom) {
   return KVQ_OK;
 }
 
+// The descriptor uses window_bufs: a bf16 window, the LogQuant reserve or the
+// key-per-channel ring.
+bool uses_ring(const kvq_cache* c) {
+  return c->window > 0 || c->logquant_w > 0 || c->key_per_channel;
+}
+
+// Rows of the bf16 ring per (sequence, KV head, K|V): R, or R + 16 in the
+// key-per-channel mode (the page still being filled waits there).
+int ring_rows(const kvq_cache* c) { return c->key_per_channel ? c->window + kvq::kPage : c->window; }
+
+// Decode kernel instantiation: 0 token-wise, 1 LogQuant, 2 key-per-channel.
+int decode_mode(const kvq_cache* c) { return c->logquant_w ? 1 : c->key_per_channel ? 2 : 0; }
+
 // check_geometry plus the device pointers of `layer`.
 kvq_status check_cache(const kvq_cache* c, int layer, kvq::LayerGeom* geom) {
   const kvq_status st = check_geometry(c, layer, geom);
@@ -94,12 +113,14 @@ kvq_status check_cache(const kvq_cache* c, int layer, kvq::LayerGeom* geom) {
     return fail(KVQ_EINVAL, "layer_pools[%d] is NULL", layer);
   if (!aligned(c->layer_pools[layer], 16))
     return fail(KVQ_EINVAL, "layer_pools[%d] is not 16-byte aligned", layer);
-  if (c->window > 0 || c->logquant_w > 0) {
+  if (uses_ring(c)) {
     if (c->max_batch < 1)
-      return fail(KVQ_EINVAL, "max_batch must be >= 1 with a window or a LogQuant reserve");
+      return fail(KVQ_EINVAL,
+                  "max_batch must be >= 1 with a window, a LogQuant reserve or per-channel keys");
     if (!c->window_bufs || !c->window_bufs[layer])
-      return fail(KVQ_EINVAL, "window_bufs[%d] is NULL but window = %d, logquant_w = %d", layer,
-                  c->window, c->logquant_w);
+      return fail(KVQ_EINVAL,
+                  "window_bufs[%d] is NULL but window = %d, logquant_w = %d, key_per_channel = %d",
+                  layer, c->window, c->logquant_w, c->key_per_channel);
     if (!aligned(c->window_bufs[layer], 16))
       return fail(KVQ_EINVAL, "window_bufs[%d] is not 16-byte aligned", layer);
   }
@@ -149,16 +170,18 @@ kvq_status plan_decode(const kvq_cache* c, const kvq::LayerGeom& g, int B, int m
   kvq::DecodeParams probe;
   std::memset(&probe, 0, sizeof probe);
   probe.stage_bytes = (g.max_head_bytes + 127) / 128 * 128;
-  probe.R = c->window;
+  probe.R = ring_rows(c);
   probe.lq_w = c->logquant_w;
+  probe.kpc = c->key_per_channel;
   const size_t smem = kvq::decode_smem_bytes(probe, c->head_dim);
   static thread_local int cache_key[4] = {0, 0, 0, 0}, cache_val[4] = {0, 0, 0, 0};
-  const int key = (static_cast<int>(smem) * 2 + (c->head_dim == 128)) * 2 + (c->logquant_w > 0);
+  const int mode = decode_mode(c);
+  const int key = (static_cast<int>(smem) * 2 + (c->head_dim == 128)) * 4 + mode + 1;
   int bps = 0;
   for (int i = 0; i < 4; ++i)
     if (cache_key[i] == key) bps = cache_val[i];
   if (!bps) {
-    bps = kvq::decode_blocks_per_sm(c->head_dim, smem, c->logquant_w > 0);
+    bps = kvq::decode_blocks_per_sm(c->head_dim, smem, mode);
     if (bps <= 0)
       return fail(KVQ_ECUDA, "decode kernel cannot be resident with %zu bytes of shared memory",
                   smem);
@@ -170,9 +193,9 @@ kvq_status plan_decode(const kvq_cache* c, const kvq::LayerGeom& g, int B, int m
     cache_val[0] = bps;
   }
   const long long units = static_cast<long long>(B) * c->num_kv_heads;
-  // with a window (or a LogQuant reserve), each unit's window CTA takes one of
-  // the wave's slots
-  const int extra = (c->window > 0 || c->logquant_w > 0) ? 1 : 0;
+  // with a window (a LogQuant reserve, a key-per-channel ring), each unit's
+  // window CTA takes one of the wave's slots
+  const int extra = uses_ring(c) ? 1 : 0;
   long long s = static_cast<long long>(sms) * bps / units - extra;
   const long long cap = (max_pages + 7) / 8;
   if (s > cap) s = cap;
@@ -200,10 +223,11 @@ kvq_status set_last_error(kvq_status status, const char* message) {
 
 namespace {
 
+// check_only: every host check, no launch.
 kvq_status decode_impl(const kvq_cache* cache, int layer, const void* K_new, const void* V_new,
                        const void* q, int q_is_fp32, const int32_t* page_table, int max_pages,
                        const int32_t* seq_lens, int B, int Hq, float softmax_scale, float* o,
-                       void* workspace, size_t ws_bytes, void* stream) {
+                       void* workspace, size_t ws_bytes, void* stream, bool check_only = false) {
   kvq::DecodeParams p;
   std::memset(&p, 0, sizeof p);
   kvq_status st = check_cache(cache, layer, &p.geom);
@@ -224,8 +248,10 @@ kvq_status decode_impl(const kvq_cache* cache, int layer, const void* K_new, con
   const int G = Hq / hkv;
   if (G != 1 && G != 2 && G != 4)
     return fail(KVQ_EUNSUPPORTED, "GQA group %d not built (1, 2, 4)", G);
-  if ((cache->window > 0 || cache->logquant_w > 0) && B > cache->max_batch)
+  if (uses_ring(cache) && B > cache->max_batch)
     return fail(KVQ_EINVAL, "B %d exceeds the window buffers' max_batch %d", B, cache->max_batch);
+  if (step && cache->key_per_channel)
+    return fail(KVQ_EINVAL, "key-per-channel decode steps append before the decode");
   if (!std::isfinite(softmax_scale) || softmax_scale < 0.f)
     return fail(KVQ_EINVAL, "softmax_scale must be finite and >= 0");
   Plan pl;
@@ -236,9 +262,7 @@ kvq_status decode_impl(const kvq_cache* cache, int layer, const void* K_new, con
   const float scale =
       softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cache->head_dim));
   p.pool = static_cast<const uint8_t*>(cache->layer_pools[layer]);
-  p.window = (cache->window > 0 || cache->logquant_w > 0)
-                 ? static_cast<const uint16_t*>(cache->window_bufs[layer])
-                 : nullptr;
+  p.window = uses_ring(cache) ? static_cast<const uint16_t*>(cache->window_bufs[layer]) : nullptr;
   p.q = q;
   p.page_table = page_table;
   p.seq_lens = seq_lens;
@@ -252,7 +276,8 @@ kvq_status decode_impl(const kvq_cache* cache, int layer, const void* K_new, con
   p.Hq = Hq;
   p.Hkv = hkv;
   p.G = G;
-  p.R = cache->window;
+  p.R = ring_rows(cache);
+  p.kpc = cache->key_per_channel;
   p.lq_w = cache->logquant_w;
   p.lq_a = cache->logquant_w ? kvq::lq_log2(cache->logquant_w) : 0;
   p.lq_rows = cache->logquant_w ? kvq::lq_rows(cache->logquant_w, p.lq_a) : 0;
@@ -269,6 +294,7 @@ kvq_status decode_impl(const kvq_cache* cache, int layer, const void* K_new, con
   p.step = step ? 1 : 0;
   p.k_new = static_cast<const uint16_t*>(K_new);
   p.v_new = static_cast<const uint16_t*>(V_new);
+  if (check_only) return KVQ_OK;
   const cudaError_t e = kvq::launch_decode(p, cache->head_dim, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "decode launch: %s", cudaGetErrorString(e));
   return KVQ_OK;
@@ -284,9 +310,15 @@ size_t kvq_page_bytes(const kvq_cache* cache, int layer) {
   return static_cast<size_t>(g.page_bytes);
 }
 
-kvq_status kvq_append(const kvq_cache* cache, int layer, const void* K, const void* V,
-                      const int32_t* page_table, int max_pages, const int32_t* seq_lens, int B,
-                      int T_new, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// kvq_append; lens_after: seq_lens already count the T_new tokens (a
+// key-per-channel decode step).
+kvq_status append_impl(const kvq_cache* cache, int layer, const void* K, const void* V,
+                       const int32_t* page_table, int max_pages, const int32_t* seq_lens, int B,
+                       int T_new, int lens_after, void* stream) {
   kvq::AppendParams p;
   std::memset(&p, 0, sizeof p);
   kvq_status st = check_cache(cache, layer, &p.geom);
@@ -303,14 +335,12 @@ kvq_status kvq_append(const kvq_cache* cache, int layer, const void* K, const vo
   if (max_pages < 1) return fail(KVQ_EINVAL, "max_pages must be >= 1");
   if (static_cast<long long>(B) * T_new > (1ll << 28))
     return fail(KVQ_EINVAL, "B * T_new too large");
-  if ((cache->window > 0 || cache->logquant_w > 0) && B > cache->max_batch)
+  if (uses_ring(cache) && B > cache->max_batch)
     return fail(KVQ_EINVAL, "B %d exceeds the window buffers' max_batch %d", B, cache->max_batch);
   p.K = static_cast<const uint16_t*>(K);
   p.V = static_cast<const uint16_t*>(V);
   p.pool = static_cast<uint8_t*>(cache->layer_pools[layer]);
-  p.window = (cache->window > 0 || cache->logquant_w > 0)
-                 ? static_cast<uint16_t*>(cache->window_bufs[layer])
-                 : nullptr;
+  p.window = uses_ring(cache) ? static_cast<uint16_t*>(cache->window_bufs[layer]) : nullptr;
   p.page_table = page_table;
   p.seq_lens = seq_lens;
   p.status = cache->status_dev;
@@ -318,18 +348,37 @@ kvq_status kvq_append(const kvq_cache* cache, int layer, const void* K, const vo
   p.B = B;
   p.T = T_new;
   p.Hkv = cache->num_kv_heads;
-  p.R = cache->window;
+  p.R = ring_rows(cache);
   p.num_pages = cache->num_pages;
   p.warps_per_group = static_cast<int>((static_cast<long long>(B) * T_new + 15) / 16);
   p.lq_w = cache->logquant_w;
   p.lq_a = cache->logquant_w ? kvq::lq_log2(cache->logquant_w) : 0;
   p.lq_rows = cache->logquant_w ? kvq::lq_rows(cache->logquant_w, p.lq_a) : 0;
+  p.kpc = cache->key_per_channel;
+  p.lens_after = lens_after;
+  if (p.kpc) {
+    if (B > 65535) return fail(KVQ_EUNSUPPORTED, "B %d above the grid limit 65535", B);
+    const cudaError_t e = kvq::launch_kpc_append(p, cache->head_dim, cache->had_block,
+                                                 static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(KVQ_ECUDA, "append launch: %s", cudaGetErrorString(e));
+    return KVQ_OK;
+  }
   cudaError_t e = cudaSuccess;
   if (p.lq_w) e = kvq::launch_lq_carry(p, cache->head_dim, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "LogQuant carry launch: %s", cudaGetErrorString(e));
   e = kvq::launch_append(p, cache->head_dim, cache->had_block, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "append launch: %s", cudaGetErrorString(e));
   return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_append(const kvq_cache* cache, int layer, const void* K, const void* V,
+                      const int32_t* page_table, int max_pages, const int32_t* seq_lens, int B,
+                      int T_new, void* stream) {
+  return append_impl(cache, layer, K, V, page_table, max_pages, seq_lens, B, T_new, 0, stream);
 }
 
 int kvq_logquant_rows(int w) {
@@ -360,7 +409,8 @@ size_t kvq_window_bytes(const kvq_cache* cache) {
   const size_t planes = static_cast<size_t>(cache->max_batch) * cache->num_kv_heads * 2;
   if (cache->logquant_w > 0)
     return planes * static_cast<size_t>(kvq_logquant_rows(cache->logquant_w)) * per_row;
-  if (cache->window > 0) return planes * static_cast<size_t>(cache->window) * per_row;
+  if (cache->window > 0 || cache->key_per_channel)
+    return planes * static_cast<size_t>(ring_rows(cache)) * per_row;
   return 0;
 }
 
@@ -394,6 +444,20 @@ kvq_status kvq_decode_step(const kvq_cache* cache, int layer, const void* K_new,
                            const int32_t* seq_lens, int B, int Hq, float softmax_scale, float* o,
                            void* workspace, size_t ws_bytes, void* stream) {
   if (!K_new || !V_new) return fail(KVQ_EINVAL, "K_new and V_new must be non-NULL");
+  if (cache && cache->key_per_channel == 1) {
+    // the token's page is quantized (once complete) by the append; then the
+    // decode, whose arguments are checked before anything is launched
+    kvq_status st = decode_impl(cache, layer, nullptr, nullptr, q, q_is_fp32, page_table,
+                                max_pages, seq_lens, B, Hq, softmax_scale, o, workspace, ws_bytes,
+                                stream, true);
+    if (st != KVQ_OK) return st;
+    if (!aligned(K_new, 16) || !aligned(V_new, 16))
+      return fail(KVQ_EINVAL, "K_new and V_new must be 16-byte aligned");
+    st = append_impl(cache, layer, K_new, V_new, page_table, max_pages, seq_lens, B, 1, 1, stream);
+    if (st != KVQ_OK) return st;
+    return decode_impl(cache, layer, nullptr, nullptr, q, q_is_fp32, page_table, max_pages,
+                       seq_lens, B, Hq, softmax_scale, o, workspace, ws_bytes, stream);
+  }
   return decode_impl(cache, layer, K_new, V_new, q, q_is_fp32, page_table, max_pages, seq_lens, B,
                      Hq, softmax_scale, o, workspace, ws_bytes, stream);
 }

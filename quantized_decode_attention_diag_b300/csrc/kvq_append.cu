@@ -20,6 +20,7 @@
 // computed on packed fp32 pairs, packed by shifted sums and written with
 // 16-byte stores.
 #include <climits>
+#include <type_traits>
 
 #include "kvq_logquant.h"
 #include "kvq_quant.cuh"
@@ -316,6 +317,161 @@ __global__ void __launch_bounds__(128) lq_carry_kernel(const __grid_constant__ A
   }
 }
 
+// ---------------------------------------------------- key-per-channel mode
+// RateQuant technical summary, Methodology section 3 (KIVI: symmetric
+// per-channel keys, asymmetric per-token values); "LogQuant ...", section 5
+// (key-per-channel).  A page is quantized once all its 16 positions have left
+// the window: the quantized prefix of length L is Q(L) = 16 floor(max(L - R,
+// 0) / 16), and positions Q(L) .. L - 1 keep bf16 rows in a ring of R + 16 rows
+// (p.R here), slot p mod (R + 16).
+__device__ __forceinline__ int kpc_prefix(int len, int ring) {
+  return kPage * (max(0, len - (ring - kPage)) / kPage);
+}
+
+// Sequence length before the append (p.lens_after: seq_lens already count the
+// appended tokens, as in a decode step).
+__device__ __forceinline__ int append_len0(const AppendParams& p, int b) {
+  return __ldg(p.seq_lens + b) - (p.lens_after ? p.T : 0);
+}
+
+// The bf16 row of position pos of (b, h, kv): the ring (older than the
+// append) or the appended input.
+template <int D>
+__device__ __forceinline__ const uint16_t* kpc_row(const AppendParams& p, int b, int h, int kv,
+                                                   int pos, int l0) {
+  if (pos < l0)
+    return p.window + ((static_cast<size_t>(b) * p.Hkv + h) * 2 + kv) * p.R * D +
+           static_cast<size_t>(pos % p.R) * D;
+  return (kv ? p.V : p.K) + ((static_cast<size_t>(b) * p.T + (pos - l0)) * p.Hkv + h) * D;
+}
+
+// One CTA per (page completed by this append, KV head, sequence); warp 0
+// quantizes the page's 16 keys per channel, warp 1 its 16 values token-wise.
+// Lanes 2 r and 2 r + 1 hold halves of token r (the append's layout).  Keys:
+// the rotated halves go to shared memory, lane j forms the scale of channels
+// j, j + 32, ... (max |u| over the 16 tokens / (2^(b-1) - 1), fp16 rounded up)
+// and its fp32 reciprocal, then every lane codes its own half.
+template <int D, int NB>
+__global__ void __launch_bounds__(64) kpc_page_kernel(const __grid_constant__ AppendParams p) {
+  constexpr int E = D / 2;
+  constexpr int LD = D + 4;                    // padded row of the key buffer (floats)
+  __shared__ __align__(16) float kbuf[kPage * LD];
+  __shared__ float invs[D];
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, r = lane >> 1, u = lane & 1;
+  const int l0 = append_len0(p, b), len = l0 + p.T;
+  if (l0 < 0 || static_cast<long long>(len) > static_cast<long long>(p.max_pages) * kPage) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(p.status, KVQ_DEV_BAD_LENGTH);
+    return;
+  }
+  const int pg = kpc_prefix(l0, p.R) / kPage + static_cast<int>(blockIdx.x);
+  if (pg >= kpc_prefix(len, p.R) / kPage) return;
+  const int pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
+  if (pid < 0 || pid >= p.num_pages) {
+    if (threadIdx.x == 0) flag_status(p.status, KVQ_DEV_BAD_PAGE);
+    return;
+  }
+  const int bk = p.geom.bits[h][0], bv = p.geom.bits[h][1];
+  const int kb = D * bk / 8, vb = D * bv / 8;
+  uint8_t* seg = p.pool + static_cast<size_t>(pid) * p.geom.page_bytes + p.geom.head_off[h];
+  const int kv = warp;
+  const uint16_t* src = kpc_row<D>(p, b, h, kv, pg * kPage + r, l0);
+  float v[E];
+  if constexpr (NB > E) load_row_top<D>(src, u, v);
+  else load_half_row<D>(src, u, v);
+
+  if (kv == 1) {                               // values: the token-wise rule
+    uint8_t* vsz = seg + kPage * (kb + vb) + 2 * D + r * 4;
+    auto quant = [&](auto bits_tag) {
+      constexpr int BITS = decltype(bits_tag)::value;
+      constexpr int NW = D * BITS / 64;
+      uint32_t words[NW];
+      __half sh, zh;
+      rotate_quantize_half<D, NB, BITS>(v, u, words, sh, zh);
+      store_code_words<NW>(seg + kPage * kb + r * (D * BITS / 8) + u * (D * BITS / 16), words);
+      if (u == 0) {
+        *reinterpret_cast<uint32_t*>(vsz) = pack_half2(sh, zh);
+        if (!(isfinite(__half2float(sh)) && isfinite(__half2float(zh))))
+          flag_status(p.status, KVQ_DEV_NONFINITE);
+      }
+    };
+    if (bv == 2) quant(std::integral_constant<int, 2>{});
+    else if (bv == 4) quant(std::integral_constant<int, 4>{});
+    else quant(std::integral_constant<int, 8>{});
+    return;
+  }
+
+  // keys: per-channel scales over the page's 16 tokens
+  rotate_half<D, NB>(v);
+#pragma unroll
+  for (int i = 0; i < E / 4; ++i)
+    *reinterpret_cast<float4*>(kbuf + r * LD + u * E + 4 * i) =
+        make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  __syncwarp();
+  const float qmax = static_cast<float>((1 << (bk - 1)) - 1);
+  __half* scales = reinterpret_cast<__half*>(seg + kPage * (kb + vb));
+  bool bad = false;
+#pragma unroll
+  for (int m = 0; m < D / 32; ++m) {
+    const int ch = lane + 32 * m;
+    float amax = 0.f;
+#pragma unroll
+    for (int t = 0; t < kPage; ++t) amax = fmaxf(amax, fabsf(kbuf[t * LD + ch]));
+    const __half sh = __float2half_ru(__fdiv_rn(amax, qmax));
+    const float sf = __half2float(sh);
+    bad |= !isfinite(sf);
+    scales[ch] = sh;
+    invs[ch] = sf > 0.f ? __frcp_rn(sf) : 0.f;
+  }
+  if (bad) flag_status(p.status, KVQ_DEV_NONFINITE);
+  __syncwarp();
+  auto codes = [&](auto bits_tag) {
+    constexpr int BITS = decltype(bits_tag)::value;
+    constexpr int NW = D * BITS / 64;
+    uint32_t words[NW];
+    quantize_channels_half<D, BITS>(v, invs + u * E, words);
+    store_code_words<NW>(seg + r * (D * BITS / 8) + u * (D * BITS / 16), words);
+  };
+  if (bk == 2) codes(std::integral_constant<int, 2>{});
+  else if (bk == 4) codes(std::integral_constant<int, 4>{});
+  else codes(std::integral_constant<int, 8>{});
+}
+
+// After kpc_page_kernel: the appended positions that stay in bf16 (from
+// max(l0, Q(len)) on) into the ring.  Grid (rows / 4, Hkv, B), one warp per
+// position copying its K and V rows.
+template <int D>
+__global__ void __launch_bounds__(128) kpc_ring_kernel(const __grid_constant__ AppendParams p) {
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int l0 = append_len0(p, b), len = l0 + p.T;
+  if (l0 < 0 || static_cast<long long>(len) > static_cast<long long>(p.max_pages) * kPage) return;
+  const int pos = max(l0, kpc_prefix(len, p.R)) + static_cast<int>(blockIdx.x) * 4 + warp;
+  if (pos >= len) return;
+  constexpr int C = D / 8;                     // 16-byte chunks per row
+  for (int idx = lane; idx < 2 * C; idx += 32) {
+    const int kv = idx / C, ci = idx - kv * C;
+    const uint4* from = reinterpret_cast<const uint4*>(
+        (kv ? p.V : p.K) + ((static_cast<size_t>(b) * p.T + (pos - l0)) * p.Hkv + h) * D);
+    uint4* to = reinterpret_cast<uint4*>(p.window + ((static_cast<size_t>(b) * p.Hkv + h) * 2 + kv) *
+                                                        p.R * D +
+                                         static_cast<size_t>(pos % p.R) * D);
+    to[ci] = from[ci];
+  }
+}
+
+template <int D, int NB>
+cudaError_t launch_kpc(const AppendParams& p, cudaStream_t s) {
+  // pages a sequence can complete: (T + 15) / 16 + 1; rows it can keep: R + 15
+  const int pages = (p.T + kPage - 1) / kPage + 1;
+  kpc_page_kernel<D, NB><<<dim3(pages, p.Hkv, p.B), 64, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int rows = min(p.T, p.R - 1);
+  kpc_ring_kernel<D><<<dim3((rows + 3) / 4, p.Hkv, p.B), 128, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 int sm_count_cached() {
   static int cached[64] = {0};
   int dev = 0;
@@ -358,6 +514,20 @@ cudaError_t launch_lq_carry(const AppendParams& p, int head_dim, cudaStream_t s)
   else if (head_dim == 64) lq_carry_kernel<64><<<grid, 128, 0, s>>>(p);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
+}
+
+cudaError_t launch_kpc_append(const AppendParams& p, int head_dim, int had_block, cudaStream_t s) {
+  if (head_dim == 128) {
+    if (had_block == 128) return launch_kpc<128, 128>(p, s);
+    if (had_block == 64) return launch_kpc<128, 64>(p, s);
+    if (had_block == 32) return launch_kpc<128, 32>(p, s);
+    if (had_block == 1) return launch_kpc<128, 1>(p, s);
+  } else if (head_dim == 64) {
+    if (had_block == 64) return launch_kpc<64, 64>(p, s);
+    if (had_block == 32) return launch_kpc<64, 32>(p, s);
+    if (had_block == 1) return launch_kpc<64, 1>(p, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_append(const AppendParams& p, int head_dim, int had_block, cudaStream_t s) {

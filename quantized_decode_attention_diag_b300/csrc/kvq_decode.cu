@@ -56,6 +56,10 @@ namespace kvq {
 namespace {
 
 constexpr int kThreads = kDecodeWarps * 32;
+// kernel instantiations: token-wise keys and values, LogQuant, key-per-channel
+constexpr int kModeTokenWise = 0;
+constexpr int kModeLogQuant = 1;
+constexpr int kModeKeyChannel = 2;
 constexpr int kMaxSplits = 256;
 constexpr int kMaxCluster = 4;    // largest cluster the merge uses (CTA 0 holds its partials)
 constexpr float kMaxSlack = 8.f;  // p <= 2^kMaxSlack under the lazy running maximum
@@ -77,12 +81,17 @@ struct Smem {
 template <int D>
 __host__ __device__ constexpr int merge_floats() { return kDecodeWarps * kMaxGroup * (D + 2); }
 
-__host__ __device__ constexpr int header_bytes(int d) {
+// alias_merge (the key-per-channel kernel): the warps' merge region shares
+// the stage area instead of having its own, so that four CTAs of the larger
+// page segments still fit an SM.  Its first write comes after the barrier at
+// which every warp is done with its stages (or with the window's rows).
+__host__ __device__ constexpr int header_bytes(int d, bool alias_merge = false) {
   return ((d * kMaxGroup * 4 + 64 + kDecodeWarps * kDecodeStages * 8 +
-           (kDecodeWarps + 1 + kMaxCluster) * kMaxGroup * (d + 2) * 4) + 127) / 128 * 128 + 128;
+           ((alias_merge ? 0 : kDecodeWarps) + 1 + kMaxCluster) * kMaxGroup * (d + 2) * 4) +
+          127) / 128 * 128 + 128;
 }
 
-template <int D>
+template <int D, bool ALIAS_MERGE = false>
 __device__ __forceinline__ Smem carve(uint8_t* base) {
   Smem s;
   s.qtab = reinterpret_cast<float*>(base);
@@ -94,11 +103,12 @@ __device__ __forceinline__ Smem carve(uint8_t* base) {
   s.qscl = reinterpret_cast<float*>(misc + 32);
   s.bars = reinterpret_cast<uint64_t*>(misc + 64);
   s.merge = reinterpret_cast<float*>(misc + 64 + kDecodeWarps * kDecodeStages * 8);
-  s.cpart = s.merge + merge_floats<D>();
+  s.cpart = ALIAS_MERGE ? s.merge : s.merge + merge_floats<D>();
   // then rbuf [kMaxCluster][kMaxGroup * (D + 2)] (cluster mode, CTA 0: every
   // CTA's partial, pushed there through distributed shared memory; see rbuf())
   uint8_t* a = reinterpret_cast<uint8_t*>(s.cpart + (1 + kMaxCluster) * kMaxGroup * (D + 2));
   s.area = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(a) + 127) & ~uintptr_t(127));
+  if (ALIAS_MERGE) s.merge = reinterpret_cast<float*>(s.area);
   return s;
 }
 
@@ -179,6 +189,42 @@ __device__ __forceinline__ uint32_t kpair(const uint32_t* w, int i) {
     }
   } else {
     return h2_sub1024(__byte_perm(w[i >> 1], 0x64646464u, (i & 1) ? 0x4342 : 0x4140));
+  }
+}
+
+// Key-per-channel mode: the stored field is c + 2^(BITS-1) (offset binary);
+// the same LOP3 and one HSUB / HFMA whose constant also takes off 2^(BITS-1)
+// give the signed code c exactly.
+__device__ __forceinline__ uint32_t h2_sub(uint32_t x, float c) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&x), __half2(__half(c), __half(c)));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+template <int K>
+__device__ __forceinline__ uint32_t h2_unscale_off(uint32_t x, float off) {
+  constexpr float inv = 1.0f / float(1 << K);
+  const float c = -1024.0f / float(1 << K) - off;
+  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&x), __half2(__half(inv), __half(inv)),
+                      __half2(__half(c), __half(c)));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+template <int BITS>
+__device__ __forceinline__ uint32_t kpair_signed(const uint32_t* w, int i) {
+  constexpr float off = float(1 << (BITS - 1));
+  if constexpr (BITS == 4) {
+    const uint32_t x = (i & 2) ? (w[i >> 2] >> 8) : w[i >> 2];
+    return (i & 1) ? h2_unscale_off<4>(lop_or_magic(x, 0x00f000f0u), off)
+                   : h2_sub(lop_or_magic(x, 0x000f000fu), 1024.f + off);
+  } else if constexpr (BITS == 2) {
+    const int k = i & 7;
+    const uint32_t x = (k & 4) ? (w[i >> 3] >> 8) : w[i >> 3];
+    switch (k & 3) {
+      case 0: return h2_sub(lop_or_magic(x, 0x00030003u), 1024.f + off);
+      case 1: return h2_unscale_off<2>(lop_or_magic(x, 0x000c000cu), off);
+      case 2: return h2_unscale_off<4>(lop_or_magic(x, 0x00300030u), off);
+      default: return h2_unscale_off<6>(lop_or_magic(x, 0x00c000c0u), off);
+    }
+  } else {
+    return h2_sub(__byte_perm(w[i >> 1], 0x64646464u, (i & 1) ? 0x4342 : 0x4140), 1024.f + off);
   }
 }
 
@@ -344,7 +390,9 @@ __device__ __forceinline__ uint32_t hilo_pair(float x) {
 // (hi = fp16(x), lo = fp16(x - hi)) stay normal and together carry ~22 bits
 // of x.  Writes qtab[i][d] = the packed pair (hi, lo) (as raw bits),
 // qsum[i] = e_i sum_d q''_d and qscl[i] = 1 / e_i.
-template <int D>
+// RAW (key-per-channel mode): qtab[i][d] = e_i q''_d as fp32 instead of the
+// packed pair; the B fragments are formed per page with its channel scales.
+template <int D, bool RAW = false>
 __device__ void query_quant_prologue(const DecodeParams& p, const Smem& sm, float (&v)[D / 32]) {
   constexpr int E = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -371,7 +419,7 @@ __device__ void query_quant_prologue(const DecodeParams& p, const Smem& sm, floa
   const float scl = ldexpf(1.f, ex);
   uint32_t* qt = reinterpret_cast<uint32_t*>(sm.qtab) + warp * D + E * lane;
 #pragma unroll
-  for (int e = 0; e < E; ++e) qt[e] = hilo_pair(v[e] * scl);
+  for (int e = 0; e < E; ++e) qt[e] = RAW ? __float_as_uint(v[e] * scl) : hilo_pair(v[e] * scl);
   if (lane == 0) {
     sm.qsum[warp] = s * scl;
     sm.qscl[warp] = ldexpf(1.f, -ex);
@@ -563,12 +611,16 @@ __device__ __forceinline__ void patch_stage(uint32_t st, const uint8_t* pbuf, in
 // of the quantized part; warp w takes pages w, w + 4, ... two at a time.
 // LQ: LogQuant mode -- the members of B (full precision, attended by the
 // reserve split) are left out here, on the rounds whose pages can hold one.
-template <int D, int BK, int BV, bool LQ>
+template <int D, int BK, int BV, int MODE>
 __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h, int split,
                             int lq, float (&qv)[D / 32], int chunk0, uint32_t (&tok)[D / 32]) {
+  constexpr bool LQ = MODE == kModeLogQuant;
+  constexpr bool KPC = MODE == kModeKeyChannel;
   constexpr int KB = D * BK / 8;                 // K code bytes per token
   constexpr int VB = D * BV / 8;
-  constexpr int CHUNK = kPage * (KB + VB + 8);   // one (page, head) segment
+  // one (page, head) segment: codes, then K (s, z) per token or K scales per
+  // channel, then V (s, z) per token
+  constexpr int CHUNK = KPC ? kPage * (KB + VB) + 2 * D + 4 * kPage : kPage * (KB + VB + 8);
   constexpr int NJ = D / 16;                     // MMAs along d
   constexpr int KSLICE = KB / 4;                 // bytes of a token row per k-slot group
   constexpr int VSLICE = VB / 8;                 // bytes of a token row per dim group
@@ -579,8 +631,8 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   static_assert((BV == 2 ? 16 : BV == 4 ? 8 : 4) * VWORDS >= 2 * NJ, "value slice too small");
   constexpr int NST = kDecodeStages;
   static_assert(NST % 2 == 0, "stages are consumed in pairs");
-  constexpr uint32_t KSZ = kPage * (KB + VB);    // offset of the K (s, z) pairs
-  constexpr uint32_t VSZ = KSZ + 4 * kPage;      // offset of the V (s, z) pairs
+  constexpr uint32_t KSZ = kPage * (KB + VB);    // offset of the K (s, z) pairs or scales
+  constexpr uint32_t VSZ = KSZ + (KPC ? 2 * D : 4 * kPage);  // offset of the V (s, z) pairs
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -657,7 +709,7 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   // quantizes the token there while its first copies are in flight
   int kpatch = -1;
   uint8_t* pbuf = reinterpret_cast<uint8_t*>(sm.merge);
-  if (p.step && lq > 0) {
+  if (!KPC && p.step && lq > 0) {   // (the key-per-channel mode appends before the launch)
     const int pl = npages - 1;
     if (pl >= pg0 && pl < pg1 && (pl - pg0) % kDecodeWarps == warp) {
       kpatch = (pl - pg0) / kDecodeWarps;
@@ -666,12 +718,13 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   }
   const int pslot = (lq - 1) % kPage;
 
-  query_quant_prologue<D>(p, sm, qv);
+  query_quant_prologue<D, KPC>(p, sm, qv);
 
   // ---- B fragments of the K-side MMA: column n = g is query head g / 2, its
-  //      hi part for even g and lo part for odd g
+  //      hi part for even g and lo part for odd g (per page in the
+  //      key-per-channel mode)
   uint32_t bq[NJ][2];
-  {
+  if constexpr (!KPC) {
     const uint32_t* qh = reinterpret_cast<const uint32_t*>(sm.qtab) + (g >> 1) * D;
     const int sh = (g & 1) ? 16 : 0;
 #pragma unroll
@@ -714,6 +767,58 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     }
     sc0 = __fmaf_rn(k0.x, a[0] + a[1], k0.y * qs);
     sc1 = __fmaf_rn(k1.x, a[2] + a[3], k1.y * qs);
+  };
+  // key-per-channel mode: score = sum_d (e q''_d) s_d c_d with the page's
+  // channel scales s_d.  Column g of the B fragments takes head g / 2's
+  // x_d = (e q''_d)(s_d 2^-E), hi part (even g) or lo part (odd g), where 2^E
+  // is the binade of the page's largest scale (x < 2^15 stays inside fp16);
+  // the scaled score is (a0 + a1) 2^E.  Codes are signed, no zero term.
+  constexpr int QD = D / 4;                      // dims of a k-slot group
+  auto scores_kpc = [&](uint32_t st, float& sc0, float& sc1) {
+    uint32_t w0[KWORDS], w1[KWORDS];
+    lds_u32<KSLICE>(st + koff, w0);
+    lds_u32<KSLICE>(st + koff + 8 * KB, w1);
+    uint32_t sw[QD / 2];                         // scales of dims [c QD, (c + 1) QD)
+#pragma unroll
+    for (int i = 0; i < QD / 16; ++i) lds_u32<32>(st + KSZ + c * (QD * 2) + 32 * i, sw + 8 * i);
+    uint32_t mx = sw[0];                         // scales are >= 0: fp16 bits order them
+#pragma unroll
+    for (int i = 1; i < QD / 2; ++i) mx = __vmaxu2(mx, sw[i]);
+    mx = max(mx & 0xffffu, mx >> 16);
+    mx = max(mx, __shfl_xor_sync(kFullMask, mx, 1));
+    mx = max(mx, __shfl_xor_sync(kFullMask, mx, 2));
+    const int ex = max(static_cast<int>(mx >> 10), 1) - 15;    // subnormal: -14
+    const float down = __int_as_float((127 - ex) << 23), up = __int_as_float((127 + ex) << 23);
+    float qf[QD];
+    const uint32_t qa = smem_u32(sm.qtab + (g >> 1) * D + c * QD);
+#pragma unroll
+    for (int i = 0; i < QD / 4; ++i)
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(qf[4 * i]), "=f"(qf[4 * i + 1]), "=f"(qf[4 * i + 2]), "=f"(qf[4 * i + 3])
+                   : "r"(qa + 16 * i));
+    auto bfrag = [&](int i) -> uint32_t {
+      int d0, d1;
+      kpair_dims<D, BK>(0, i, d0, d1);           // dims within the group
+      const float s0 = __half2float(__ushort_as_half(static_cast<unsigned short>(
+                           sw[d0 >> 1] >> (16 * (d0 & 1)))));
+      const float s1 = __half2float(__ushort_as_half(static_cast<unsigned short>(
+                           sw[d1 >> 1] >> (16 * (d1 & 1)))));
+      const float x0 = qf[d0] * (s0 * down), x1 = qf[d1] * (s1 * down);
+      const __half2 hi = __floats2half2_rn(x0, x1);
+      const float2 hf = __half22float2(hi);
+      const __half2 lo = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+      const __half2 r = (g & 1) ? lo : hi;
+      return *reinterpret_cast<const uint32_t*>(&r);
+    };
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const uint32_t x[4] = {kpair_signed<BK>(w0, 2 * j), kpair_signed<BK>(w1, 2 * j),
+                             kpair_signed<BK>(w0, 2 * j + 1), kpair_signed<BK>(w1, 2 * j + 1)};
+      mma_16816(a, x, bfrag(2 * j), bfrag(2 * j + 1));
+    }
+    sc0 = (a[0] + a[1]) * up;
+    sc1 = (a[2] + a[3]) * up;
   };
   // p s -> B fragments of the V-side MMA (via two 8x8 transposes); l, zacc.
   // With `guard`, a token with p = 0 (masked) contributes nothing even if its
@@ -779,8 +884,13 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   auto round = [&](uint32_t sta, bool has_b, bool mask, int tok_a) {
     const uint32_t stb = sta + stage_bytes;
     float sa0, sa1, sb0 = -CUDART_INF_F, sb1 = -CUDART_INF_F;
-    scores(sta, sa0, sa1);
-    if (has_b) scores(stb, sb0, sb1);
+    if constexpr (KPC) {
+      scores_kpc(sta, sa0, sa1);
+      if (has_b) scores_kpc(stb, sb0, sb1);
+    } else {
+      scores(sta, sa0, sa1);
+      if (has_b) scores(stb, sb0, sb1);
+    }
     if (mask) {
       const int tok_b = tok_a + kDecodeWarps * kPage;
       if (excluded(tok_a + g)) sa0 = -CUDART_INF_F;
@@ -885,8 +995,10 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     if (!__all_sync(kFullMask, ok)) {
       timed_out = true;
     } else {
-      if (kpatch >= 0 && (kpatch - k) >= 0 && (kpatch - k) < (has_b ? 2 : 1))
-        patch_stage<D, BK, BV>(st0 + (sa + kpatch - k) * stage_bytes, pbuf, pslot);
+      if constexpr (!KPC) {
+        if (kpatch >= 0 && (kpatch - k) >= 0 && (kpatch - k) < (has_b ? 2 : 1))
+          patch_stage<D, BK, BV>(st0 + (sa + kpatch - k) * stage_bytes, pbuf, pslot);
+      }
       round(st0 + sa * stage_bytes, has_b, last_partial || LQ,
             (first + kDecodeWarps * k) * kPage);
     }
@@ -1089,6 +1201,9 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nw = len - lq;
   const int R = p.R;
+  // the key-per-channel ring (R + 16 rows) holds positions lq .. len - 1 at
+  // slots p % R: a run of nw slots from lq % R that may wrap around the end
+  const int s0 = p.kpc ? lq % R : 0;
   const uint16_t* kring = p.window + ((static_cast<size_t>(b) * p.Hkv + h) * 2 + 0) * R * D;
   const uint16_t* vring = kring + static_cast<size_t>(R) * D;
   const int snew = (p.step && nw > 0) ? (len - 1) % R : -1;
@@ -1103,7 +1218,12 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
     __syncthreads();                    // everyone is done with buf
     if (tid == 0) {
       mbar_expect_tx(bar, static_cast<unsigned>(n) * D * 2);
-      bulk_g2s(buf, plane + static_cast<size_t>(c0) * D, static_cast<unsigned>(n) * D * 2, bar);
+      const int first = (s0 + c0) % R;
+      const int n1 = min(n, R - first); // rows before the ring's end
+      bulk_g2s(buf, plane + static_cast<size_t>(first) * D, static_cast<unsigned>(n1) * D * 2, bar);
+      if (n1 < n)
+        bulk_g2s(buf + static_cast<size_t>(n1) * D, plane, static_cast<unsigned>(n - n1) * D * 2,
+                 bar);
     }
     if (!mbar_wait_bounded(bar, ph)) {
       if (tid == 0) flag_status(p.status, KVQ_DEV_COPY_TIMEOUT);
@@ -1445,12 +1565,12 @@ __device__ __forceinline__ void push_partial(const Smem& sm, uint32_t rank) {
 }
 
 // -------------------------------------------------------------- the kernel --
-// LQ: LogQuant mode (its own instantiation, so that the ordinary kernel's
-// code is untouched by the masking and the reserve split).
-template <int D, bool LQ>
+// MODE: token-wise, LogQuant or key-per-channel, each its own instantiation,
+// so that the token-wise kernel's code is untouched by the other modes.
+template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  const Smem sm = carve<D>(smem_raw);
+  const Smem sm = carve<D, MODE == kModeKeyChannel>(smem_raw);
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5;
 
@@ -1472,7 +1592,11 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
     if (tid == 0) flag_status(p.status, KVQ_DEV_BAD_LENGTH);
     len = 0;
   }
-  const int lq = p.R ? max(0, len - p.R) : len;
+  // quantized prefix: the tokens before the window, or (key-per-channel, a
+  // ring of R + 16 rows) the pages that lie wholly before the last R tokens
+  const int lq = MODE == kModeKeyChannel ? kPage * (max(0, len - (p.R - kPage)) / kPage)
+                 : p.R                   ? max(0, len - p.R)
+                                         : len;
   const bool is_window = split >= p.S;
 
   if (tid == 0) {
@@ -1483,7 +1607,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
   }
   __syncthreads();
 
-  if (LQ && is_window) {
+  if (MODE == kModeLogQuant && is_window) {
     grid_wait();
     if (p.overlap) load_query<D>(p, b, h, qv);
     query_window_prologue<D>(p, sm, qv);
@@ -1494,7 +1618,8 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
     // for K and V, before the wait (a hint; L2 is coherent with the writes
     // of the previous kernel)
     if (tid == 0 && len > 0) {
-      const int nw = len - lq;
+      // (the key-per-channel ring's run may wrap: the whole ring)
+      const int nw = MODE == kModeKeyChannel ? p.R : len - lq;
       const uint16_t* kring = p.window + (static_cast<size_t>(b) * p.Hkv + h) * 2 * p.R * D;
       const uint32_t bytes = static_cast<uint32_t>(nw) * D * 2;
       l2_prefetch_bulk(kring, bytes);
@@ -1507,15 +1632,15 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
   } else {
     const int bk = p.geom.bits[h][0], bv = p.geom.bits[h][1];
     switch (bk * 16 + bv) {
-      case 0x22: quant_split<D, 2, 2, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x24: quant_split<D, 2, 4, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x28: quant_split<D, 2, 8, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x42: quant_split<D, 4, 2, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x44: quant_split<D, 4, 4, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x48: quant_split<D, 4, 8, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x82: quant_split<D, 8, 2, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x84: quant_split<D, 8, 4, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x88: quant_split<D, 8, 8, LQ>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x22: quant_split<D, 2, 2, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x24: quant_split<D, 2, 4, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x28: quant_split<D, 2, 8, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x42: quant_split<D, 4, 2, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x44: quant_split<D, 4, 4, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x48: quant_split<D, 4, 8, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x82: quant_split<D, 8, 2, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x84: quant_split<D, 8, 4, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x88: quant_split<D, 8, 8, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
       default: break;
     }
     __syncthreads();   // the warps' partials are in the merge region
@@ -1558,12 +1683,17 @@ size_t smem_bytes(const DecodeParams& p) {
   // member list [3W]
   const size_t win = p.lq_w ? static_cast<size_t>(kMaxGroup + 1) * 3 * p.lq_w * 4
                             : (p.R > 0 ? win_bytes(p.R, D) : 0);
+  if (p.kpc) {   // the merge region lives in the stage area
+    const size_t merge = static_cast<size_t>(merge_floats<D>()) * 4;
+    const size_t area = stages > win ? stages : win;
+    return header_bytes(D, true) + (area > merge ? area : merge);
+  }
   return header_bytes(D) + (stages > win ? stages : win);
 }
 
-// Lets decode_kernel<D, LQ> use up to the device's opt-in shared memory (set
+// Lets decode_kernel<D, MODE> use up to the device's opt-in shared memory (set
 // once per device; never lowered, so any smaller size launches too).
-template <int D, bool LQ>
+template <int D, int MODE>
 cudaError_t allow_smem() {
   static int done[64] = {0};
   int dev = 0;
@@ -1573,17 +1703,17 @@ cudaError_t allow_smem() {
   int optin = 0;
   e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_kernel<D, LQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(decode_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            optin);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
   return e;
 }
 
-template <int D, bool LQ>
+template <int D, int MODE>
 cudaError_t launch_d(const DecodeParams& p, cudaStream_t s) {
   const size_t bytes = smem_bytes<D>(p);
   if (bytes > 48 * 1024) {
-    const cudaError_t e = allow_smem<D, LQ>();
+    const cudaError_t e = allow_smem<D, MODE>();
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -1607,16 +1737,30 @@ cudaError_t launch_d(const DecodeParams& p, cudaStream_t s) {
   }
   cfg.attrs = n ? attr : nullptr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<D, LQ>, p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, MODE>, p);
 }
 
-template <int D, bool LQ>
+template <int D, int MODE>
 int blocks_per_sm(size_t smem) {
   int n = 0;
-  cudaError_t e = allow_smem<D, LQ>();
+  cudaError_t e = allow_smem<D, MODE>();
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, LQ>, kThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, MODE>, kThreads, smem);
   return e == cudaSuccess ? n : -1;
+}
+
+template <int D>
+int blocks_per_sm_mode(size_t smem, int mode) {
+  return mode == kModeLogQuant    ? blocks_per_sm<D, kModeLogQuant>(smem)
+         : mode == kModeKeyChannel ? blocks_per_sm<D, kModeKeyChannel>(smem)
+                                   : blocks_per_sm<D, kModeTokenWise>(smem);
+}
+
+template <int D>
+cudaError_t launch_mode(const DecodeParams& p, cudaStream_t s) {
+  return p.lq_w  ? launch_d<D, kModeLogQuant>(p, s)
+         : p.kpc ? launch_d<D, kModeKeyChannel>(p, s)
+                 : launch_d<D, kModeTokenWise>(p, s);
 }
 
 }  // namespace
@@ -1624,9 +1768,8 @@ int blocks_per_sm(size_t smem) {
 int decode_max_splits() { return kMaxSplits; }
 int decode_max_cluster() { return kMaxCluster; }
 
-int decode_blocks_per_sm(int head_dim, size_t smem, bool logquant) {
-  if (head_dim == 128) return logquant ? blocks_per_sm<128, true>(smem) : blocks_per_sm<128, false>(smem);
-  return logquant ? blocks_per_sm<64, true>(smem) : blocks_per_sm<64, false>(smem);
+int decode_blocks_per_sm(int head_dim, size_t smem, int mode) {
+  return head_dim == 128 ? blocks_per_sm_mode<128>(smem, mode) : blocks_per_sm_mode<64>(smem, mode);
 }
 
 size_t decode_smem_bytes(const DecodeParams& p, int head_dim) {
@@ -1634,8 +1777,8 @@ size_t decode_smem_bytes(const DecodeParams& p, int head_dim) {
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, cudaStream_t s) {
-  if (head_dim == 128) return p.lq_w ? launch_d<128, true>(p, s) : launch_d<128, false>(p, s);
-  if (head_dim == 64) return p.lq_w ? launch_d<64, true>(p, s) : launch_d<64, false>(p, s);
+  if (head_dim == 128) return launch_mode<128>(p, s);
+  if (head_dim == 64) return launch_mode<64>(p, s);
   return cudaErrorInvalidValue;
 }
 

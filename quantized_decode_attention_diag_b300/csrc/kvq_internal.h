@@ -35,6 +35,8 @@ struct AppendParams {
   int warps_per_group;           // ceil(B * T / 16)
   int lq_w, lq_a, lq_rows;       // LogQuant base window W (0: off), log2 W, reserve rows
                                  // per plane; `window` is then the reserve
+  int kpc;                       // key-per-channel mode: R is then the ring's R + 16 rows
+  int lens_after;                // 1: seq_lens already count the T appended tokens
   LayerGeom geom;
 };
 
@@ -65,6 +67,8 @@ struct DecodeParams {
                                  // split after the S quantized ones is the reserve's
   int wait_log2;                 // the main loop gives up on a page copy after
                                  // ~2^wait_log2 cycles (31 unless debugging)
+  int kpc;                       // key-per-channel mode: per-channel K scales in the
+                                 // pages; R is the ring's R + 16 rows; never a step
   LayerGeom geom;
 };
 
@@ -97,10 +101,15 @@ cudaError_t launch_append(const AppendParams& p, int head_dim, int had_block, cu
 // LogQuant mode, before the append: the reserve's older members that the
 // append's halvings thin move from the ring to their level buffers.
 cudaError_t launch_lq_carry(const AppendParams& p, int head_dim, cudaStream_t s);
+// Key-per-channel mode: quantizes the pages the append completes (keys per
+// channel, values token-wise), then writes the positions that stay in bf16
+// into the ring (two launches, in this order).
+cudaError_t launch_kpc_append(const AppendParams& p, int head_dim, int had_block, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, cudaStream_t s);
 size_t decode_smem_bytes(const DecodeParams& p, int head_dim);
-int decode_blocks_per_sm(int head_dim, size_t smem, bool logquant);   // resident CTAs per SM,
-                                                                     // -1 on error
+// resident CTAs per SM of the decode kernel (mode: 0 token-wise, 1 LogQuant,
+// 2 key-per-channel), -1 on error
+int decode_blocks_per_sm(int head_dim, size_t smem, int mode);
 int decode_max_splits();
 int decode_max_cluster();                               // largest cluster the merge uses
 

@@ -65,23 +65,13 @@ __device__ __forceinline__ void load_row_top(const uint16_t* row, int u, float (
   }
 }
 
-// Rotates the vector held by the lane pair (lane ^ 1 is the partner; every
-// lane of the warp must call this) and quantizes it: this lane's packed codes
-// (half u of the row, D * BITS / 16 bytes as 32-bit words), and the pair's
-// fp16 scale and zero.  When the block spans both halves (NB > D / 2) the
-// caller has applied the top stage already (load_row_top); the other stages
-// then stay inside the lane.
-template <int D, int NB, int BITS>
-__device__ __forceinline__ void rotate_quantize_half(float (&v)[D / 2], int u,
-                                                     uint32_t (&words)[D * BITS / 64], __half& sh,
-                                                     __half& zh) {
+// The Sylvester butterflies of the stages inside a lane's half (natural
+// order: stage hs pairs (i, i + hs); NB == 1: no rotation, u = x).  When the
+// block spans both halves (NB > D / 2) the caller has applied the top stage
+// already (load_row_top).
+template <int D, int NB>
+__device__ __forceinline__ void rotate_half(float (&v)[D / 2]) {
   constexpr int E = D / 2;                 // elements per lane
-  constexpr int M = (1 << BITS) - 1;
-  constexpr int NW = D * BITS / 64;        // 32-bit words per lane
-  constexpr int CPW = 32 / BITS;           // codes per word
-
-  // ---- Sylvester butterflies, natural order: stage hs pairs (i, i + hs)
-  // (NB == 1: no rotation, u = x)
   constexpr int IN_REG = NB < E ? NB : E;
   if constexpr (NB >= 2) {
 #pragma unroll
@@ -98,6 +88,24 @@ __device__ __forceinline__ void rotate_quantize_half(float (&v)[D / 2], int u,
       if (!(e & hs)) addsub2(v[e], v[e + 1], v[e + hs], v[e + hs + 1]);
     }
   }
+}
+
+// Rotates the vector held by the lane pair (lane ^ 1 is the partner; every
+// lane of the warp must call this) and quantizes it: this lane's packed codes
+// (half u of the row, D * BITS / 16 bytes as 32-bit words), and the pair's
+// fp16 scale and zero.  When the block spans both halves (NB > D / 2) the
+// caller has applied the top stage already (load_row_top); the other stages
+// then stay inside the lane.
+template <int D, int NB, int BITS>
+__device__ __forceinline__ void rotate_quantize_half(float (&v)[D / 2], int u,
+                                                     uint32_t (&words)[D * BITS / 64], __half& sh,
+                                                     __half& zh) {
+  constexpr int E = D / 2;                 // elements per lane
+  constexpr int M = (1 << BITS) - 1;
+  constexpr int NW = D * BITS / 64;        // 32-bit words per lane
+  constexpr int CPW = 32 / BITS;           // codes per word
+
+  rotate_half<D, NB>(v);
 
   // ---- per-vector min / max over both lanes (eight independent chains: min
   //      and max are exact, so the order does not matter)
@@ -154,6 +162,33 @@ __device__ __forceinline__ void rotate_quantize_half(float (&v)[D / 2], int u,
     words[w] = acc;
   }
   (void)M;
+}
+
+// Key-per-channel mode: this lane's packed codes of its E = D / 2 rotated
+// values for the page's channel reciprocals inv[] (dims [u E, u E + E)): code
+// round-half-even(v * inv) stored as c + 2^(BITS-1), by the magic-number add
+// (the offset is even, so ties still go to the even code).  The scale rounded
+// up keeps |v * inv| <= 2^(BITS-1) - 1 + 2^-20, so no clamp is needed.
+template <int D, int BITS>
+__device__ __forceinline__ void quantize_channels_half(const float (&v)[D / 2], const float* inv,
+                                                       uint32_t (&words)[D * BITS / 64]) {
+  constexpr int NW = D * BITS / 64;
+  constexpr int CPW = 32 / BITS;
+  constexpr float kMagicOff = kMagicRound + float(1 << (BITS - 1));
+  constexpr uint32_t kMagicBits = 0x4B400000u;
+  uint32_t ksum = 0;
+#pragma unroll
+  for (int i = 0; i < CPW; ++i) ksum += kMagicBits << (BITS * i);
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    uint32_t acc = 0u - ksum;
+#pragma unroll
+    for (int i = 0; i < CPW; ++i) {
+      const float f = __fmaf_rn(v[w * CPW + i], inv[w * CPW + i], kMagicOff);
+      acc += __float_as_uint(f) << (BITS * i);
+    }
+    words[w] = acc;
+  }
 }
 
 // Stores this lane's packed code words (NW of them) at dst (16-, 8- or

@@ -14,6 +14,8 @@ Codes and scale/zero ("bit-exact except at rounding boundaries"):
     rounding error of u and z, carried into units of codes); such flips must
     be fewer than 1e-5 of all codes (a sample of fewer than 1e5 codes may
     hold one).
+Per-channel keys (key-per-channel mode): the channel scale and the signed
+codes by the same boundary rules (compare_key_channels).
 Attention outputs: max |o_gpu - o_oracle| <= 2e-3 and mean <= 2e-4 (fp32
 accumulation), with the oracle run over the GPU-written cache.
 """
@@ -38,9 +40,13 @@ def _near_fp16_boundary(x: np.ndarray) -> np.ndarray:
 
 
 def compare_written(gpu_pool: np.ndarray, written: dict, page_table: np.ndarray, d: int,
-                    bits: np.ndarray) -> dict:
-    """Check what the GPU wrote for every (b, h, kv) the oracle append wrote."""
-    view = layout.PageView(gpu_pool, d, bits)
+                    bits: np.ndarray, kpc: bool = False) -> dict:
+    """Check what the GPU wrote for every (b, h, kv) the oracle append wrote
+    (in the key-per-channel mode: the values; the keys go to
+    compare_key_channels)."""
+    view = layout.PageView(gpu_pool, d, bits, kpc)
+    if kpc:
+        written = {key: val for key, val in written.items() if key[2] == 1}
     stats = dict(vectors=0, codes=0, flips=0, sz_boundary=0)
     for (b, h, kv), (pos, codes, s, z, u32) in written.items():
         if len(pos) == 0:
@@ -95,4 +101,47 @@ def compare_outputs(o_gpu: np.ndarray, o_ref: np.ndarray, rows=None) -> dict:
     assert np.isfinite(o_gpu[mask]).all(), "non-finite GPU output"
     assert stats["max_abs"] <= O_MAX_ABS, stats
     assert stats["mean_abs"] <= O_MEAN_ABS, stats
+    return stats
+
+
+def compare_key_channels(gpu_pool: np.ndarray, written: dict, page_table: np.ndarray, d: int,
+                         bits: np.ndarray) -> dict:
+    """Key-per-channel mode: the GPU's channel scales and signed key codes of
+    every page the oracle append quantized, by the same rules as the token-wise
+    codes -- the scale bit-exact except where max |u| / Q lies within 1e-6 of an
+    fp16 grid point, and, given the GPU's scale, each code equal to
+    round-half-even(u / s) except by +-1 within the 1e-6 band of a half-integer."""
+    view = layout.PageView(gpu_pool, d, bits, kpc=True)
+    stats = dict(pages=0, codes=0, flips=0, s_boundary=0)
+    for (b, h, kv), (pos, codes, s, _, u32) in written.items():
+        if kv != 0 or len(pos) == 0:
+            continue
+        b_ = int(bits[h, 0])
+        q = np.float32(quantizer.channel_levels(b_))
+        groups = u32.reshape(-1, 16, d)
+        for i, p0 in enumerate(pos[::16]):
+            pg = int(page_table[b, p0 // 16])
+            gc, gs = view.read_key_channels(pg, h)
+            g = groups[i]
+            same = gs.view(np.uint16) == s[i].view(np.uint16)
+            if not same.all():
+                quo = (np.abs(g).max(axis=0) / q).astype(np.float32)
+                assert _near_fp16_boundary(quo[~same]).all(), (
+                    f"channel scale mismatch away from an fp16 boundary at b={b} h={h} "
+                    f"page {p0 // 16} channels {np.nonzero(~same)[0][:5]}")
+                stats["s_boundary"] += int((~same).sum())
+            want = quantizer.channel_codes_given(g, gs, b_)
+            diff = gc - want
+            stats["pages"] += 1
+            stats["codes"] += diff.size
+            if diff.any():
+                rows, cols = np.nonzero(diff)
+                assert np.all(np.abs(diff[rows, cols]) == 1), "key code differs by more than 1"
+                t = g[rows, cols].astype(np.float64) / gs[cols].astype(np.float64)
+                band = CODE_REL * np.abs(t)
+                assert np.all(np.abs(np.abs(t - np.floor(t)) - 0.5) <= band + 1e-12), (
+                    f"key code flip away from a rounding boundary at b={b} h={h}")
+                stats["flips"] += len(rows)
+    if stats["codes"]:
+        assert stats["flips"] <= max(1.0, FLIP_FRACTION * stats["codes"]), stats
     return stats

@@ -59,6 +59,31 @@ def test_page_bytes_mixed_heads():
     assert kvq.kvq_page_bytes(desc, 0) == layout.page_bytes(128, b[0])
 
 
+@pytest.mark.parametrize("hkv,d,bits", [(8, 128, (4, 4)), (4, 64, (2, 8)), (3, 128, (8, 2))])
+def test_key_per_channel_page_and_ring_bytes(hkv, d, bits):
+    desc = _desc(hkv=hkv, d=d, block=min(d, 64), bits=bits, window=5)
+    desc.key_per_channel = 1
+    assert kvq.kvq_page_bytes(desc, 0) == layout.page_bytes(d, np.array([bits] * hkv), True)
+    # a ring of R + 16 rows per (sequence, head, K|V), for max_batch = 4 sequences
+    assert kvq.kvq_window_bytes(desc) == 4 * hkv * 2 * (5 + 16) * d * 2
+    desc.window = 0
+    assert kvq.kvq_window_bytes(desc) == 4 * hkv * 2 * 16 * d * 2
+
+
+def test_key_per_channel_host_checks():
+    fake = 1 << 20
+    pools = (ctypes.c_void_p * 1)(fake)
+    ap = lambda d: kvq.kvq_append(d, 0, fake, fake, fake, 4, fake, 2, 3, 0)
+    desc = _desc()
+    desc.layer_pools = pools
+    desc.key_per_channel = 1
+    assert _checked(ap, desc) == kvq.KVQ_EINVAL         # the ring is needed even with R = 0
+    desc.key_per_channel = 2
+    assert _checked(ap, desc) == kvq.KVQ_EINVAL
+    desc.key_per_channel, desc.logquant_w = 1, 16
+    assert _checked(ap, desc) == kvq.KVQ_EUNSUPPORTED   # not built with LogQuant
+
+
 @pytest.mark.parametrize("seed", range(20))
 def test_alloc_bits_matches_oracle(seed):
     rng = np.random.default_rng(seed)
