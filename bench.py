@@ -901,8 +901,8 @@ def key_channel_bench(kvq, torch, dev, n_layers, steps, warmup) -> dict:
     return {"workload": f"key-per-channel: batch {bsz} x {ctx} tokens, {hq} q / {hkv} KV heads, "
                         f"head_dim {d}, K4 per channel / V4 per token, Hadamard {w.had_block}, "
                         f"{n_layers} layer caches",
-            "step": "per layer: kvq_decode_attn (cluster merge; the window CTA covers the "
-                    "open page)",
+            "step": "per layer: kvq_decode_attn (cluster merge; the last split attends to "
+                    "the open page's bf16 rows)",
             "bytes_per_token_head": seg // 16,
             "ms_per_step": round(ms, 4), "GB_per_step": round(sb / 1e9, 4),
             "roofline": _roofline(sb, ms, n_layers, iso, per)}

@@ -194,8 +194,10 @@ kvq_status plan_decode(const kvq_cache* c, const kvq::LayerGeom& g, int B, int m
   }
   const long long units = static_cast<long long>(B) * c->num_kv_heads;
   // with a window (a LogQuant reserve, a key-per-channel ring), each unit's
-  // window CTA takes one of the wave's slots
-  const int extra = uses_ring(c) ? 1 : 0;
+  // window CTA takes one of the wave's slots; the key-per-channel ring of a
+  // cache without a window holds at most the 15 rows of the open page, which
+  // the last split attends to itself
+  const int extra = uses_ring(c) && !(c->key_per_channel && c->window == 0) ? 1 : 0;
   long long s = static_cast<long long>(sms) * bps / units - extra;
   const long long cap = (max_pages + 7) / 8;
   if (s > cap) s = cap;

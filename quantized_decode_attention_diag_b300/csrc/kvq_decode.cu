@@ -613,7 +613,8 @@ __device__ __forceinline__ void patch_stage(uint32_t st, const uint8_t* pbuf, in
 // reserve split) are left out here, on the rounds whose pages can hold one.
 template <int D, int BK, int BV, int MODE>
 __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h, int split,
-                            int lq, float (&qv)[D / 32], int chunk0, uint32_t (&tok)[D / 32]) {
+                            int lq, int len, float (&qv)[D / 32], int chunk0,
+                            uint32_t (&tok)[D / 32]) {
   constexpr bool LQ = MODE == kModeLogQuant;
   constexpr bool KPC = MODE == kModeKeyChannel;
   constexpr int KB = D * BK / 8;                 // K code bytes per token
@@ -788,7 +789,13 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     mx = max(mx, __shfl_xor_sync(kFullMask, mx, 1));
     mx = max(mx, __shfl_xor_sync(kFullMask, mx, 2));
     const int ex = max(static_cast<int>(mx >> 10), 1) - 15;    // subnormal: -14
-    const float down = __int_as_float((127 - ex) << 23), up = __int_as_float((127 + ex) << 23);
+    const float up = __int_as_float((127 + ex) << 23);
+    // 2^-ex as fp16 (2^-16 .. 2^14; below 2^-14 a subnormal): s 2^-ex is exact
+    // unless it falls below 2^-14, i.e. for scales under 2^-15 of the page's
+    // largest, whose terms are then rounded at 2^-24 -- far below the
+    // precision of the largest terms' hi / lo parts
+    const unsigned dh = -ex >= -14 ? static_cast<unsigned>(15 - ex) << 10 : 1u << (24 - ex);
+    const uint32_t down2 = dh | (dh << 16);
     float qf[QD];
     const uint32_t qa = smem_u32(sm.qtab + (g >> 1) * D + c * QD);
 #pragma unroll
@@ -799,14 +806,18 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     auto bfrag = [&](int i) -> uint32_t {
       int d0, d1;
       kpair_dims<D, BK>(0, i, d0, d1);           // dims within the group
-      const float s0 = __half2float(__ushort_as_half(static_cast<unsigned short>(
-                           sw[d0 >> 1] >> (16 * (d0 & 1)))));
-      const float s1 = __half2float(__ushort_as_half(static_cast<unsigned short>(
-                           sw[d1 >> 1] >> (16 * (d1 & 1)))));
-      const float x0 = qf[d0] * (s0 * down), x1 = qf[d1] * (s1 * down);
+      // (s_d0, s_d1) in one fp16 pair, times 2^-ex, widened
+      const uint32_t sp = __byte_perm(sw[d0 >> 1], sw[d1 >> 1],
+                                      ((d0 & 1) ? 0x0032u : 0x0010u) | ((d1 & 1) ? 0x7600u : 0x5400u));
+      __half2 sd = __hmul2(*reinterpret_cast<const __half2*>(&sp),
+                           *reinterpret_cast<const __half2*>(&down2));
+      const float2 sf = __half22float2(sd);
+      float x0, x1, l0, l1;
+      mul2(qf[d0], qf[d1], sf.x, sf.y, x0, x1);
       const __half2 hi = __floats2half2_rn(x0, x1);
       const float2 hf = __half22float2(hi);
-      const __half2 lo = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+      sub2(x0, x1, hf.x, hf.y, l0, l1);
+      const __half2 lo = __floats2half2_rn(l0, l1);
       const __half2 r = (g & 1) ? lo : hi;
       return *reinterpret_cast<const uint32_t*>(&r);
     };
@@ -1014,6 +1025,55 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
       if (++s == NST) {
         s = 0;
         q ^= 1u;
+      }
+    }
+  }
+
+  // ---- key-per-channel mode without a window: the open page's bf16 rows
+  //      (positions lq .. len - 1, at most 15, ring slots p % 16) join the
+  //      last split's online softmax, so that no window CTA holds a slot of
+  //      the wave.  Each row is rotated like the query (H k, H v; lane l holds
+  //      dims [E l, E l + E)): score = sum_d qtab[c][d] (H k)_d, the same
+  //      scaled units as the pages' scores; lane (g, c) adds p (H v) over its
+  //      accumulator dims [g D / 8, (g + 1) D / 8), held by lanes 4 g .. 4 g + 3.
+  if constexpr (KPC) {
+    if (!timed_out && p.NS == p.S && split == p.S - 1) {
+      constexpr int E = D / 32;
+      const uint16_t* kplane = p.window + (static_cast<size_t>(b) * p.Hkv + h) * 2 * p.R * D;
+      const uint16_t* vplane = kplane + static_cast<size_t>(p.R) * D;
+      for (int t = lq + warp; t < len; t += kDecodeWarps) {
+        const size_t row = static_cast<size_t>(t % p.R) * D + E * lane;
+        float kx[E], vx[E];
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+          const uint32_t kw = *reinterpret_cast<const uint32_t*>(kplane + row + e);
+          const uint32_t vw = *reinterpret_cast<const uint32_t*>(vplane + row + e);
+          kx[e] = bf16lo(kw); kx[e + 1] = bf16hi(kw);
+          vx[e] = bf16lo(vw); vx[e + 1] = bf16hi(vw);
+        }
+        warp_fwht<E>(kx, p.had_block);
+        float a[kMaxGroup];
+#pragma unroll
+        for (int i = 0; i < kMaxGroup; ++i) {
+          a[i] = 0.f;
+#pragma unroll
+          for (int e = 0; e < E; ++e) a[i] = __fmaf_rn(sm.qtab[i * D + E * lane + e], kx[e], a[i]);
+          a[i] = warp_sum(a[i]);
+        }
+        const float sc = c == 0 ? a[0] : c == 1 ? a[1] : c == 2 ? a[2] : a[3];
+        if (__any_sync(kFullMask, sc > thr)) rescale(sc);
+        const float pr = ex2(__fmaf_rn(sc, iscl, mneg));
+        if (g == 0) l += pr;
+        warp_fwht<E>(vx, p.had_block);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const float val = __shfl_sync(kFullMask, vx[e], (lane & ~3) + k4);
+            const int m = E * k4 + e;               // dim g D / 8 + m
+            oacc[m >> 1][(m & 1) * 2] = __fmaf_rn(pr, val, oacc[m >> 1][(m & 1) * 2]);
+          }
+        }
       }
     }
   }
@@ -1632,15 +1692,15 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
   } else {
     const int bk = p.geom.bits[h][0], bv = p.geom.bits[h][1];
     switch (bk * 16 + bv) {
-      case 0x22: quant_split<D, 2, 2, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x24: quant_split<D, 2, 4, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x28: quant_split<D, 2, 8, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x42: quant_split<D, 4, 2, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x44: quant_split<D, 4, 4, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x48: quant_split<D, 4, 8, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x82: quant_split<D, 8, 2, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x84: quant_split<D, 8, 4, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
-      case 0x88: quant_split<D, 8, 8, MODE>(p, sm, b, h, split, lq, qv, chunk0, tok); break;
+      case 0x22: quant_split<D, 2, 2, MODE>(p, sm, b, h, split, lq, len, qv, chunk0, tok); break;
+      case 0x24: quant_split<D, 2, 4, MODE>(p, sm, b, h, split, lq, len, qv, chunk0, tok); break;
+      case 0x28: quant_split<D, 2, 8, MODE>(p, sm, b, h, split, lq, len, qv, chunk0, tok); break;
+      case 0x42: quant_split<D, 4, 2, MODE>(p, sm, b, h, split, lq, len, qv, chunk0, tok); break;
+      case 0x44: quant_split<D, 4, 4, MODE>(p, sm, b, h, split, lq, len, qv, chunk0, tok); break;
+      case 0x48: quant_split<D, 4, 8, MODE>(p, sm, b, h, split, lq, len, qv, chunk0, tok); break;
+      case 0x82: quant_split<D, 8, 2, MODE>(p, sm, b, h, split, lq, len, qv, chunk0, tok); break;
+      case 0x84: quant_split<D, 8, 4, MODE>(p, sm, b, h, split, lq, len, qv, chunk0, tok); break;
+      case 0x88: quant_split<D, 8, 8, MODE>(p, sm, b, h, split, lq, len, qv, chunk0, tok); break;
       default: break;
     }
     __syncthreads();   // the warps' partials are in the merge region

@@ -62,6 +62,27 @@ __device__ __forceinline__ void subfma2(float x0, float x1, float z, float inv, 
       : "f"(x0), "f"(x1), "f"(z), "f"(inv), "f"(c));
 }
 
+// (r0, r1) = (a0 b0, a1 b1) and (a0 - b0, a1 - b1): packed fp32 pairs,
+// round-to-nearest per element (sm_100+).
+__device__ __forceinline__ void mul2(float a0, float a1, float b0, float b1, float& r0, float& r1) {
+  asm("{\n\t.reg .b64 ra, rb, rr;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rr, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rr;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void sub2(float a0, float a1, float b0, float b1, float& r0, float& r1) {
+  asm("{\n\t.reg .b64 ra, rb, rr;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rr, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rr;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Prefetch of `bytes` (a multiple of 16; 16-byte aligned address) into L2 by
 // the bulk-copy engine; a hint, nothing waits for it.
 __device__ __forceinline__ void l2_prefetch_bulk(const void* src, uint32_t bytes) {

@@ -100,6 +100,30 @@ def test_decode_groups_and_merges(g, q_fp32, ctx):
     pair.decode_check(q, pt, lens, q_fp32)
 
 
+@pytest.mark.parametrize("d,g", [(128, 4), (64, 2)])
+def test_open_page_in_the_last_split(d, g):
+    # without a window the open page's bf16 rows (at most 15) are attended by
+    # the last quantized split itself: lengths around page boundaries, and
+    # sequences with no full page at all
+    lens = np.array([1, 7, 15, 16, 17, 40, 47, 300], np.int32)
+    bsz, hkv = len(lens), 2
+    mp = 20
+    pt = page_table(340 + d, bsz, mp)
+    pair = KpcPair(hkv, d, d, (4, 2), bsz * mp, 0, max_batch=bsz)
+    k, v = _kv(341, bsz, int(lens.max()), hkv, d)
+    for b in range(bsz):
+        pair.gpu.append(0, dev_bf16(k[b:b + 1, :lens[b]]), dev_bf16(v[b:b + 1, :lens[b]]),
+                        dev_i32(pt[b:b + 1]), dev_i32(np.zeros(1, np.int32)), window_row=b)
+        ocache.append(pair.ora, 0, k[b:b + 1, :lens[b]], v[b:b + 1, :lens[b]], pt[b:b + 1],
+                      np.zeros(1, np.int32), window_row=b)
+    torch.cuda.synchronize()
+    assert pair.gpu.get_status() == 0
+    assert np.array_equal(pair.gpu.window_host(0), pair.ora.windows[0])
+    for q_fp32 in (False, True):
+        q = queries(342 + d, int(q_fp32), bsz, g * hkv, d, q_fp32)
+        pair.decode_check(q, pt, lens, q_fp32)
+
+
 def test_ragged_prefills_one_sequence_at_a_time():
     bsz, hkv, d, window = 4, 2, 128, 20
     lens = np.array([0, 9, 16, 333], np.int32)
