@@ -37,8 +37,8 @@ log-spaced bf16 tokens, W = 128) and "quant_error" (error of the cache's
 attention against float64 attention over the original bf16 K/V, with and
 without the rotation, computed with torch on the device), "key_per_channel"
 (the Llama-3-8B-shaped layer with keys quantized per channel, decode attention
-alone).  --only {mixed,long,logquant,key_channel} runs one of them alone over
---layers layer caches.
+alone).  --only {append,mixed,long,logquant,key_channel} runs one of them (or the
+append sweep) alone over --layers layer caches.
 
 --impl reference times the CPU oracle itself as the reference arm (this
 library has no third-party reference implementation to install).
@@ -984,6 +984,8 @@ def run_section(args) -> None:
                                args.warmup, n_layers=N_LAYERS)
     elif args.only == "long":
         out = long_context_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
+    elif args.only == "append":
+        out = append_sweep(kvq, torch, dev)
     elif args.only == "logquant":
         out = logquant_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
     else:
@@ -1002,7 +1004,7 @@ def main() -> None:
     ap.add_argument("--skip-configs", action="store_true",
                     help="leave out the mixed-bits, long-context and quantization-error sections")
     ap.add_argument("--only", default="all",
-                    choices=["all", "mixed", "long", "logquant", "key_channel"],
+                    choices=["all", "append", "mixed", "long", "logquant", "key_channel"],
                     help="run one section alone and print it (profiling a small case)")
     ap.add_argument("--layers", type=int, default=32,
                     help="distinct layer caches per step (profiling uses a small case)")

@@ -74,9 +74,10 @@ __device__ __forceinline__ int row_pid(const AppendParams& p, const RowRef& rr, 
 
 // Row chunk of a warp: 16 vectors (rows) of one (KV head, K|V), 16 consecutive
 // (sequence, token) pairs.  The warp's lane pair (row = lane / 2, u = lane % 2)
-// holds half u of row `row`.  Rows are prefetched into a per-warp shared-memory
-// buffer with cp.async, one chunk ahead of the one being quantized; 16-byte
-// chunk ci of row r sits at position ci ^ ((2 r + ci / (D / 16)) & 7), so that
+// quantizes half u of row `row`.  Rows are prefetched into a per-warp
+// shared-memory buffer with cp.async, one chunk ahead of the one being
+// quantized; 16-byte chunk ci of row r sits at position
+// ci ^ ((2 r + ci / (D / 16)) & 7), so that
 // the eight lanes of a 16-byte shared-memory phase hit distinct banks.
 template <int D>
 __device__ __forceinline__ int swz(int row, int ci) {
@@ -88,18 +89,28 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
                : "memory");
 }
 
+// The chunk's 16 rows are rows r0 .. r0 + 15 of the (sequence, token) order,
+// so row k's input is at ((r0 + k) Hkv + h) D.  Each copy instruction moves
+// whole rows: D / 8 lanes per 16-byte chunk of a row, 32 / (D / 8) rows at a
+// time, every 32-byte sector read once.
 template <int D>
-__device__ __forceinline__ void prefetch_chunk(const AppendParams& p, const RowRef& rr, uint4* buf) {
-  const int lane = threadIdx.x & 31, row = lane >> 1, u = lane & 1;
-  if (rr.b >= 0) {
-    const int h = rr.grp >> 1, kv = rr.grp & 1;
-    const uint4* src = reinterpret_cast<const uint4*>(
-        (kv ? p.V : p.K) + ((static_cast<size_t>(rr.b) * p.T + rr.t) * p.Hkv + h) * D);
+__device__ __forceinline__ void prefetch_chunk(const AppendParams& p, int c, uint4* buf) {
+  constexpr int LPR = D / 8;                   // lanes per row
+  constexpr int RPI = 32 / LPR;                // rows per instruction
+  const int lane = threadIdx.x & 31;
+  const int grp = c / p.warps_per_group;       // chunk c: group grp, rows blk * 16 ..
+  const int blk = c - grp * p.warps_per_group;
+  const int h = grp >> 1, kv = grp & 1;
+  const long long rows = static_cast<long long>(p.B) * p.T;
+  const uint16_t* base = kv ? p.V : p.K;
+  const int ci = lane % LPR;
 #pragma unroll
-    for (int i = 0; i < D / 16; ++i) {
-      const int ci = u * (D / 16) + i;
-      cp_async16(buf + row * (D / 8) + swz<D>(row, ci), src + ci);
-    }
+  for (int i = 0; i < 16 / RPI; ++i) {
+    const int k = RPI * i + lane / LPR;
+    const long long r = static_cast<long long>(blk) * 16 + k;
+    if (r < rows)
+      cp_async16(buf + k * (D / 8) + swz<D>(k, ci),
+                 reinterpret_cast<const uint4*>(base + (r * p.Hkv + h) * D) + ci);
   }
 }
 
@@ -234,13 +245,16 @@ __device__ __forceinline__ void append_chunk(const AppendParams& p, const RowRef
 }
 
 template <int D, int NB>
-__global__ void __launch_bounds__(kAppendWarps * 32, 2)
+__global__ void __launch_bounds__(kAppendWarps * 32, kAppendCtas)
     append_kernel(const __grid_constant__ AppendParams p) {
-  extern __shared__ uint4 abuf[];           // [warps][2][16 rows][D / 8] 16-byte chunks
+  // [warps][kAppendBufs][16 rows][D / 8] 16-byte chunks: the chunk being
+  // quantized and the next kAppendBufs - 1 in flight
+  extern __shared__ uint4 abuf[];
   const int warp = threadIdx.x >> 5;
   const int total = 2 * p.Hkv * p.warps_per_group;
   const int stride = gridDim.x * kAppendWarps;
-  uint4* mine = abuf + warp * 2 * 16 * (D / 8);
+  uint4* mine = abuf + warp * kAppendBufs * 16 * (D / 8);
+  auto slot = [&](int i) { return mine + (i % kAppendBufs) * 16 * (D / 8); };
   int c = blockIdx.x * kAppendWarps + warp;
   // metadata pipeline: lengths two chunks ahead, page ids one chunk ahead
   RowRef rc = row_ref(p, c < total ? c : 0);
@@ -248,21 +262,24 @@ __global__ void __launch_bounds__(kAppendWarps * 32, 2)
   int l0_c = c < total ? row_len0(p, rc) : INT_MIN;
   int l0_n = c + stride < total ? row_len0(p, rn) : INT_MIN;
   int pid_c = c < total ? row_pid(p, rc, l0_c) : -1;
-  if (c < total) prefetch_chunk<D>(p, rc, mine);
-  asm volatile("cp.async.commit_group;" ::: "memory");
+  // rows of the first kAppendBufs - 1 chunks
+  for (int i = 0; i < kAppendBufs - 1; ++i) {
+    const int ci = c + i * stride;
+    if (ci < total) prefetch_chunk<D>(p, ci, slot(i));
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
   for (int it = 0; c < total; c += stride, ++it) {
     const int cn = c + stride, cnn = cn + stride;
     const RowRef rnn = row_ref(p, cnn < total ? cnn : 0);
     int pid_n = -1, l0_nn = INT_MIN;
-    if (cn < total) {
-      prefetch_chunk<D>(p, rn, mine + ((it + 1) & 1) * 16 * (D / 8));
-      pid_n = row_pid(p, rn, l0_n);
-    }
+    if (cn < total) pid_n = row_pid(p, rn, l0_n);
     if (cnn < total) l0_nn = row_len0(p, rnn);
+    const int cf = c + (kAppendBufs - 1) * stride;   // the chunk whose rows go out now
+    if (cf < total) prefetch_chunk<D>(p, cf, slot(it + kAppendBufs - 1));
     asm volatile("cp.async.commit_group;" ::: "memory");
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    asm volatile("cp.async.wait_group %0;" ::"n"(kAppendBufs - 1) : "memory");
     __syncwarp();
-    const uint4* buf = mine + (it & 1) * 16 * (D / 8);
+    const uint4* buf = slot(it);
     switch (p.geom.bits[rc.grp >> 1][rc.grp & 1]) {  // warp-uniform
       case 2: append_chunk<D, NB, 2>(p, rc, buf, l0_c, pid_c); break;
       case 4: append_chunk<D, NB, 4>(p, rc, buf, l0_c, pid_c); break;
@@ -486,7 +503,7 @@ int sm_count_cached() {
 
 template <int D, int NB>
 cudaError_t launch(const AppendParams& p, cudaStream_t s) {
-  constexpr size_t smem = static_cast<size_t>(kAppendWarps) * 2 * 16 * D * 2;
+  constexpr size_t smem = static_cast<size_t>(kAppendWarps) * kAppendBufs * 16 * D * 2;
   static int attr_set[64] = {0};   // per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -498,8 +515,8 @@ cudaError_t launch(const AppendParams& p, cudaStream_t s) {
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
   const long long chunks = 2ll * p.Hkv * p.warps_per_group;
-  // one resident wave of warps (two CTAs per SM), each looping over its chunks
-  const long long wave = 2ll * kAppendWarps * sm_count_cached();
+  // one resident wave of warps (kAppendCtas CTAs per SM), each looping over its chunks
+  const long long wave = static_cast<long long>(kAppendCtas) * kAppendWarps * sm_count_cached();
   const long long warps = chunks < wave ? chunks : wave;
   const unsigned blocks = static_cast<unsigned>((warps + kAppendWarps - 1) / kAppendWarps);
   append_kernel<D, NB><<<blocks, kAppendWarps * 32, smem, s>>>(p);

@@ -83,6 +83,18 @@ __device__ __forceinline__ void sub2(float a0, float a1, float b0, float b1, flo
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// Three-input minimum and maximum (sm_100+).
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Prefetch of `bytes` (a multiple of 16; 16-byte aligned address) into L2 by
 // the bulk-copy engine; a hint, nothing waits for it.
 __device__ __forceinline__ void l2_prefetch_bulk(const void* src, uint32_t bytes) {

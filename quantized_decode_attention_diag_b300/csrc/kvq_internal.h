@@ -95,6 +95,11 @@ static_assert(kDecodeWarps >= 4, "the query prologue uses one warp per query hea
 static_assert(kDecodeRoundPages == 1 || kDecodeRoundPages == 2, "1 or 2 pages per round");
 static_assert(kDecodeStages % kDecodeRoundPages == 0, "stages are consumed a round at a time");
 constexpr int kAppendWarps = 8;
+// append: row buffers per warp (the chunk being quantized and the next one in
+// flight; a third buffer measured slower) and resident CTAs per SM (the
+// register allocation is sized for it)
+constexpr int kAppendBufs = 2;
+constexpr int kAppendCtas = 2;
 
 // Launchers (defined in the .cu files).  Return cudaSuccess or the launch error.
 cudaError_t launch_append(const AppendParams& p, int head_dim, int had_block, cudaStream_t s);

@@ -107,30 +107,42 @@ __device__ __forceinline__ void rotate_quantize_half(float (&v)[D / 2], int u,
 
   rotate_half<D, NB>(v);
 
-  // ---- per-vector min / max over both lanes (eight independent chains: min
-  //      and max are exact, so the order does not matter)
+  // ---- per-vector min / max over both lanes (eight independent chains of
+  //      three-input min / max: min and max are exact, so the order does not
+  //      matter)
   constexpr int RK = E >= 8 ? 8 : E;
   float mnk[RK], mxk[RK];
 #pragma unroll
   for (int j = 0; j < RK; ++j) mnk[j] = mxk[j] = v[j];
+  int e0 = RK;
 #pragma unroll
-  for (int e = RK; e < E; e += RK) {
+  for (; e0 + 2 * RK <= E; e0 += 2 * RK) {
 #pragma unroll
     for (int j = 0; j < RK; ++j) {
-      mnk[j] = fminf(mnk[j], v[e + j]);
-      mxk[j] = fmaxf(mxk[j], v[e + j]);
+      mnk[j] = fmin3(mnk[j], v[e0 + j], v[e0 + RK + j]);
+      mxk[j] = fmax3(mxk[j], v[e0 + j], v[e0 + RK + j]);
     }
   }
 #pragma unroll
-  for (int w = RK / 2; w > 0; w >>= 1) {
+  for (; e0 < E; e0 += RK) {
 #pragma unroll
-    for (int j = 0; j < w; ++j) {
-      mnk[j] = fminf(mnk[j], mnk[j + w]);
-      mxk[j] = fmaxf(mxk[j], mxk[j + w]);
+    for (int j = 0; j < RK; ++j) {
+      mnk[j] = fminf(mnk[j], v[e0 + j]);
+      mxk[j] = fmaxf(mxk[j], v[e0 + j]);
     }
   }
-  float mn = fminf(mnk[0], __shfl_xor_sync(kFullMask, mnk[0], 1));
-  float mx = fmaxf(mxk[0], __shfl_xor_sync(kFullMask, mxk[0], 1));
+  float mn = mnk[0], mx = mxk[0];
+#pragma unroll
+  for (int j = 1; j + 1 < RK; j += 2) {
+    mn = fmin3(mn, mnk[j], mnk[j + 1]);
+    mx = fmax3(mx, mxk[j], mxk[j + 1]);
+  }
+  if constexpr (RK % 2 == 0) {
+    mn = fminf(mn, mnk[RK - 1]);
+    mx = fmaxf(mx, mxk[RK - 1]);
+  }
+  mn = fminf(mn, __shfl_xor_sync(kFullMask, mn, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 1));
 
   // ---- fp16 zero (round down) and scale (round up)
   zh = __float2half_rd(mn);
