@@ -888,7 +888,7 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   // sequence has any) and, in LogQuant mode, the members of B (lq = len then)
   const int lq_w = LQ ? p.lq_w : 0, lq_a = LQ ? p.lq_a : 0;
   auto excluded = [&](int t) -> bool {
-    return t >= lq || (LQ && lq_member(t, lq, lq_w, lq_a));
+    return t >= lq || (LQ && lq_member32(t, lq, lq_w, lq_a));
   };
   // one round: pages A (stage at sta) and, if has_b, B (the next stage); mask
   // applies excluded() to its tokens
@@ -976,7 +976,10 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
       // lq_lo() on
       const int t0 = (first + kDecodeWarps * k) * kPage;
       const int t1 = t0 + (RP == 2 ? kDecodeWarps * kPage : 0) + kPage;
-      round(st0 + sa * stage_bytes, RP == 2, t0 < lq_w || t1 > lq_from, t0);
+      // masked rounds are rare (block 0 and the newest positions): a literal
+      // flag per call gives the common unmasked round its own copy
+      if (t0 < lq_w || t1 > lq_from) round(st0 + sa * stage_bytes, RP == 2, true, t0);
+      else round(st0 + sa * stage_bytes, RP == 2, false, t0);
     } else {
       round(st0 + sa * stage_bytes, RP == 2, false, 0);
     }

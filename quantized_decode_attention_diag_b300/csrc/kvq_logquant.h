@@ -70,6 +70,20 @@ KVQ_HD bool lq_member(long long p, long long n, int w, int a) {
   return ((p & (w - 1)) & ((2ll << j) - 1)) == 0;
 }
 
+// lq_member for 32-bit positions and lengths (n < 2^31 - w), as the decode
+// kernel's masked rounds use it.
+KVQ_HD bool lq_member32(int p, int n, int w, int a) {
+  if (p < 0 || p >= n) return false;
+  if (n < 3 * w) return true;
+  const int k = ((n - 3 * w) >> a) + 1;
+  if (p >= ((k + 1) << a)) return true;
+  const int blk = p >> a;
+  if (blk == 0) return k <= a ? (p & ((1 << k) - 1)) == 0 : p == 0;
+  const int j = k - blk;
+  if (j >= a) return false;
+  return ((p & (w - 1)) & ((2 << j) - 1)) == 0;
+}
+
 // Reserve row of member p after n appends (see the header comment).
 KVQ_HD int lq_row(long long p, long long n, int w, int a) {
   if (n < 3ll * w) return static_cast<int>(p % (3ll * w));

@@ -41,3 +41,39 @@ def test_descriptor_checks():
     assert "needs window 0" in kvq.kvq_last_error()
     d.window, d.logquant_w = 0, 24                 # not a power of two
     assert kvq.kvq_window_bytes(d) == 0
+
+
+def test_decode_membership_rule_equals_the_host_rule(tmp_path):
+    # the decode kernel's masked rounds use the 32-bit form of the closed-form
+    # membership; compiled from the same header, it must agree with the
+    # 64-bit form that kvq_logquant_members (pinned against the oracle above)
+    # uses, for every position of every length up to 12 W and a few long ones
+    import os
+    import shutil
+    import subprocess
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        pytest.skip("no C++ compiler")
+    csrc = os.path.join(os.path.dirname(kvq.LIB_PATH), "csrc")
+    src = tmp_path / "lq32.cpp"
+    src.write_text(
+        '#include <cstdio>\n#include "kvq_logquant.h"\n'
+        "int main() {\n"
+        "  long long bad = 0, checked = 0;\n"
+        "  for (int a = 1; a <= 8; ++a) {\n"
+        "    const int w = 1 << a;\n"
+        "    const int longs[] = {20 * w + 3, 131072, 131071, 1000003};\n"
+        "    for (int n = 0; n < 12 * w + 4; ++n)\n"
+        "      for (int p = -1; p <= n; ++p, ++checked)\n"
+        "        bad += kvq::lq_member(p, n, w, a) != kvq::lq_member32(p, n, w, a);\n"
+        "    for (int n : longs)\n"
+        "      for (int p = 0; p < n; p += (p < 4 * w || p > n - 16 * w) ? 1 : 7, ++checked)\n"
+        "        bad += kvq::lq_member(p, n, w, a) != kvq::lq_member32(p, n, w, a);\n"
+        "  }\n"
+        '  std::printf("%lld %lld\\n", bad, checked);\n'
+        "  return 0;\n}\n")
+    exe = tmp_path / "lq32"
+    subprocess.run([cxx, "-O1", "-std=c++17", "-I", csrc, str(src), "-o", str(exe)], check=True)
+    bad, checked = map(int, subprocess.run([str(exe)], check=True, capture_output=True,
+                                           text=True).stdout.split())
+    assert checked > 100000 and bad == 0
