@@ -1466,7 +1466,7 @@ __device__ void reserve_split(const DecodeParams& p, const Smem& sm, int b, int 
   const int ncand = nb0 + max(0, len - max(lo, nb0));
   for (int t = tid; t < ncand; t += kThreads) {
     const int pos = t < nb0 ? t : max(lo, nb0) + (t - nb0);
-    if (lq_member(pos, len, w, a)) list[atomicAdd(count, 1)] = lq_row(pos, len, w, a);
+    if (lq_member32(pos, len, w, a)) list[atomicAdd(count, 1)] = lq_row32(pos, len, w, a);
   }
   __syncthreads();
   const int nm = *count;
@@ -1671,6 +1671,15 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
   __syncthreads();
 
   if (MODE == kModeLogQuant && is_window) {
+    // the reserve's two planes of (b, h) are contiguous: one bulk prefetch into
+    // L2 each, before the wait (a hint, as for the window), so that the member
+    // rows the attention gathers are L2 hits when it starts
+    if (tid == 0 && len > 0) {
+      const uint16_t* kplane = p.window + (static_cast<size_t>(b) * p.Hkv + h) * 2 * p.lq_rows * D;
+      const uint32_t bytes = static_cast<uint32_t>(p.lq_rows) * D * 2;
+      l2_prefetch_bulk(kplane, bytes);
+      l2_prefetch_bulk(kplane + static_cast<size_t>(p.lq_rows) * D, bytes);
+    }
     grid_wait();
     if (p.overlap) load_query<D>(p, b, h, qv);
     query_window_prologue<D>(p, sm, qv);

@@ -94,6 +94,16 @@ KVQ_HD int lq_row(long long p, long long n, int w, int a) {
   return 3 * w + level * (w / 2) + static_cast<int>((p & (w - 1)) >> 1);
 }
 
+// lq_row for 32-bit positions and lengths (the decode kernel's member list).
+KVQ_HD int lq_row32(int p, int n, int w, int a) {
+  if (n < 3 * w) return p % (3 * w);
+  const int k = ((n - 3 * w) >> a) + 1;
+  if (p >= ((k + 1) << a)) return p % (3 * w);
+  const int blk = p >> a;
+  const int level = blk == 0 ? a : blk % a;
+  return 3 * w + level * (w / 2) + ((p & (w - 1)) >> 1);
+}
+
 // The members of B at length n lie in block 0 and from lq_lo() on.
 KVQ_HD int lq_lo(long long n, int w, int a) {
   if (n < 3ll * w) return 0;

@@ -44,10 +44,11 @@ def test_descriptor_checks():
 
 
 def test_decode_membership_rule_equals_the_host_rule(tmp_path):
-    # the decode kernel's masked rounds use the 32-bit form of the closed-form
-    # membership; compiled from the same header, it must agree with the
-    # 64-bit form that kvq_logquant_members (pinned against the oracle above)
-    # uses, for every position of every length up to 12 W and a few long ones
+    # the decode kernel's masked rounds and member list use 32-bit forms of the
+    # closed-form membership and reserve row; compiled from the same header,
+    # they must agree with the 64-bit forms that kvq_logquant_members (pinned
+    # against the oracle above) uses, for every position of every length up to
+    # 12 W and a few long ones
     import os
     import shutil
     import subprocess
@@ -65,10 +66,14 @@ def test_decode_membership_rule_equals_the_host_rule(tmp_path):
         "    const int longs[] = {20 * w + 3, 131072, 131071, 1000003};\n"
         "    for (int n = 0; n < 12 * w + 4; ++n)\n"
         "      for (int p = -1; p <= n; ++p, ++checked)\n"
-        "        bad += kvq::lq_member(p, n, w, a) != kvq::lq_member32(p, n, w, a);\n"
+        "        bad += kvq::lq_member(p, n, w, a) != kvq::lq_member32(p, n, w, a) ||\n"
+        "               (p >= 0 && p < n && kvq::lq_member(p, n, w, a) &&\n"
+        "                kvq::lq_row(p, n, w, a) != kvq::lq_row32(p, n, w, a));\n"
         "    for (int n : longs)\n"
         "      for (int p = 0; p < n; p += (p < 4 * w || p > n - 16 * w) ? 1 : 7, ++checked)\n"
-        "        bad += kvq::lq_member(p, n, w, a) != kvq::lq_member32(p, n, w, a);\n"
+        "        bad += kvq::lq_member(p, n, w, a) != kvq::lq_member32(p, n, w, a) ||\n"
+        "               (kvq::lq_member(p, n, w, a) &&\n"
+        "                kvq::lq_row(p, n, w, a) != kvq::lq_row32(p, n, w, a));\n"
         "  }\n"
         '  std::printf("%lld %lld\\n", bad, checked);\n'
         "  return 0;\n}\n")
