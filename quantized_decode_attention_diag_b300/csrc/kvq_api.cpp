@@ -197,8 +197,12 @@ kvq_status plan_decode(const kvq_cache* c, const kvq::LayerGeom& g, int B, int m
   // window CTA takes one of the wave's slots; the key-per-channel ring of a
   // cache without a window holds at most the 15 rows of the open page, which
   // the last split attends to itself
-  const int extra = uses_ring(c) && !(c->key_per_channel && c->window == 0) ? 1 : 0;
-  long long s = static_cast<long long>(sms) * bps / units - extra;
+  int extra = uses_ring(c) && !(c->key_per_channel && c->window == 0) ? 1 : 0;
+  const long long slots = static_cast<long long>(sms) * bps / units;   // per unit
+  // the LogQuant reserve (up to 3W gathered rows) splits over two or four CTAs
+  // when a unit has many slots (few sequences): one CTA alone would end last
+  if (c->logquant_w > 0 && slots >= 16) extra = slots >= 32 ? 4 : 2;
+  long long s = slots - extra;
   const long long cap = (max_pages + 7) / 8;
   if (s > cap) s = cap;
   if (s > kvq::decode_max_splits()) s = kvq::decode_max_splits();

@@ -1421,7 +1421,7 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
 // attended over.
 template <int D>
 __device__ void reserve_split(const DecodeParams& p, const Smem& sm, int b, int h, int len,
-                              float* part) {
+                              int r, int nr, float* part) {
   const int tid = threadIdx.x;
   const int w = p.lq_w, a = p.lq_a, half = w / 2;
   const int ldsc = 3 * w;                       // |B| <= 3W
@@ -1432,8 +1432,13 @@ __device__ void reserve_split(const DecodeParams& p, const Smem& sm, int b, int 
                      ((static_cast<size_t>(b) * p.Hkv + h) * 2) * p.lq_rows * D;
   uint16_t* vplane = kplane + static_cast<size_t>(p.lq_rows) * D;
   constexpr int C = D / 8;                      // uint4 chunks per row
-  if (p.step && len > 0) {
-    const int k0 = lq_halvings(len - 1, w), k1 = lq_halvings(len, w);
+  // a decode step's halving (block 1 + k0, and block 0 at the first one) and
+  // new token: reserve CTA 0 writes them for the later steps, and every reserve
+  // CTA reads those rows where they were before this step (the ring, k_new /
+  // v_new), so that none depends on another's writes
+  const int k0 = p.step && len > 0 ? lq_halvings(len - 1, w) : 0;
+  const int k1 = p.step && len > 0 ? lq_halvings(len, w) : 0;
+  if (p.step && len > 0 && r == 0) {
     if (k1 > k0) {                              // one halving: block 1 + k0 (and block 0)
       for (int pass = 0; pass < (k0 == 0 ? 2 : 1); ++pass) {
         const int bb = pass ? 0 : 1 + k0;
@@ -1460,19 +1465,32 @@ __device__ void reserve_split(const DecodeParams& p, const Smem& sm, int b, int 
   }
   if (tid == 0) *count = 0;
   __syncthreads();
-  // member list: block 0 and the positions from lq_lo on
+  // member list: block 0 and the positions from lq_lo on, candidates t with
+  // t mod nr = r for reserve CTA r; the row each is read from (-1: the new
+  // token, read from k_new / v_new)
   const int lo = lq_lo(len, w, a);
   const int nb0 = min(w, len);
   const int ncand = nb0 + max(0, len - max(lo, nb0));
-  for (int t = tid; t < ncand; t += kThreads) {
+  const int moved = k1 > k0 ? 1 + k0 : -1;      // block moved by this step's halving
+  for (int t = r + nr * tid; t < ncand; t += nr * kThreads) {
     const int pos = t < nb0 ? t : max(lo, nb0) + (t - nb0);
-    if (lq_member32(pos, len, w, a)) list[atomicAdd(count, 1)] = lq_row32(pos, len, w, a);
+    if (!lq_member32(pos, len, w, a)) continue;
+    int row = lq_row32(pos, len, w, a);
+    if (p.step) {
+      if (pos == len - 1) row = -1;
+      else if (moved >= 0 && ((pos >> a) == moved || (k0 == 0 && (pos >> a) == 0)))
+        row = pos % (3 * w);                    // still in the ring before this step
+    }
+    list[atomicAdd(count, 1)] = row;
   }
   __syncthreads();
   const int nm = *count;
+  const uint16_t* knew = p.step ? p.k_new + (static_cast<size_t>(b) * p.Hkv + h) * D : nullptr;
+  const uint16_t* vnew = p.step ? p.v_new + (static_cast<size_t>(b) * p.Hkv + h) * D : nullptr;
   attend_rows<D>(
-      p, sm, nm, sc, ldsc, [&](int t) { return kplane + static_cast<size_t>(list[t]) * D; },
-      [&](int t) { return vplane + static_cast<size_t>(list[t]) * D; }, part);
+      p, sm, nm, sc, ldsc,
+      [&](int t) { return list[t] < 0 ? knew : kplane + static_cast<size_t>(list[t]) * D; },
+      [&](int t) { return list[t] < 0 ? vnew : vplane + static_cast<size_t>(list[t]) * D; }, part);
 }
 
 // E consecutive floats (E = 4 or 2; 16- or 8-byte aligned) bypassing L1.
@@ -1504,7 +1522,7 @@ __device__ void combine_global(const DecodeParams& p, int b, int h, const float*
   float mm = -CUDART_INF_F;
   for (int s = lane; s < NS; s += 32) mm = fmaxf(mm, __ldcg(part_m<D>(parts + s * PS) + i));
   mm = warp_max(mm);
-  float ll = 0.f, acc[E], ww = 0.f;
+  float ll = 0.f, acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   for (int s0 = 0; s0 < NS; s0 += 32) {
@@ -1516,7 +1534,6 @@ __device__ void combine_global(const DecodeParams& p, int b, int h, const float*
         ll = __fmaf_rn(w, __ldcg(part_l<D>(parts + (s0 + lane) * PS) + i), ll);
       }
     }
-    if (NS > nq && nq >= s0 && nq < s0 + 32) ww = __shfl_sync(kFullMask, w, nq - s0);
     const int cnt = min(32, nq - s0);   // quantized splits of this group
     for (int k0 = 0; k0 < cnt; k0 += UN) {
       float rows[UN][E];
@@ -1543,11 +1560,15 @@ __device__ void combine_global(const DecodeParams& p, int b, int h, const float*
   const float inv_nb = 1.f / static_cast<float>(p.had_block);
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] *= inv_nb;
-  if (NS > nq && ww != 0.f) {
+  // the unrotated partials (window, reserve) after the quantized ones
+  for (int s = nq; s < NS; ++s) {
+    const float ms = __ldcg(part_m<D>(parts + s * PS) + i);
+    if (ms == -CUDART_INF_F) continue;
+    const float ws = exp2f(ms - mm);
     float row[E];
-    ldcg_vec<E>(part_acc<D>(parts + nq * PS, i) + E * lane, row);
+    ldcg_vec<E>(part_acc<D>(parts + s * PS, i) + E * lane, row);
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(ww, row[e], acc[e]);
+    for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(ws, row[e], acc[e]);
   }
   float* o = p.o + (static_cast<size_t>(b) * p.Hq + h * p.G + i) * D + E * lane;
 #pragma unroll
@@ -1601,9 +1622,9 @@ __device__ void combine_cluster(const DecodeParams& p, const Smem& sm, int b, in
   const float inv_nb = 1.f / static_cast<float>(p.had_block);
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] *= inv_nb;
-  if (NS > nq) {
-    const float ws = __shfl_sync(kFullMask, w, nq);
-    const float* row = part_acc<D>(rb + nq * PS, i) + E * lane;
+  for (int s = nq; s < NS; ++s) {           // the unrotated partials
+    const float ws = __shfl_sync(kFullMask, w, s);
+    const float* row = part_acc<D>(rb + s * PS, i) + E * lane;
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(ws, row[e], acc[e]);
   }
@@ -1683,7 +1704,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
     grid_wait();
     if (p.overlap) load_query<D>(p, b, h, qv);
     query_window_prologue<D>(p, sm, qv);
-    reserve_split<D>(p, sm, b, h, len, sm.cpart);
+    reserve_split<D>(p, sm, b, h, len, split - p.S, p.NS - p.S, sm.cpart);
   } else if (is_window) {
     // the window's valid slots are a prefix of the ring (all R of them once
     // the sequence is longer than the window): one bulk prefetch into L2 each

@@ -52,7 +52,7 @@ struct DecodeParams {
   int* status;
   int q_fp32, max_pages, B, Hq, Hkv, G, R, num_pages, had_block;
   int S;                         // quantized-token splits per (sequence, KV head)
-  int NS;                        // S + (R > 0): the window gets its own split
+  int NS;                        // S + the window or LogQuant reserve CTAs (0 to 4)
   int pages_per_split;       // host plan (page-table width / S); the kernel uses the lengths
   int overlap;               // launched with programmatic stream serialization
   int cluster;                   // 1: the NS CTAs of a unit form a cluster and merge
