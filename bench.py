@@ -856,7 +856,7 @@ def logquant_bench(kvq, torch, dev, n_layers, steps, warmup, w=128) -> dict:
                         f"head_dim {d}, K2V2, Hadamard {L.had_block}, base window W = {w} "
                         f"({members} full-precision positions), {n_layers} layer caches",
             "step": "per layer: kvq_decode_step (members masked in the quantized splits, "
-                    "a reserve CTA attends over their bf16 rows)",
+                    "reserve CTAs attend over their bf16 rows)",
             "ms_per_step": round(ms, 4), "GB_per_step": round(sb / 1e9, 4),
             "roofline": _roofline(sb, ms, n_layers, iso, per)}
 
