@@ -237,8 +237,9 @@ size_t kvq_decode_workspace_bytes(const kvq_cache* cache, int B, int Hq, int max
  *                gets o = 0.
  *   workspace    device, ws_bytes >= kvq_decode_workspace_bytes(cache, B, Hq,
  *                max_pages), 16-byte aligned, zero-filled before its first use.
- * In LogQuant mode the quantized splits leave out the members of B and one more
- * CTA per (sequence, KV head) attends over their bf16 rows in the reserve.  In
+ * In LogQuant mode the quantized splits leave out the members of B, and one to
+ * four more CTAs per (sequence, KV head) attend over their bf16 rows in the
+ * reserve (more of them when the batch leaves the wave room).  In
  * the key-per-channel mode the splits read each page's channel scales and one
  * more CTA attends over the ring's positions Q(L) .. L - 1.
  * One kernel launch.  Returns KVQ_OK once enqueued.

@@ -10,7 +10,7 @@
 //
 // Grid (NS, Hkv, B): split s < S covers a contiguous range of quantized pages of
 // sequence b for KV head h and its G <= 4 query heads; split S (when R > 0)
-// covers the bf16 window.  Each CTA merges its warps into one online-softmax
+// covers the bf16 window, splits S .. NS - 1 the LogQuant reserve.  Each CTA merges its warps into one online-softmax
 // partial (m, l, rotated acc[d] per query head).  Merge of the NS partials of a
 // (b, h):
 //   - cluster mode (NS <= 4): the NS CTAs form a thread-block cluster; each
@@ -1413,12 +1413,12 @@ __device__ void window_split(const DecodeParams& p, const Smem& sm, int b, int h
   }
 }
 
-// Reserve split (LogQuant mode) of (b, h) at length len.  A decode step first
-// carries out its halving, if its token fills B to 3W (the block thinned for
-// the first time moves from the ring to its level buffer; the first halving
-// moves block 0 too), and writes its token's bf16 rows into the ring.  Then
-// the rows of every member of B are listed in shared memory (any order) and
-// attended over.
+// Reserve split r of nr (LogQuant mode) of (b, h) at length len.  In a decode
+// step, split 0 carries out the halving, if the token fills B to 3W (the block
+// thinned for the first time moves from the ring to its level buffer; the
+// first halving moves block 0 too), and writes the token's bf16 rows into the
+// ring.  Then each split lists the rows of its share of B's members in shared
+// memory (any order) and attends over them.
 template <int D>
 __device__ void reserve_split(const DecodeParams& p, const Smem& sm, int b, int h, int len,
                               int r, int nr, float* part) {
