@@ -879,49 +879,56 @@ def logquant_bench(kvq, torch, dev, n_layers, steps, warmup, w=128) -> dict:
 
 def key_channel_bench(kvq, torch, dev, n_layers, steps, warmup) -> dict:
     """Key-per-channel mode on the Llama-3-8B-shaped decode layer: batch 16,
-    32 query / 8 KV heads, head_dim 128, context 4096, K and V INT4 with
-    Hadamard 128, keys quantized per channel (one fp16 scale per page, head
-    and channel), values token-wise, no window.  One step = decode attention
-    over n_layers distinct layer caches (the append of a step's token is a
-    separate launch in this mode; the decode is the kernel measured)."""
+    32 query / 8 KV heads, head_dim 128, context 4096, Hadamard 128, keys
+    quantized per channel (one fp16 scale per page, head and channel), values
+    token-wise, no window; K4V4 (as the token-wise headline) and K2V2 (the
+    2-bit setting of KIVI and LogQuant).  One step = decode attention over
+    n_layers distinct layer caches (the append of a step's token is a separate
+    launch in this mode; the decode is the kernel measured)."""
     w = LLAMA3_8B_LAYER
     hkv, hq, d, bsz, ctx = w.hkv, w.hq, w.head_dim, w.batch, w.ctx
     mp = ctx // 16
-    bits = np.full((n_layers, hkv, 2), 4)
-    cache = kvq.Cache(n_layers, hkv, d, w.had_block, bits, bsz * mp, max_batch=bsz, device=dev,
-                      overlap=True, key_per_channel=True)
-    pt = torch.from_numpy(page_table(w.seed, bsz, mp)).to(dev)
-    zero = torch.zeros(bsz, dtype=torch.int32, device=dev)
-    for half in range(2):          # the inputs for 8 sequences at a time, shared by the layers
-        rows = slice(8 * half, 8 * half + 8)
-        k = kv_tokens(w.seed, 0, 8, ctx, hkv, d, w.k_outliers, w.outlier_lo, w.outlier_hi, seq0=8 * half)
-        v = kv_tokens(w.seed, 1, 8, ctx, hkv, d, w.v_outliers, w.outlier_lo, w.outlier_hi, seq0=8 * half)
-        kd = torch.from_numpy(k).to(dev).to(torch.bfloat16)
-        vd = torch.from_numpy(v).to(dev).to(torch.bfloat16)
-        del k, v
-        for l in range(n_layers):
-            cache.append(l, kd, vd, pt[rows].contiguous(), zero[rows].contiguous(), window_row=8 * half)
-        del kd, vd
-    q_all = torch.from_numpy(np.stack([queries(w.seed, l, bsz, hq, d, False)
-                                       for l in range(n_layers)])).to(dev).to(torch.bfloat16)
-    o_all = torch.empty((n_layers, bsz, hq, d), dtype=torch.float32, device=dev)
-    lens = torch.full((bsz,), ctx, dtype=torch.int32, device=dev)
-    ws = cache.workspace(bsz, hq, mp)
-    torch.cuda.synchronize(dev)
-    ms, iso = graph_step_bench(torch, dev, cache, n_layers, None, None, q_all, pt, lens, o_all,
-                               ws, steps, warmup, decode_only=True)
-    seg = cache.page_bytes[0] // hkv                     # one (page, head) segment
-    per = bsz * mp * hkv * seg + bsz * hq * d * (2 + 4) + bsz * mp * 4
-    sb = per * n_layers
-    del cache
+    variants = []
+    for kb, vb in ((4, 4), (2, 2)):
+        bits = np.tile(np.array([kb, vb]), (n_layers, hkv, 1))
+        cache = kvq.Cache(n_layers, hkv, d, w.had_block, bits, bsz * mp, max_batch=bsz,
+                          device=dev, overlap=True, key_per_channel=True)
+        pt = torch.from_numpy(page_table(w.seed, bsz, mp)).to(dev)
+        zero = torch.zeros(bsz, dtype=torch.int32, device=dev)
+        for half in range(2):       # the inputs for 8 sequences at a time, shared by the layers
+            rows = slice(8 * half, 8 * half + 8)
+            k = kv_tokens(w.seed, 0, 8, ctx, hkv, d, w.k_outliers, w.outlier_lo, w.outlier_hi,
+                          seq0=8 * half)
+            v = kv_tokens(w.seed, 1, 8, ctx, hkv, d, w.v_outliers, w.outlier_lo, w.outlier_hi,
+                          seq0=8 * half)
+            kd = torch.from_numpy(k).to(dev).to(torch.bfloat16)
+            vd = torch.from_numpy(v).to(dev).to(torch.bfloat16)
+            del k, v
+            for l in range(n_layers):
+                cache.append(l, kd, vd, pt[rows].contiguous(), zero[rows].contiguous(),
+                             window_row=8 * half)
+            del kd, vd
+        q_all = torch.from_numpy(np.stack([queries(w.seed, l, bsz, hq, d, False)
+                                           for l in range(n_layers)])).to(dev).to(torch.bfloat16)
+        o_all = torch.empty((n_layers, bsz, hq, d), dtype=torch.float32, device=dev)
+        lens = torch.full((bsz,), ctx, dtype=torch.int32, device=dev)
+        ws = cache.workspace(bsz, hq, mp)
+        torch.cuda.synchronize(dev)
+        ms, iso = graph_step_bench(torch, dev, cache, n_layers, None, None, q_all, pt, lens, o_all,
+                                   ws, steps, warmup, decode_only=True)
+        seg = cache.page_bytes[0] // hkv                 # one (page, head) segment
+        per = bsz * mp * hkv * seg + bsz * hq * d * (2 + 4) + bsz * mp * 4
+        sb = per * n_layers
+        variants.append({"bits": f"K{kb} per channel / V{vb}", "bytes_per_token_head": seg // 16,
+                         "ms_per_step": round(ms, 4), "GB_per_step": round(sb / 1e9, 4),
+                         "roofline": _roofline(sb, ms, n_layers, iso, per)})
+        del cache, ws, q_all, o_all
+        torch.cuda.synchronize(dev)
     return {"workload": f"key-per-channel: batch {bsz} x {ctx} tokens, {hq} q / {hkv} KV heads, "
-                        f"head_dim {d}, K4 per channel / V4 per token, Hadamard {w.had_block}, "
-                        f"{n_layers} layer caches",
+                        f"head_dim {d}, Hadamard {w.had_block}, {n_layers} layer caches",
             "step": "per layer: kvq_decode_attn (cluster merge; the last split attends to "
                     "the open page's bf16 rows)",
-            "bytes_per_token_head": seg // 16,
-            "ms_per_step": round(ms, 4), "GB_per_step": round(sb / 1e9, 4),
-            "roofline": _roofline(sb, ms, n_layers, iso, per)}
+            "variants": variants}
 
 
 def _exact_attention_torch(torch, q, k, v, scale):

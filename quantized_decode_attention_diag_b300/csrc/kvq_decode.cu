@@ -719,13 +719,17 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   }
   const int pslot = (lq - 1) % kPage;
 
-  query_quant_prologue<D, KPC>(p, sm, qv);
+  // key-per-channel codes of 2 bits are -1, 0 or 1, so c s is exact in fp16:
+  // the page's scales go into the A operand and the query keeps its constant
+  // B fragments (KPC2); wider codes form B per page from fp32 queries
+  constexpr bool KPC2 = KPC && BK == 2;
+  query_quant_prologue<D, KPC && !KPC2>(p, sm, qv);
 
   // ---- B fragments of the K-side MMA: column n = g is query head g / 2, its
   //      hi part for even g and lo part for odd g (per page in the
   //      key-per-channel mode)
   uint32_t bq[NJ][2];
-  if constexpr (!KPC) {
+  if constexpr (!KPC || KPC2) {
     const uint32_t* qh = reinterpret_cast<const uint32_t*>(sm.qtab) + (g >> 1) * D;
     const int sh = (g & 1) ? 16 : 0;
 #pragma unroll
@@ -775,6 +779,40 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   // is the binade of the page's largest scale (x < 2^15 stays inside fp16);
   // the scaled score is (a0 + a1) 2^E.  Codes are signed, no zero term.
   constexpr int QD = D / 4;                      // dims of a k-slot group
+  // 2-bit key-per-channel: A = c s_d (exact), B the constant query fragments;
+  // the scaled score is a_hi + a_lo (no zero term)
+  auto scores_kpc2 = [&](uint32_t st, float& sc0, float& sc1) {
+    uint32_t w0[KWORDS], w1[KWORDS];
+    lds_u32<KSLICE>(st + koff, w0);
+    lds_u32<KSLICE>(st + koff + 8 * KB, w1);
+    uint32_t sw[QD / 2];                         // scales of dims [c QD, (c + 1) QD)
+#pragma unroll
+    for (int i = 0; i < QD / 16; ++i) lds_u32<32>(st + KSZ + c * (QD * 2) + 32 * i, sw + 8 * i);
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      uint32_t sp[2];
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        int d0, d1;
+        kpair_dims<D, BK>(0, 2 * j + s2, d0, d1);
+        sp[s2] = __byte_perm(sw[d0 >> 1], sw[d1 >> 1],
+                             ((d0 & 1) ? 0x0032u : 0x0010u) | ((d1 & 1) ? 0x7600u : 0x5400u));
+      }
+      auto scaled = [&](uint32_t code2, uint32_t s2v) -> uint32_t {
+        const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&code2),
+                                  *reinterpret_cast<const __half2*>(&s2v));
+        return *reinterpret_cast<const uint32_t*>(&r);
+      };
+      const uint32_t x[4] = {scaled(kpair_signed<BK>(w0, 2 * j), sp[0]),
+                             scaled(kpair_signed<BK>(w1, 2 * j), sp[0]),
+                             scaled(kpair_signed<BK>(w0, 2 * j + 1), sp[1]),
+                             scaled(kpair_signed<BK>(w1, 2 * j + 1), sp[1])};
+      mma_16816(a, x, bq[j][0], bq[j][1]);
+    }
+    sc0 = a[0] + a[1];
+    sc1 = a[2] + a[3];
+  };
   auto scores_kpc = [&](uint32_t st, float& sc0, float& sc1) {
     uint32_t w0[KWORDS], w1[KWORDS];
     lds_u32<KSLICE>(st + koff, w0);
@@ -895,7 +933,10 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   auto round = [&](uint32_t sta, bool has_b, bool mask, int tok_a) {
     const uint32_t stb = sta + stage_bytes;
     float sa0, sa1, sb0 = -CUDART_INF_F, sb1 = -CUDART_INF_F;
-    if constexpr (KPC) {
+    if constexpr (KPC2) {
+      scores_kpc2(sta, sa0, sa1);
+      if (has_b) scores_kpc2(stb, sb0, sb1);
+    } else if constexpr (KPC) {
       scores_kpc(sta, sa0, sa1);
       if (has_b) scores_kpc(stb, sb0, sb1);
     } else {
@@ -1060,7 +1101,15 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
         for (int i = 0; i < kMaxGroup; ++i) {
           a[i] = 0.f;
 #pragma unroll
-          for (int e = 0; e < E; ++e) a[i] = __fmaf_rn(sm.qtab[i * D + E * lane + e], kx[e], a[i]);
+          for (int e = 0; e < E; ++e) {
+            float qe = sm.qtab[i * D + E * lane + e];
+            if constexpr (KPC2) {                // the packed (hi, lo) pair of e q''
+              const uint32_t hl = __float_as_uint(qe);
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hl));
+              qe = f.x + f.y;
+            }
+            a[i] = __fmaf_rn(qe, kx[e], a[i]);
+          }
           a[i] = warp_sum(a[i]);
         }
         const float sc = c == 0 ? a[0] : c == 1 ? a[1] : c == 2 ? a[2] : a[3];

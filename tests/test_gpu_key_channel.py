@@ -100,8 +100,9 @@ def test_decode_groups_and_merges(g, q_fp32, ctx):
     pair.decode_check(q, pt, lens, q_fp32)
 
 
-@pytest.mark.parametrize("d,g", [(128, 4), (64, 2)])
-def test_open_page_in_the_last_split(d, g):
+@pytest.mark.parametrize("d,g,bits", [(128, 4, (4, 2)), (64, 2, (4, 2)), (128, 4, (2, 2)),
+                                      (64, 1, (2, 4))])
+def test_open_page_in_the_last_split(d, g, bits):
     # without a window the open page's bf16 rows (at most 15) are attended by
     # the last quantized split itself: lengths around page boundaries, and
     # sequences with no full page at all
@@ -109,7 +110,7 @@ def test_open_page_in_the_last_split(d, g):
     bsz, hkv = len(lens), 2
     mp = 20
     pt = page_table(340 + d, bsz, mp)
-    pair = KpcPair(hkv, d, d, (4, 2), bsz * mp, 0, max_batch=bsz)
+    pair = KpcPair(hkv, d, d, bits, bsz * mp, 0, max_batch=bsz)
     k, v = _kv(341, bsz, int(lens.max()), hkv, d)
     for b in range(bsz):
         pair.gpu.append(0, dev_bf16(k[b:b + 1, :lens[b]]), dev_bf16(v[b:b + 1, :lens[b]]),
