@@ -723,13 +723,15 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   // the page's scales go into the A operand and the query keeps its constant
   // B fragments (KPC2); wider codes form B per page from fp32 queries
   constexpr bool KPC2 = KPC && BK == 2;
-  query_quant_prologue<D, KPC && !KPC2>(p, sm, qv);
+  // 4-bit codes (|c| <= 7) take the page's scales split in two exact parts
+  constexpr bool KPC4 = KPC && BK == 4;
+  query_quant_prologue<D, KPC && !KPC2 && !KPC4>(p, sm, qv);
 
   // ---- B fragments of the K-side MMA: column n = g is query head g / 2, its
   //      hi part for even g and lo part for odd g (per page in the
   //      key-per-channel mode)
   uint32_t bq[NJ][2];
-  if constexpr (!KPC || KPC2) {
+  if constexpr (!KPC || KPC2 || KPC4) {
     const uint32_t* qh = reinterpret_cast<const uint32_t*>(sm.qtab) + (g >> 1) * D;
     const int sh = (g & 1) ? 16 : 0;
 #pragma unroll
@@ -812,6 +814,62 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     }
     sc0 = a[0] + a[1];
     sc1 = a[2] + a[3];
+  };
+  // 4-bit key-per-channel: the page's scales, normalised by 2^-E (2^E the
+  // binade of the largest, so every s' < 2), split as s' = s_hi + s_lo with
+  // s_hi keeping 8 significant bits and s_lo the other 3: c s_hi and c s_lo
+  // (|c| <= 7) are exact in fp16, and two MMAs against the constant query
+  // fragments give sum_d c s'_d q_d; the scaled score is (a_hi + a_lo) 2^E
+  auto scores_kpc4 = [&](uint32_t st, float& sc0, float& sc1) {
+    uint32_t w0[KWORDS], w1[KWORDS];
+    lds_u32<KSLICE>(st + koff, w0);
+    lds_u32<KSLICE>(st + koff + 8 * KB, w1);
+    uint32_t sw[QD / 2];                         // scales of dims [c QD, (c + 1) QD)
+#pragma unroll
+    for (int i = 0; i < QD / 16; ++i) lds_u32<32>(st + KSZ + c * (QD * 2) + 32 * i, sw + 8 * i);
+    uint32_t mx = sw[0];                         // scales are >= 0: fp16 bits order them
+#pragma unroll
+    for (int i = 1; i < QD / 2; ++i) mx = __vmaxu2(mx, sw[i]);
+    mx = max(mx & 0xffffu, mx >> 16);
+    mx = max(mx, __shfl_xor_sync(kFullMask, mx, 1));
+    mx = max(mx, __shfl_xor_sync(kFullMask, mx, 2));
+    const int ex = max(static_cast<int>(mx >> 10), 1) - 15;    // subnormal: -14
+    const float up = __int_as_float((127 + ex) << 23);
+    const unsigned dh = -ex >= -14 ? static_cast<unsigned>(15 - ex) << 10 : 1u << (24 - ex);
+    const uint32_t down2 = dh | (dh << 16);
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      uint32_t shi[2], slo[2];
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        int d0, d1;
+        kpair_dims<D, BK>(0, 2 * j + s2, d0, d1);
+        uint32_t sp = __byte_perm(sw[d0 >> 1], sw[d1 >> 1],
+                                  ((d0 & 1) ? 0x0032u : 0x0010u) | ((d1 & 1) ? 0x7600u : 0x5400u));
+        __half2 sn = __hmul2(*reinterpret_cast<const __half2*>(&sp),
+                             *reinterpret_cast<const __half2*>(&down2));
+        const uint32_t snb = *reinterpret_cast<const uint32_t*>(&sn);
+        shi[s2] = snb & 0xfff8fff8u;             // the low 3 mantissa bits cleared
+        const __half2 lo = __hsub2(sn, *reinterpret_cast<const __half2*>(&shi[s2]));
+        slo[s2] = *reinterpret_cast<const uint32_t*>(&lo);
+      }
+      auto scaled = [&](uint32_t code2, uint32_t s2v) -> uint32_t {
+        const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&code2),
+                                  *reinterpret_cast<const __half2*>(&s2v));
+        return *reinterpret_cast<const uint32_t*>(&r);
+      };
+      const uint32_t c00 = kpair_signed<BK>(w0, 2 * j), c10 = kpair_signed<BK>(w1, 2 * j);
+      const uint32_t c01 = kpair_signed<BK>(w0, 2 * j + 1), c11 = kpair_signed<BK>(w1, 2 * j + 1);
+      const uint32_t xh[4] = {scaled(c00, shi[0]), scaled(c10, shi[0]), scaled(c01, shi[1]),
+                              scaled(c11, shi[1])};
+      const uint32_t xl[4] = {scaled(c00, slo[0]), scaled(c10, slo[0]), scaled(c01, slo[1]),
+                              scaled(c11, slo[1])};
+      mma_16816(a, xh, bq[j][0], bq[j][1]);
+      mma_16816(a, xl, bq[j][0], bq[j][1]);
+    }
+    sc0 = (a[0] + a[1]) * up;
+    sc1 = (a[2] + a[3]) * up;
   };
   auto scores_kpc = [&](uint32_t st, float& sc0, float& sc1) {
     uint32_t w0[KWORDS], w1[KWORDS];
@@ -936,6 +994,9 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     if constexpr (KPC2) {
       scores_kpc2(sta, sa0, sa1);
       if (has_b) scores_kpc2(stb, sb0, sb1);
+    } else if constexpr (KPC4) {
+      scores_kpc4(sta, sa0, sa1);
+      if (has_b) scores_kpc4(stb, sb0, sb1);
     } else if constexpr (KPC) {
       scores_kpc(sta, sa0, sa1);
       if (has_b) scores_kpc(stb, sb0, sb1);
@@ -1103,7 +1164,7 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
 #pragma unroll
           for (int e = 0; e < E; ++e) {
             float qe = sm.qtab[i * D + E * lane + e];
-            if constexpr (KPC2) {                // the packed (hi, lo) pair of e q''
+            if constexpr (KPC2 || KPC4) {        // the packed (hi, lo) pair of e q''
               const uint32_t hl = __float_as_uint(qe);
               const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hl));
               qe = f.x + f.y;
