@@ -401,7 +401,7 @@ def run_kvq(args) -> None:
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
         t_start = time.time()
-        ms = timed(graph.replay, args.steps)
+        ms = nvtx(torch, "decode step graph (timed)", timed, graph.replay, args.steps)
         clocks.mark(t_start, time.time())
     # isolated launches (events between them), after the timed region
     for _ in range(3):
@@ -474,7 +474,7 @@ def run_kvq(args) -> None:
     for _ in range(max(1, args.warmup)):
         with torch.cuda.stream(stream):
             e2e_graph.replay()
-    ms_e2e = timed(e2e_graph.replay, args.steps)
+    ms_e2e = nvtx(torch, "e2e step graph (timed)", timed, e2e_graph.replay, args.steps)
     o_check = torch.from_numpy(o_h.numpy().copy())
     assert torch.equal(o_check, o_all.cpu()), "e2e: host copy of o differs from the device o"
     h2d = q_h.numel() * 2 + knew_h.numel() * 2 + vnew_h.numel() * 2
@@ -483,8 +483,10 @@ def run_kvq(args) -> None:
     del cache, ws, knew, vnew, q_all, o_all
     torch.cuda.synchronize(dev)
     # append sweep: 8 sequences x 8192 new tokens into empty caches
-    append = append_sweep(kvq, torch, dev) if not args.skip_append else None
-    calib = calibration_bench(kvq, torch, dev) if not args.skip_append else None
+    append = nvtx(torch, "append sweep", append_sweep, kvq, torch, dev) \
+        if not args.skip_append else None
+    calib = nvtx(torch, "calibration", calibration_bench, kvq, torch, dev) \
+        if not args.skip_append else None
     mixed = long_ctx = qerr = lq = kpc = None
     if not args.skip_configs:
         # the mixed-bits allocation takes (alpha, beta) from the calibration
@@ -494,12 +496,15 @@ def run_kvq(args) -> None:
             alpha = np.ones(N_LAYERS * hkv * 2)
             beta = np.full(N_LAYERS * hkv * 2, 4.0)
         if N_LAYERS == MIXED_32L.num_layers:
-            mixed = mixed_bits_bench(kvq, torch, dev, alpha, beta, min(args.steps, 10),
-                                     args.warmup)
-        long_ctx = long_context_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
-        lq = logquant_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
-        kpc = key_channel_bench(kvq, torch, dev, N_LAYERS, args.steps, args.warmup)
-        qerr = quant_error_report(kvq, torch, dev)
+            mixed = nvtx(torch, "mixed bits", mixed_bits_bench, kvq, torch, dev, alpha, beta,
+                         min(args.steps, 10), args.warmup)
+        long_ctx = nvtx(torch, "long context", long_context_bench, kvq, torch, dev, N_LAYERS,
+                        args.steps, args.warmup)
+        lq = nvtx(torch, "LogQuant", logquant_bench, kvq, torch, dev, N_LAYERS, args.steps,
+                  args.warmup)
+        kpc = nvtx(torch, "key-per-channel", key_channel_bench, kvq, torch, dev, N_LAYERS,
+                   args.steps, args.warmup)
+        qerr = nvtx(torch, "quantization error", quant_error_report, kvq, torch, dev)
     if calib is not None:
         calib.pop("_alpha")
         calib.pop("_beta")
@@ -638,6 +643,16 @@ def calibration_bench(kvq, torch, dev) -> dict:
             "fit_ms": round(fit_s * 1e3, 3),
             "beta_range": [round(float(beta.min()), 3), round(float(beta.max()), 3)],
             "_alpha": alpha, "_beta": beta}
+
+
+def nvtx(torch, name, fn, *a, **kw):
+    """fn(*a, **kw) inside an NVTX range named `name` (visible to a timeline
+    profiler; no effect otherwise)."""
+    torch.cuda.nvtx.range_push(name)
+    try:
+        return fn(*a, **kw)
+    finally:
+        torch.cuda.nvtx.range_pop()
 
 
 def graph_step_bench(torch, dev, cache, n_layers, knew, vnew, q_all, pt, after, o_all, ws,

@@ -86,3 +86,35 @@ def test_quant_error_long_context():
     w = LONG_CONTEXT
     out = _errors(w, [(0, 0), (0, 3), (0, 6)])
     _assert_rotation_helps(out, w.had_block)
+
+
+def test_keys_with_larger_norms_want_the_bits_on_the_gpu():
+    """"Quantize What Counts: More for Keys, Less for Values", through the
+    kernels: the Llama-3-8B-shaped layer's keys (4 outlier channels x10..50)
+    outweigh its values, and at the same total bits the K4V2 cache has the
+    lower attention error against unquantized attention than K2V4 (2 sequences
+    x 1024 tokens, every head of both)."""
+    w = LLAMA3_8B_LAYER
+    bsz, n = 2, 1024
+    k = kv_tokens(w.seed, 0, bsz, n, w.hkv, w.head_dim, w.k_outliers, w.outlier_lo, w.outlier_hi)
+    v = kv_tokens(w.seed, 1, bsz, n, w.hkv, w.head_dim, w.v_outliers, w.outlier_lo, w.outlier_hi)
+    assert np.linalg.norm(k) > 2 * np.linalg.norm(v)
+    q = queries(w.seed, 0, bsz, w.hq, w.head_dim, False)
+    mp = n // 16
+    pt = page_table(w.seed, bsz, mp)
+    lens = np.full(bsz, n, np.int32)
+    ref = attention.exact_decode(q, k, v, lens)
+    kd, vd, ptd = _dev_bf16(k), _dev_bf16(v), _dev_i32(pt)
+    qd = torch.from_numpy(q).cuda().to(torch.bfloat16)
+    err = {}
+    for kb, vb in ((4, 2), (2, 4)):
+        bits = np.tile(np.array([kb, vb]), (1, w.hkv, 1))
+        c = kvq.Cache(1, w.hkv, w.head_dim, w.had_block, bits, bsz * mp, max_batch=bsz)
+        c.append(0, kd, vd, ptd, _dev_i32(np.zeros(bsz, np.int32)))
+        o = c.decode(0, qd, ptd, _dev_i32(lens)).cpu().numpy()
+        assert c.get_status() == 0
+        st = ocache.CacheState(w.head_dim, w.had_block, 0, bits, [c.pool_host(0)], None)
+        compare_outputs(o, attention.decode(st, 0, q.astype(np.float64), pt, lens))
+        err[(kb, vb)] = attention.quant_error(o, ref)["rel_l2"]
+    print("relative L2 error", err)
+    assert err[(4, 2)] < 0.75 * err[(2, 4)], err

@@ -170,3 +170,28 @@ def test_rotation_lowers_the_error_on_outlier_channels():
         errs[block] = attention.quant_error(attention.decode(st, 0, q, pt, np.array([n])), ref)
     assert errs[64]["rel_l2"] < errs[1]["rel_l2"]
     assert errs[64]["mean_abs"] < errs[1]["mean_abs"]
+
+
+def test_keys_with_larger_norms_want_the_bits():
+    """"Quantize What Counts: More for Keys, Less for Values": when the keys'
+    norms exceed the values', giving the keys the wider codes lowers the
+    attention error at the same total bits (K4V2 against K2V4), and K4V2 stays
+    within a factor of two of K4V4.
+    Keys with 4 outlier channels (x10..50), plain values, as in the
+    Llama-3-8B-shaped workload; Hadamard 64."""
+    n, d, hkv = 512, 64, 4
+    k = kv_tokens(2002, 0, 1, n, hkv, d, 4, 10.0, 50.0)
+    v = kv_tokens(2002, 1, 1, n, hkv, d, 0, 1.0, 1.0)
+    assert np.linalg.norm(k) > 2 * np.linalg.norm(v)
+    q = queries(2002, 0, 1, 4 * hkv, d, True)
+    pt = page_table(2002, 1, n // 16)
+    ref = attention.exact_decode(q, k, v, np.array([n]))
+    err = {}
+    for kb, vb in ((4, 2), (2, 4), (4, 4)):
+        st = cache.new_state(1, n // 16, d, 64, np.array([[[kb, vb]] * hkv]))
+        cache.append(st, 0, k, v, pt, np.zeros(1, np.int32))
+        err[(kb, vb)] = attention.quant_error(attention.decode(st, 0, q, pt, np.array([n])),
+                                              ref)["rel_l2"]
+    # (relative L2 on this data: K4V2 0.53, K2V4 1.04, K4V4 0.31)
+    assert err[(4, 2)] < 0.75 * err[(2, 4)], err
+    assert err[(4, 4)] < err[(4, 2)] < 2.0 * err[(4, 4)], err
