@@ -1920,7 +1920,7 @@ cudaError_t launch_d(const DecodeParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.NS, p.Hkv, p.B);
+  cfg.gridDim = dim3(p.NS, p.grid_heads > 0 ? p.grid_heads : p.Hkv, p.B);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = bytes;
   cfg.stream = s;

@@ -194,3 +194,13 @@ def test_step_overlapped_layers(window):
         ref = attention.decode(st, l, queries(96, l, bsz, hkv * g, d, False).astype(np.float64),
                                pt, np.full(bsz, t, np.int32))
         compare_outputs(outs[1][l], ref)
+
+
+@pytest.mark.parametrize("window", [0, 64])
+def test_step_runs_of_heads(window):
+    # 8-bit keys beside 2- and 4-bit ones: the larger segments would lower the
+    # whole launch's CTAs per SM, so the layer decodes as several launches over
+    # runs of heads (each with its own stage size and split plan, sharing the
+    # tickets); a short sequence (cluster merge) and a long one (ticket merge)
+    bits = np.array([[[4, 2], [8, 4], [8, 4], [4, 4], [2, 2], [8, 8], [4, 2], [4, 2]]])
+    _steps(8, 128, 128, bits, [40, 3000], 20, window=window)
