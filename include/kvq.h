@@ -242,10 +242,7 @@ size_t kvq_decode_workspace_bytes(const kvq_cache* cache, int B, int Hq, int max
  * reserve (more of them when the batch leaves the wave room).  In
  * the key-per-channel mode the splits read each page's channel scales and one
  * more CTA attends over the ring's positions Q(L) .. L - 1.
- * One kernel launch, or one per run of consecutive KV heads when the layer's
- * heads have page segments of such different sizes (8-bit keys beside narrower
- * ones) that one launch would hold fewer CTAs per SM; the runs touch disjoint
- * heads and share the workspace.  Returns KVQ_OK once enqueued.
+ * One kernel launch.  Returns KVQ_OK once enqueued.
  */
 kvq_status kvq_decode_attn(const kvq_cache* cache, int layer, const void* q, int q_is_fp32,
                            const int32_t* page_table, int max_pages, const int32_t* seq_lens,
@@ -276,8 +273,7 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, int layer, const void* q, int
  * In the key-per-channel mode the step is kvq_append of the token (whose page,
  * once complete and out of the window, is quantized) followed by the decode:
  * three launches.  Two steps on one cache must be stream-ordered.  Otherwise
- * one kernel launch (one per run of heads, as for kvq_decode_attn).  Returns
- * KVQ_OK once enqueued.
+ * one kernel launch.  Returns KVQ_OK once enqueued.
  */
 kvq_status kvq_decode_step(const kvq_cache* cache, int layer, const void* K_new,
                            const void* V_new, const void* q, int q_is_fp32,

@@ -2,7 +2,6 @@
 // split planning, kernel dispatch, and the RateQuant greedy allocator.
 #include <cuda_runtime_api.h>
 
-#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -160,34 +159,18 @@ struct Plan {
   size_t counter_bytes, bytes;
 };
 
-// Split count for one layer: as many splits per (sequence, KV head) as keep the
-// whole grid resident in one wave (CTAs per SM from the occupancy calculator
-// for this layer's shared-memory size), at least 8 pages (two per warp) per
-// split, at most the kernel's split limit.
-// Bytes of head h's segment in a page of this geometry.
-int head_bytes(const kvq_cache* c, const kvq::LayerGeom& g, int h) {
-  return static_cast<int>((h + 1 < c->num_kv_heads ? g.head_off[h + 1] : g.page_bytes) -
-                          g.head_off[h]);
-}
-
-// Resident CTAs per SM of this cache's decode kernel with `stage_bytes` stages
-// (cached per shared-memory size), -1 on error.
-int resident_ctas(const kvq_cache* c, int stage_bytes) {
-  kvq::DecodeParams probe;
-  std::memset(&probe, 0, sizeof probe);
-  probe.stage_bytes = stage_bytes;
-  probe.R = ring_rows(c);
-  probe.lq_w = c->logquant_w;
-  probe.kpc = c->key_per_channel;
-  const size_t smem = kvq::decode_smem_bytes(probe, c->head_dim);
-  static thread_local int cache_key[8] = {0}, cache_val[8] = {0};
+// Resident decode CTAs per SM with `smem` bytes of shared memory (the
+// occupancy calculator's answer, cached per size, head_dim and mode); <= 0 when
+// none fits.
+int resident_ctas(const kvq_cache* c, size_t smem) {
+  static thread_local int cache_key[4] = {0, 0, 0, 0}, cache_val[4] = {0, 0, 0, 0};
   const int mode = decode_mode(c);
   const int key = (static_cast<int>(smem) * 2 + (c->head_dim == 128)) * 4 + mode + 1;
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < 4; ++i)
     if (cache_key[i] == key) return cache_val[i];
   const int bps = kvq::decode_blocks_per_sm(c->head_dim, smem, mode);
   if (bps > 0) {
-    for (int i = 7; i > 0; --i) {
+    for (int i = 3; i > 0; --i) {
       cache_key[i] = cache_key[i - 1];
       cache_val[i] = cache_val[i - 1];
     }
@@ -197,27 +180,26 @@ int resident_ctas(const kvq_cache* c, int stage_bytes) {
   return bps;
 }
 
-int stage_of(int head_bytes) { return (head_bytes + 127) / 128 * 128; }
-
-// The split plan of a launch over heads [h0, h1) of this layer.
+// Split count for one layer: as many splits per (sequence, KV head) as keep the
+// whole grid resident in one wave (CTAs per SM from the occupancy calculator
+// for this layer's shared-memory size), at least 8 pages (two per warp) per
+// split, at most the kernel's split limit.
 kvq_status plan_decode(const kvq_cache* c, const kvq::LayerGeom& g, int B, int max_pages,
-                       Plan* pl, int h0 = 0, int h1 = -1) {
-  if (h1 < 0) h1 = c->num_kv_heads;
+                       Plan* pl) {
   const int sms = sm_count();
   if (sms <= 0) return fail(KVQ_ECUDA, "no CUDA device visible");
   kvq::DecodeParams probe;
   std::memset(&probe, 0, sizeof probe);
-  int maxh = 0;
-  for (int h = h0; h < h1; ++h) maxh = std::max(maxh, head_bytes(c, g, h));
-  probe.stage_bytes = stage_of(maxh);
+  probe.stage_bytes = (g.max_head_bytes + 127) / 128 * 128;
   probe.R = ring_rows(c);
   probe.lq_w = c->logquant_w;
   probe.kpc = c->key_per_channel;
-  const int bps = resident_ctas(c, probe.stage_bytes);
+  const size_t smem = kvq::decode_smem_bytes(probe, c->head_dim);   // no cluster merge
+  const int bps = resident_ctas(c, smem);
   if (bps <= 0)
     return fail(KVQ_ECUDA, "decode kernel cannot be resident with %zu bytes of shared memory",
-                kvq::decode_smem_bytes(probe, c->head_dim));
-  const long long units = static_cast<long long>(B) * (h1 - h0);
+                smem);
+  const long long units = static_cast<long long>(B) * c->num_kv_heads;
   // with a window (a LogQuant reserve, a key-per-channel ring), each unit's
   // window CTA takes one of the wave's slots; the key-per-channel ring of a
   // cache without a window holds at most the 15 rows of the open page, which
@@ -238,66 +220,17 @@ kvq_status plan_decode(const kvq_cache* c, const kvq::LayerGeom& g, int B, int m
   pl->stage_bytes = probe.stage_bytes;
   pl->NS = pl->S + extra;
   pl->cluster = pl->NS <= kvq::decode_max_cluster() ? 1 : 0;
-  // tickets for every (sequence, KV head) of the layer; partials indexed with
-  // the layer's head stride
-  const size_t all = static_cast<size_t>(B) * c->num_kv_heads;
-  pl->counter_bytes = (all * 4 + 255) / 256 * 256;
-  pl->bytes = pl->counter_bytes + all * pl->NS * kvq::kMaxGroup * (c->head_dim + 2) * sizeof(float);
-  return KVQ_OK;
-}
-
-// A layer's decode as up to kMaxRuns launches over runs of consecutive heads.
-// One launch normally; when some heads' page segments are so much larger than
-// the others' (8-bit keys beside 4-bit ones) that their stage size lowers the
-// resident CTAs per SM of the whole launch, the heads of each size class form
-// runs of their own, each with its own stage size and split plan (more CTAs
-// per SM for the smaller segments, more splits for the larger).
-constexpr int kMaxRuns = 8;
-struct LayerPlan {
-  int nruns;
-  int h0[kMaxRuns], h1[kMaxRuns];
-  Plan pl[kMaxRuns];
-  size_t part_off[kMaxRuns];   // each run's partials, after the shared tickets
-  size_t bytes;                // workspace bytes of the whole layer
-};
-
-kvq_status plan_layer(const kvq_cache* c, const kvq::LayerGeom& g, int B, int max_pages,
-                      LayerPlan* lp) {
-  const int hkv = c->num_kv_heads;
-  int best = 0, single = -1, fast[kvq::kMaxHeads];
-  int maxh = 0;
-  for (int h = 0; h < hkv; ++h) maxh = std::max(maxh, head_bytes(c, g, h));
-  single = resident_ctas(c, stage_of(maxh));
-  for (int h = 0; h < hkv; ++h) {
-    fast[h] = resident_ctas(c, stage_of(head_bytes(c, g, h)));
-    best = std::max(best, fast[h]);
+  if (pl->cluster && pl->NS > 1) {
+    // the cluster merge gathers the NS partials in CTA 0's shared memory: it is
+    // kept while that leaves the CTAs per SM the split count assumed, else the
+    // partials meet in global memory
+    probe.cluster = 1;
+    probe.NS = pl->NS;
+    if (resident_ctas(c, kvq::decode_smem_bytes(probe, c->head_dim)) < bps) pl->cluster = 0;
   }
-  lp->nruns = 1;
-  lp->h0[0] = 0;
-  lp->h1[0] = hkv;
-  if (single > 0 && best > single) {
-    int n = 0, h0 = 0;
-    for (int h = 1; h <= hkv; ++h) {
-      if (h == hkv || (fast[h] == best) != (fast[h0] == best)) {
-        if (n == kMaxRuns) { n = kMaxRuns + 1; break; }
-        lp->h0[n] = h0;
-        lp->h1[n] = h;
-        ++n;
-        h0 = h;
-      }
-    }
-    if (n <= kMaxRuns) lp->nruns = n;
-    else { lp->h0[0] = 0; lp->h1[0] = hkv; lp->nruns = 1; }
-  }
-  size_t off = 0;
-  for (int r = 0; r < lp->nruns; ++r) {
-    const kvq_status st = plan_decode(c, g, B, max_pages, &lp->pl[r], lp->h0[r], lp->h1[r]);
-    if (st != KVQ_OK) return st;
-    if (r == 0) off = lp->pl[0].counter_bytes;
-    lp->part_off[r] = off;
-    off += lp->pl[r].bytes - lp->pl[r].counter_bytes;
-  }
-  lp->bytes = off;
+  pl->counter_bytes = (static_cast<size_t>(units) * 4 + 255) / 256 * 256;
+  pl->bytes = pl->counter_bytes + static_cast<size_t>(units) * pl->NS * kvq::kMaxGroup *
+                                      (c->head_dim + 2) * sizeof(float);
   return KVQ_OK;
 }
 
@@ -342,11 +275,11 @@ kvq_status decode_impl(const kvq_cache* cache, int layer, const void* K_new, con
     return fail(KVQ_EINVAL, "key-per-channel decode steps append before the decode");
   if (!std::isfinite(softmax_scale) || softmax_scale < 0.f)
     return fail(KVQ_EINVAL, "softmax_scale must be finite and >= 0");
-  LayerPlan lp;
-  st = plan_layer(cache, p.geom, B, max_pages, &lp);
+  Plan pl;
+  st = plan_decode(cache, p.geom, B, max_pages, &pl);
   if (st != KVQ_OK) return st;
-  if (ws_bytes < lp.bytes)
-    return fail(KVQ_EWORKSPACE, "workspace of %zu bytes < %zu required", ws_bytes, lp.bytes);
+  if (ws_bytes < pl.bytes)
+    return fail(KVQ_EWORKSPACE, "workspace of %zu bytes < %zu required", ws_bytes, pl.bytes);
   const float scale =
       softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(cache->head_dim));
   p.pool = static_cast<const uint8_t*>(cache->layer_pools[layer]);
@@ -355,7 +288,8 @@ kvq_status decode_impl(const kvq_cache* cache, int layer, const void* K_new, con
   p.page_table = page_table;
   p.seq_lens = seq_lens;
   p.o = o;
-
+  p.counters = static_cast<unsigned int*>(workspace);
+  p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.counter_bytes);
   p.status = cache->status_dev;
   p.q_fp32 = q_is_fp32 ? 1 : 0;
   p.max_pages = max_pages;
@@ -370,47 +304,20 @@ kvq_status decode_impl(const kvq_cache* cache, int layer, const void* K_new, con
   p.lq_rows = cache->logquant_w ? kvq::lq_rows(cache->logquant_w, p.lq_a) : 0;
   p.num_pages = cache->num_pages;
   p.had_block = cache->had_block;
+  p.S = pl.S;
+  p.NS = pl.NS;
+  p.pages_per_split = pl.pages_per_split;
   p.overlap = (cache->launch_flags & KVQ_LAUNCH_OVERLAP) ? 1 : 0;
+  p.cluster = pl.cluster;
+  p.stage_bytes = pl.stage_bytes;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.wait_log2 = copy_wait_log2();
   p.step = step ? 1 : 0;
   p.k_new = static_cast<const uint16_t*>(K_new);
   p.v_new = static_cast<const uint16_t*>(V_new);
   if (check_only) return KVQ_OK;
-  // one launch per run of heads: the per-head pointers and the geometry start
-  // at the run's first head, the head stride stays the layer's (Hkv)
-  const kvq::LayerGeom geom = p.geom;
-  const size_t qelem = q_is_fp32 ? 4 : 2;
-  const size_t plane = uses_ring(cache)
-                           ? static_cast<size_t>(2) * (p.lq_w ? p.lq_rows : p.R) * cache->head_dim
-                           : 0;
-  for (int r = 0; r < lp.nruns; ++r) {
-    const int h0 = lp.h0[r], nh = lp.h1[r] - lp.h0[r];
-    const Plan& pl = lp.pl[r];
-    kvq::DecodeParams pr = p;
-    for (int h = 0; h < nh; ++h) {
-      pr.geom.head_off[h] = geom.head_off[h0 + h];
-      pr.geom.bits[h][0] = geom.bits[h0 + h][0];
-      pr.geom.bits[h][1] = geom.bits[h0 + h][1];
-    }
-    pr.grid_heads = nh;
-    pr.q = static_cast<const uint8_t*>(q) + static_cast<size_t>(h0) * G * cache->head_dim * qelem;
-    pr.o = o + static_cast<size_t>(h0) * G * cache->head_dim;
-    if (p.window) pr.window = p.window + static_cast<size_t>(h0) * plane;
-    if (step) {
-      pr.k_new = p.k_new + static_cast<size_t>(h0) * cache->head_dim;
-      pr.v_new = p.v_new + static_cast<size_t>(h0) * cache->head_dim;
-    }
-    pr.counters = static_cast<unsigned int*>(workspace) + h0;
-    pr.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lp.part_off[r]);
-    pr.S = pl.S;
-    pr.NS = pl.NS;
-    pr.pages_per_split = pl.pages_per_split;
-    pr.cluster = pl.cluster;
-    pr.stage_bytes = pl.stage_bytes;
-    const cudaError_t e = kvq::launch_decode(pr, cache->head_dim, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return fail(KVQ_ECUDA, "decode launch: %s", cudaGetErrorString(e));
-  }
+  const cudaError_t e = kvq::launch_decode(p, cache->head_dim, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "decode launch: %s", cudaGetErrorString(e));
   return KVQ_OK;
 }
 
@@ -537,10 +444,10 @@ size_t kvq_decode_workspace_bytes(const kvq_cache* cache, int B, int Hq, int max
   size_t most = 0;   // enough for every layer
   for (int layer = 0; layer < cache->num_layers; ++layer) {
     kvq::LayerGeom g;
-    LayerPlan lp;
+    Plan pl;
     if (check_geometry(cache, layer, &g) != KVQ_OK) return 0;
-    if (plan_layer(cache, g, B, max_pages, &lp) != KVQ_OK) return 0;
-    if (lp.bytes > most) most = lp.bytes;
+    if (plan_decode(cache, g, B, max_pages, &pl) != KVQ_OK) return 0;
+    if (pl.bytes > most) most = pl.bytes;
   }
   return most;
 }

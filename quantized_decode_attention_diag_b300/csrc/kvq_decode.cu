@@ -81,18 +81,27 @@ struct Smem {
 template <int D>
 __host__ __device__ constexpr int merge_floats() { return kDecodeWarps * kMaxGroup * (D + 2); }
 
-// alias_merge (the key-per-channel kernel): the warps' merge region shares
-// the stage area instead of having its own, so that four CTAs of the larger
-// page segments still fit an SM.  Its first write comes after the barrier at
-// which every warp is done with its stages (or with the window's rows).
-__host__ __device__ constexpr int header_bytes(int d, bool alias_merge = false) {
+// CTAs whose partials CTA 0 gathers in shared memory: those of a cluster merge
+// over more than one split (a single split combines its own partial).
+__host__ __device__ constexpr int rbuf_ctas(int cluster, int ns) {
+  return cluster && ns > 1 ? ns : 0;
+}
+
+// Bytes before the stage area: query fragments, a few words, the page-copy
+// barriers, this CTA's partial, the cluster receive buffer of rbuf_ctas
+// partials, and 128 bytes of slack for aligning the area.  The warps' merge
+// region has no room of its own: it shares the stage area, and its first write
+// comes after the barrier at which every warp is done with its stages (or with
+// the window's rows), so that four CTAs of 8-bit keys with 4-bit values still
+// fit an SM.
+__host__ __device__ constexpr int header_bytes(int d, int rbuf_n) {
   return ((d * kMaxGroup * 4 + 64 + kDecodeWarps * kDecodeStages * 8 +
-           ((alias_merge ? 0 : kDecodeWarps) + 1 + kMaxCluster) * kMaxGroup * (d + 2) * 4) +
+           (1 + rbuf_n) * kMaxGroup * (d + 2) * 4) +
           127) / 128 * 128 + 128;
 }
 
-template <int D, bool ALIAS_MERGE = false>
-__device__ __forceinline__ Smem carve(uint8_t* base) {
+template <int D>
+__device__ __forceinline__ Smem carve(uint8_t* base, int rbuf_n) {
   Smem s;
   s.qtab = reinterpret_cast<float*>(base);
   uint8_t* misc = base + kMaxGroup * D * 4;
@@ -102,13 +111,12 @@ __device__ __forceinline__ Smem carve(uint8_t* base) {
   s.wait_log2 = reinterpret_cast<int*>(misc + 24);
   s.qscl = reinterpret_cast<float*>(misc + 32);
   s.bars = reinterpret_cast<uint64_t*>(misc + 64);
-  s.merge = reinterpret_cast<float*>(misc + 64 + kDecodeWarps * kDecodeStages * 8);
-  s.cpart = ALIAS_MERGE ? s.merge : s.merge + merge_floats<D>();
-  // then rbuf [kMaxCluster][kMaxGroup * (D + 2)] (cluster mode, CTA 0: every
-  // CTA's partial, pushed there through distributed shared memory; see rbuf())
-  uint8_t* a = reinterpret_cast<uint8_t*>(s.cpart + (1 + kMaxCluster) * kMaxGroup * (D + 2));
+  s.cpart = reinterpret_cast<float*>(misc + 64 + kDecodeWarps * kDecodeStages * 8);
+  // then rbuf [rbuf_n][kMaxGroup * (D + 2)] (cluster mode, CTA 0: every CTA's
+  // partial, pushed there through distributed shared memory; see rbuf())
+  uint8_t* a = reinterpret_cast<uint8_t*>(s.cpart + (1 + rbuf_n) * kMaxGroup * (D + 2));
   s.area = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(a) + 127) & ~uintptr_t(127));
-  if (ALIAS_MERGE) s.merge = reinterpret_cast<float*>(s.area);
+  s.merge = reinterpret_cast<float*>(s.area);
   return s;
 }
 
@@ -709,7 +717,7 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   // decode step: the warp owning the page of the last quantized position
   // quantizes the token there while its first copies are in flight
   int kpatch = -1;
-  uint8_t* pbuf = reinterpret_cast<uint8_t*>(sm.merge);
+  uint8_t* pbuf = reinterpret_cast<uint8_t*>(sm.cpart);   // free until the warps merge
   if (!KPC && p.step && lq > 0) {   // (the key-per-channel mode appends before the launch)
     const int pl = npages - 1;
     if (pl >= pg0 && pl < pg1 && (pl - pg0) % kDecodeWarps == warp) {
@@ -1334,6 +1342,7 @@ __device__ void attend_rows(const DecodeParams& p, const Smem& sm, int nw, float
       }
     }
   }
+  __syncthreads();  // every warp is done with the scores (the merge region shares them)
   float* macc = sm.merge;                       // [warps][kMaxGroup][D]
 #pragma unroll
   for (int i = 0; i < kMaxGroup; ++i)
@@ -1699,7 +1708,7 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank)
 }
 // Cluster mode, CTA 0 after the cluster barrier: warp i merges query head i
 // of (b, h) over the NS partials in rbuf (partial s from CTA rank s), as
-// combine_global.
+// combine_global; a single split's own partial is cpart.
 template <int D>
 __device__ void combine_cluster(const DecodeParams& p, const Smem& sm, int b, int h) {
   constexpr int E = D / 32;
@@ -1707,7 +1716,7 @@ __device__ void combine_cluster(const DecodeParams& p, const Smem& sm, int b, in
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= p.G) return;
   const int i = warp, NS = p.NS, nq = p.S;
-  const float* rb = rbuf<D>(sm);
+  const float* rb = NS > 1 ? rbuf<D>(sm) : sm.cpart;
   float ms = -CUDART_INF_F, ls = 0.f;
   if (lane < NS) {
     ms = part_m<D>(rb + lane * PS)[i];
@@ -1764,7 +1773,7 @@ __device__ __forceinline__ void push_partial(const Smem& sm, uint32_t rank) {
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  const Smem sm = carve<D, MODE == kModeKeyChannel>(smem_raw);
+  const Smem sm = carve<D>(smem_raw, rbuf_ctas(p.cluster, p.NS));
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5;
 
@@ -1853,7 +1862,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
 
   if (p.cluster) {
     const uint32_t rank = cluster_rank();
-    push_partial<D>(sm, rank);
+    if (p.NS > 1) push_partial<D>(sm, rank);
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     if (rank != 0) return;     // nothing reads this CTA's shared memory
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -1886,12 +1895,10 @@ size_t smem_bytes(const DecodeParams& p) {
   // member list [3W]
   const size_t win = p.lq_w ? static_cast<size_t>(kMaxGroup + 1) * 3 * p.lq_w * 4
                             : (p.R > 0 ? win_bytes(p.R, D) : 0);
-  if (p.kpc) {   // the merge region lives in the stage area
-    const size_t merge = static_cast<size_t>(merge_floats<D>()) * 4;
-    const size_t area = stages > win ? stages : win;
-    return header_bytes(D, true) + (area > merge ? area : merge);
-  }
-  return header_bytes(D) + (stages > win ? stages : win);
+  const size_t merge = static_cast<size_t>(merge_floats<D>()) * 4;   // shares the area
+  size_t area = stages > win ? stages : win;
+  if (merge > area) area = merge;
+  return header_bytes(D, rbuf_ctas(p.cluster, p.NS)) + area;
 }
 
 // Lets decode_kernel<D, MODE> use up to the device's opt-in shared memory (set
@@ -1920,7 +1927,7 @@ cudaError_t launch_d(const DecodeParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.NS, p.grid_heads > 0 ? p.grid_heads : p.Hkv, p.B);
+  cfg.gridDim = dim3(p.NS, p.Hkv, p.B);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = bytes;
   cfg.stream = s;

@@ -70,8 +70,6 @@ struct DecodeParams {
   int kpc;                       // key-per-channel mode: per-channel K scales in the
                                  // pages; R is the ring's R + 16 rows; never a step
   LayerGeom geom;
-  int grid_heads;                // KV heads of this launch (the grid's y; the head
-                                 // stride of every index stays Hkv; host only)
 };
 
 // Decode kernel shape (build-time tuning knobs): warps per CTA, pipeline

@@ -197,10 +197,18 @@ def test_step_overlapped_layers(window):
 
 
 @pytest.mark.parametrize("window", [0, 64])
-def test_step_runs_of_heads(window):
-    # 8-bit keys beside 2- and 4-bit ones: the larger segments would lower the
-    # whole launch's CTAs per SM, so the layer decodes as several launches over
-    # runs of heads (each with its own stage size and split plan, sharing the
-    # tickets); a short sequence (cluster merge) and a long one (ticket merge)
+def test_step_mixed_segment_sizes(window):
+    # 8-bit keys beside 2- and 4-bit ones: the largest page segment sets the
+    # layer's stage size, the narrower heads' copies fill part of a stage; a
+    # short sequence (cluster merge) and a long one (ticket merge)
     bits = np.array([[[4, 2], [8, 4], [8, 4], [4, 4], [2, 2], [8, 8], [4, 2], [4, 2]]])
     _steps(8, 128, 128, bits, [40, 3000], 20, window=window)
+
+
+def test_step_ticket_merge_for_wide_segments():
+    # 8-bit keys with 4-bit values (3200-byte stages) beside 4-bit keys, 18
+    # sequences x 8 KV heads: four CTAs per SM give 4 splits per unit on 148
+    # SMs, and a cluster merge's receive buffer for 4 partials would leave 3
+    # CTAs per SM, so the splits merge through global memory instead
+    bits = np.array([[[8, 4], [4, 2]] * 4])
+    _steps(8, 128, 128, bits, [520] * 18, 2)
