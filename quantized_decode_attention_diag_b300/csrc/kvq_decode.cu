@@ -531,11 +531,6 @@ __device__ __forceinline__ void store_codes(uint8_t* dst, const uint32_t (&c)[2]
 // them to the cache page (for later calls) and to `pbuf` in shared memory
 // (K codes [KB], V codes [VB], K (s, z), V (s, z)), from which this launch's
 // staged copy of the page gets patched.  Same rule and same bits as kvq_append.
-// Decode step, one warp: quantizes the token at position pos of (b, h) -- the
-// new token, or with a window the token leaving the ring, the new token taking
-// its ring slot -- into its page, and leaves the patch in pbuf (K codes [KB],
-// V codes [VB], K (s, z), V (s, z)), from which this launch's staged copy of
-// the page gets patched.  Same rule and same bits as kvq_append.
 template <int D>
 __device__ void step_append(const DecodeParams& p, int b, int h, int pos, int bk, int bv,
                             const uint32_t (&tok)[D / 32], uint8_t* pbuf) {
