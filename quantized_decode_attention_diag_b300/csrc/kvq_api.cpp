@@ -372,6 +372,8 @@ kvq_status append_impl(const kvq_cache* cache, int layer, const void* K, const v
   p.R = ring_rows(cache);
   p.num_pages = cache->num_pages;
   p.warps_per_group = static_cast<int>((static_cast<long long>(B) * T_new + 15) / 16);
+  p.div_wpg = kvq::make_fastdiv(static_cast<uint32_t>(p.warps_per_group));
+  p.div_T = kvq::make_fastdiv(static_cast<uint32_t>(T_new));
   p.lq_w = cache->logquant_w;
   p.lq_a = cache->logquant_w ? kvq::lq_log2(cache->logquant_w) : 0;
   p.lq_rows = cache->logquant_w ? kvq::lq_rows(cache->logquant_w, p.lq_a) : 0;

@@ -37,10 +37,10 @@ struct RowRef {
 __device__ __forceinline__ RowRef row_ref(const AppendParams& p, int c) {
   const int row = (threadIdx.x & 31) >> 1;
   RowRef rr;
-  rr.grp = c / p.warps_per_group;
+  rr.grp = static_cast<int>(fastdiv(static_cast<uint32_t>(c), p.div_wpg));
   const int r = (c - rr.grp * p.warps_per_group) * 16 + row;
   if (r < p.B * p.T) {
-    rr.b = r / p.T;
+    rr.b = static_cast<int>(fastdiv(static_cast<uint32_t>(r), p.div_T));
     rr.t = r - rr.b * p.T;
   } else {
     rr.b = -1;
@@ -98,7 +98,8 @@ __device__ __forceinline__ void prefetch_chunk(const AppendParams& p, int c, uin
   constexpr int LPR = D / 8;                   // lanes per row
   constexpr int RPI = 32 / LPR;                // rows per instruction
   const int lane = threadIdx.x & 31;
-  const int grp = c / p.warps_per_group;       // chunk c: group grp, rows blk * 16 ..
+  // chunk c: group grp, rows blk * 16 ..
+  const int grp = static_cast<int>(fastdiv(static_cast<uint32_t>(c), p.div_wpg));
   const int blk = c - grp * p.warps_per_group;
   const int h = grp >> 1, kv = grp & 1;
   const long long rows = static_cast<long long>(p.B) * p.T;

@@ -15,6 +15,31 @@ constexpr int kMaxHeads = 64;    // KV heads per layer
 constexpr int kMaxWindow = 1024; // bf16 recent-token window
 constexpr int kMaxGroup = 4;     // query heads per KV head handled per CTA
 
+// Division by a divisor fixed for a launch, for 0 <= n < 2^31 and 1 <= d < 2^31:
+// floor(n / d) = (mulhi(m, n) + n) >> l with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1 (T. Granlund and P. L. Montgomery, "Division
+// by invariant integers using multiplication", PLDI 1994, section 4).  Then
+// 2^(32+l) < (2^32 + m) d <= 2^(32+l) + 2^l, which makes the quotient exact, and
+// mulhi(m, n) < n keeps the sum below 2^32.
+struct FastDiv {
+  uint32_t m, l;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.l = 0;
+  while ((1ull << f.l) < d) ++f.l;
+  f.m = static_cast<uint32_t>((((1ull << f.l) - d) << 32) / d + 1);
+  return f;
+}
+__host__ __device__ inline uint32_t fastdiv(uint32_t n, const FastDiv& f) {
+#ifdef __CUDA_ARCH__
+  const uint32_t hi = __umulhi(n, f.m);
+#else
+  const uint32_t hi = static_cast<uint32_t>((static_cast<uint64_t>(n) * f.m) >> 32);
+#endif
+  return (hi + n) >> f.l;
+}
+
 // Per-layer page geometry, computed on the host from the bits table.
 struct LayerGeom {
   int head_off[kMaxHeads];       // byte offset of head h's segment in a page
@@ -33,6 +58,7 @@ struct AppendParams {
   int* status;
   int max_pages, B, T, Hkv, R, num_pages;
   int warps_per_group;           // ceil(B * T / 16)
+  FastDiv div_wpg, div_T;        // division by warps_per_group and by T
   int lq_w, lq_a, lq_rows;       // LogQuant base window W (0: off), log2 W, reserve rows
                                  // per plane; `window` is then the reserve
   int kpc;                       // key-per-channel mode: R is then the ring's R + 16 rows

@@ -225,3 +225,56 @@ def test_descriptor_layout_matches_the_header(tmp_path):
     assert out[0] == ctypes.sizeof(kvq.kvq_cache)
     for f, off in zip(fields, out[1:]):
         assert getattr(kvq.kvq_cache, f).offset == off, f
+
+
+def test_invariant_divisor_rule(tmp_path):
+    # the append kernel divides chunk and row indices by the launch's warps per
+    # (head, K|V) group and by T through a multiply-high, an add and a shift;
+    # compiled from the same header, that quotient must equal n / d for every
+    # divisor up to 4096, powers of two, divisors near 2^31, and dividends at
+    # each quotient's edges, near 2^31 and spread between
+    import os
+    import shutil
+    import subprocess
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        pytest.skip("no C++ compiler")
+    cuda_inc = "/usr/local/cuda/include"
+    if not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("no CUDA headers")
+    root = os.path.dirname(os.path.dirname(kvq.LIB_PATH))
+    csrc = os.path.join(os.path.dirname(kvq.LIB_PATH), "csrc")
+    src = tmp_path / "fastdiv.cpp"
+    src.write_text(
+        '#include <cstdio>\n#include <vector>\n#include "kvq_internal.h"\n'
+        "int main() {\n"
+        "  std::vector<unsigned> ds;\n"
+        "  for (unsigned d = 1; d <= 4096; ++d) ds.push_back(d);\n"
+        "  for (int k = 13; k <= 30; ++k) { ds.push_back(1u << k); ds.push_back((1u << k) - 1);\n"
+        "    ds.push_back((1u << k) + 1); }\n"
+        "  for (unsigned d : {2147483647u, 2147483646u, 1073741825u, 16777216u, 131072u, 8192u,\n"
+        "                     1000003u, 65537u, 524287u}) ds.push_back(d);\n"
+        "  long long bad = 0, checked = 0;\n"
+        "  unsigned long long x = 88172645463325252ull;\n"
+        "  for (unsigned d : ds) {\n"
+        "    const kvq::FastDiv f = kvq::make_fastdiv(d);\n"
+        "    auto check = [&](unsigned long long n) {\n"
+        "      if (n >= (1ull << 31)) return;\n"
+        "      ++checked;\n"
+        "      bad += kvq::fastdiv(static_cast<unsigned>(n), f) != n / d;\n"
+        "    };\n"
+        "    for (unsigned n = 0; n < 3000; ++n) check(n);\n"
+        "    for (unsigned long long q = 1; q * d < (1ull << 31); q = q * 3 + 1) {\n"
+        "      check(q * d - 1); check(q * d); check(q * d + 1); }\n"
+        "    const unsigned long long top = (1ull << 31) - 1;\n"
+        "    check(top); check(top - top % d); check(top - top % d - 1);\n"
+        "    for (int i = 0; i < 64; ++i) { x ^= x << 13; x ^= x >> 7; x ^= x << 17; check(x % (1ull << 31)); }\n"
+        "  }\n"
+        '  std::printf("%lld %lld\\n", bad, checked);\n'
+        "  return 0;\n}\n")
+    exe = tmp_path / "fastdiv"
+    subprocess.run([cxx, "-O1", "-std=c++17", "-I", csrc, "-I", os.path.join(root, "include"),
+                    "-I", cuda_inc, str(src), "-o", str(exe)], check=True)
+    bad, checked = map(int, subprocess.run([str(exe)], check=True, capture_output=True,
+                                           text=True).stdout.split())
+    assert checked > 10_000_000 and bad == 0
