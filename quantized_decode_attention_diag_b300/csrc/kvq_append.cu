@@ -102,16 +102,18 @@ __device__ __forceinline__ void prefetch_chunk(const AppendParams& p, int c, uin
   const int grp = static_cast<int>(fastdiv(static_cast<uint32_t>(c), p.div_wpg));
   const int blk = c - grp * p.warps_per_group;
   const int h = grp >> 1, kv = grp & 1;
-  const long long rows = static_cast<long long>(p.B) * p.T;
-  const uint16_t* base = kv ? p.V : p.K;
-  const int ci = lane % LPR;
+  const int rows = p.B * p.T;                  // <= 2^28 (checked on the host)
+  const int ci = lane % LPR, k0 = lane / LPR;
+  const int rl = blk * 16 + k0;                // this lane's first row
+  // piece ci of row r is at (r Hkv + h) D elements + ci pieces; the rows a lane
+  // copies are RPI apart, RPI Hkv D elements
+  const uint4* src = reinterpret_cast<const uint4*>((kv ? p.V : p.K) +
+                                                    (static_cast<size_t>(rl) * p.Hkv + h) * D) + ci;
+  const size_t step = static_cast<size_t>(RPI) * p.Hkv * (D / 8);
 #pragma unroll
   for (int i = 0; i < 16 / RPI; ++i) {
-    const int k = RPI * i + lane / LPR;
-    const long long r = static_cast<long long>(blk) * 16 + k;
-    if (r < rows)
-      cp_async16(buf + k * (D / 8) + swz<D>(k, ci),
-                 reinterpret_cast<const uint4*>(base + (r * p.Hkv + h) * D) + ci);
+    const int k = RPI * i + k0;
+    if (rl + RPI * i < rows) cp_async16(buf + k * (D / 8) + swz<D>(k, ci), src + i * step);
   }
 }
 
