@@ -531,9 +531,11 @@ __device__ __forceinline__ void store_codes(uint8_t* dst, const uint32_t (&c)[2]
 // them to the cache page (for later calls) and to `pbuf` in shared memory
 // (K codes [KB], V codes [VB], K (s, z), V (s, z)), from which this launch's
 // staged copy of the page gets patched.  Same rule and same bits as kvq_append.
+// pid: the page table's entry for that page (read by the caller before the
+// launch-overlap wait; an id outside [0, num_pages) is reported and not written).
 template <int D>
 __device__ void step_append(const DecodeParams& p, int b, int h, int pos, int bk, int bv,
-                            const uint32_t (&tok)[D / 32], uint8_t* pbuf) {
+                            const uint32_t (&tok)[D / 32], uint8_t* pbuf, int pid) {
   constexpr int F = D / 16;
   const int lane = threadIdx.x & 31, half = lane >> 4, l = lane & 15;
   const int bits = half ? bv : bk;
@@ -563,7 +565,6 @@ __device__ void step_append(const DecodeParams& p, int b, int h, int pos, int bk
   uint32_t codes[2];
   __half sh, zh;
   rotate_quantize_halfwarp<D>(v, p.had_block, bits, codes, sh, zh);
-  const int pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pos / kPage);
   uint8_t* seg = nullptr;
   if (pid >= 0 && pid < p.num_pages) {
     seg = const_cast<uint8_t*>(p.pool) + static_cast<size_t>(pid) * p.geom.page_bytes +
@@ -701,6 +702,18 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   if (p.wait_log2 >= kWaitLimitLog2)
     for (int kk = 0; kk < nk && kk < NST; ++kk) issue(true, kk, pid_of(kk));
 
+  // decode step: the warp owning the page of the last quantized position
+  // quantizes the token there (after the wait) while its first copies are in
+  // flight; that page's id is read now (the page table is an input)
+  int kpatch = -1, step_pid = -1;
+  if (!KPC && p.step && lq > 0) {   // (the key-per-channel mode appends before the launch)
+    const int pl = npages - 1;
+    if (pl >= pg0 && pl < pg1 && (pl - pg0) % kDecodeWarps == warp) {
+      kpatch = (pl - pg0) / kDecodeWarps;
+      step_pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pl);
+    }
+  }
+
   // with programmatic dependent launch, everything above may overlap the
   // previous kernel; q and the new token are its results
   grid_wait();
@@ -709,17 +722,8 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
     if (p.step) load_new_token<D>(p, b, h, tok);
   }
 
-  // decode step: the warp owning the page of the last quantized position
-  // quantizes the token there while its first copies are in flight
-  int kpatch = -1;
   uint8_t* pbuf = reinterpret_cast<uint8_t*>(sm.cpart);   // free until the warps merge
-  if (!KPC && p.step && lq > 0) {   // (the key-per-channel mode appends before the launch)
-    const int pl = npages - 1;
-    if (pl >= pg0 && pl < pg1 && (pl - pg0) % kDecodeWarps == warp) {
-      kpatch = (pl - pg0) / kDecodeWarps;
-      step_append<D>(p, b, h, lq - 1, BK, BV, tok, pbuf);
-    }
-  }
+  if (kpatch >= 0) step_append<D>(p, b, h, lq - 1, BK, BV, tok, pbuf, step_pid);
   const int pslot = (lq - 1) % kPage;
 
   // key-per-channel codes of 2 bits are -1, 0 or 1, so c s is exact in fp16:
