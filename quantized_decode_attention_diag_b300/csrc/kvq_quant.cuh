@@ -69,10 +69,26 @@ __device__ __forceinline__ void load_row_top(const uint16_t* row, int u, float (
 // order: stage hs pairs (i, i + hs); NB == 1: no rotation, u = x).  When the
 // block spans both halves (NB > D / 2) the caller has applied the top stage
 // already (load_row_top).
+// Blocks no wider than a quarter row (2 <= NB <= D / 4) put elements j and
+// j + D / 4 of a lane's half in different blocks that take the same stages, so
+// every stage runs on the packed pairs (v[j], v[j + D/4]); each element still
+// sees the same additions in the same order.
+template <int D, int NB>
+constexpr bool kCrossPairs = NB >= 2 && NB <= D / 4;
+
 template <int D, int NB>
 __device__ __forceinline__ void rotate_half(float (&v)[D / 2]) {
   constexpr int E = D / 2;                 // elements per lane
   constexpr int IN_REG = NB < E ? NB : E;
+  if constexpr (kCrossPairs<D, NB>) {
+#pragma unroll
+    for (int hs = 1; hs < NB; hs <<= 1) {
+#pragma unroll
+      for (int j = 0; j < E / 2; ++j)
+        if (!(j & hs)) addsub2(v[j], v[j + E / 2], v[j + hs], v[j + hs + E / 2]);
+    }
+    return;
+  }
   if constexpr (NB >= 2) {
 #pragma unroll
     for (int e = 0; e < E; e += 2) {  // hs = 1
@@ -162,16 +178,31 @@ __device__ __forceinline__ void rotate_quantize_half(float (&v)[D / 2], int u,
   uint32_t ksum = 0;
 #pragma unroll
   for (int i = 0; i < CPW; ++i) ksum += kMagicBits << (BITS * i);
+  if constexpr (kCrossPairs<D, NB>) {
+    // the rotation's pairs (v[j], v[j + E/2]): codes j and j + E/2 sit at the
+    // same place of words E/2 / CPW apart
+    static_assert((E / 2) % CPW == 0, "half of a lane's elements fill whole words");
 #pragma unroll
-  for (int w = 0; w < NW; ++w) {
-    uint32_t acc = 0u - ksum;
+    for (int w = 0; w < NW; ++w) words[w] = 0u - ksum;
 #pragma unroll
-    for (int i = 0; i < CPW; i += 2) {
+    for (int j = 0; j < E / 2; ++j) {
       uint32_t f0, f1;
-      subfma2(v[w * CPW + i], v[w * CPW + i + 1], zf, inv, kMagicRound, f0, f1);
-      acc += (f0 << (BITS * i)) + (f1 << (BITS * (i + 1)));
+      subfma2(v[j], v[j + E / 2], zf, inv, kMagicRound, f0, f1);
+      words[j / CPW] += f0 << (BITS * (j % CPW));
+      words[(j + E / 2) / CPW] += f1 << (BITS * (j % CPW));
     }
-    words[w] = acc;
+  } else {
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      uint32_t acc = 0u - ksum;
+#pragma unroll
+      for (int i = 0; i < CPW; i += 2) {
+        uint32_t f0, f1;
+        subfma2(v[w * CPW + i], v[w * CPW + i + 1], zf, inv, kMagicRound, f0, f1);
+        acc += (f0 << (BITS * i)) + (f1 << (BITS * (i + 1)));
+      }
+      words[w] = acc;
+    }
   }
   (void)M;
 }
