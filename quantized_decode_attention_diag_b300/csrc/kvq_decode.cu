@@ -688,12 +688,15 @@ __device__ void quant_split(const DecodeParams& p, const Smem& sm, int b, int h,
   const uint32_t st0 = smem_u32(stages);        // shared-window address of stage 0
   uint64_t* bars = sm.bars + warp * NST;
   const uint8_t* head_base = p.pool + p.geom.head_off[h];
-  const long long page_bytes = p.geom.page_bytes;
+  // a page holds at most 64 heads' segments (< 1 MB): its byte offset is one
+  // 32 x 32 -> 64-bit multiply-add per copy
+  const uint32_t page_bytes = static_cast<uint32_t>(p.geom.page_bytes);
   // lane 0 issues the copy of page `pid` (already validated) into `slot` when
   // `go` (predicated, no branch)
   const uint32_t bars0 = smem_u32(bars);
   auto issue = [&](bool go, int slot, int pid) {
-    bulk_g2s_if(go && lane == 0, st0 + slot * stage_bytes, head_base + pid * page_bytes, CHUNK,
+    bulk_g2s_if(go && lane == 0, st0 + slot * stage_bytes,
+                head_base + static_cast<uint32_t>(pid) * static_cast<size_t>(page_bytes), CHUNK,
                 bars0 + 8u * slot);
   };
   // start streaming before the query prologue (with a shortened copy wait, a
