@@ -1627,65 +1627,83 @@ __device__ __forceinline__ void ldcg_vec(const float* ptr, float (&v)[E]) {
 }
 
 // Ticket mode.  Warp i merges query head i of (b, h) over its NS global
-// partials: the softmax weights of the splits (lane k holds split s0 + k of
-// each group of 32), the weighted sum of the quantized splits' rotated
-// accumulators (E dims per lane), the inverse rotation x = H u / n, the window
-// split's accumulator (already in the model's basis), and o.  Loads are
-// grouped so that a few round trips to L2 cover any split count.
+// partials (L2-resident: this launch wrote them):
+//   1. every partial's m and l in one pass (lane k holds splits k + 32 j, all
+//      loads in flight at once), the maximum, the weights 2^(m_s - M) -- kept
+//      in shared memory (`wsm`, the free stage area) for the next step -- and L;
+//   2. the weighted sum of the quantized splits' rotated accumulators (E dims
+//      per lane, kCombineRows rows in flight per lane);
+//   3. the inverse rotation x = H u / n, the window or reserve splits'
+//      accumulators (already in the model's basis), and o.
+constexpr int kMaxNS = kMaxSplits + 4;      // splits + window / reserve CTAs
+constexpr int kCombineRows = 16;
 template <int D>
-__device__ void combine_global(const DecodeParams& p, int b, int h, const float* parts) {
+__device__ void combine_global(const DecodeParams& p, const Smem& sm, int b, int h,
+                               const float* parts) {
   constexpr int E = D / 32;
   constexpr int PS = kMaxGroup * (D + 2);   // floats per partial
-  constexpr int UN = 8;                     // partial rows in flight at once
+  constexpr int UN = kCombineRows;
+  constexpr int NJ = (kMaxNS + 31) / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= p.G) return;
   const int i = warp, NS = p.NS, nq = p.S;
-  float mm = -CUDART_INF_F;
-  for (int s = lane; s < NS; s += 32) mm = fmaxf(mm, __ldcg(part_m<D>(parts + s * PS) + i));
-  mm = warp_max(mm);
-  float ll = 0.f, acc[E];
+  float* wsm = reinterpret_cast<float*>(sm.area) + i * kMaxNS;
+  float ms[NJ], ls[NJ];
 #pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int s0 = 0; s0 < NS; s0 += 32) {
-    float w = 0.f;
-    if (s0 + lane < NS) {
-      const float ms = __ldcg(part_m<D>(parts + (s0 + lane) * PS) + i);
-      if (ms != -CUDART_INF_F) {
-        w = exp2f(ms - mm);
-        ll = __fmaf_rn(w, __ldcg(part_l<D>(parts + (s0 + lane) * PS) + i), ll);
-      }
+  for (int j = 0; j < NJ; ++j) {
+    const int s = lane + 32 * j;
+    ms[j] = -CUDART_INF_F;
+    ls[j] = 0.f;
+    if (s < NS) {
+      ms[j] = __ldcg(part_m<D>(parts + s * PS) + i);
+      ls[j] = __ldcg(part_l<D>(parts + s * PS) + i);
     }
-    const int cnt = min(32, nq - s0);   // quantized splits of this group
-    for (int k0 = 0; k0 < cnt; k0 += UN) {
-      float rows[UN][E];
+  }
+  float mm = ms[0];
 #pragma unroll
-      for (int k = 0; k < UN; ++k) {
-        if (k0 + k < cnt) {
-          ldcg_vec<E>(part_acc<D>(parts + (s0 + k0 + k) * PS, i) + E * lane, rows[k]);
-        } else {
+  for (int j = 1; j < NJ; ++j) mm = fmaxf(mm, ms[j]);
+  mm = warp_max(mm);
+  float ll = 0.f;
 #pragma unroll
-          for (int e = 0; e < E; ++e) rows[k][e] = 0.f;
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < UN; ++k) {
-        const float wk = __shfl_sync(kFullMask, w, (k0 + k) & 31);
-        const float wv = k0 + k < cnt ? wk : 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(wv, rows[k][e], acc[e]);
-      }
+  for (int j = 0; j < NJ; ++j) {
+    const int s = lane + 32 * j;
+    if (s < NS) {
+      const float w = ms[j] == -CUDART_INF_F ? 0.f : exp2f(ms[j] - mm);
+      ll = __fmaf_rn(w, ls[j], ll);
+      wsm[s] = w;
     }
   }
   ll = warp_sum(ll);
+  __syncwarp();
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int k0 = 0; k0 < nq; k0 += UN) {
+    float rows[UN][E];
+#pragma unroll
+    for (int k = 0; k < UN; ++k) {
+      if (k0 + k < nq) {
+        ldcg_vec<E>(part_acc<D>(parts + (k0 + k) * PS, i) + E * lane, rows[k]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) rows[k][e] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < UN; ++k) {
+      const float wv = k0 + k < nq ? wsm[k0 + k] : 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(wv, rows[k][e], acc[e]);
+    }
+  }
   warp_fwht<E>(acc, p.had_block);
   const float inv_nb = 1.f / static_cast<float>(p.had_block);
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] *= inv_nb;
   // the unrotated partials (window, reserve) after the quantized ones
   for (int s = nq; s < NS; ++s) {
-    const float ms = __ldcg(part_m<D>(parts + s * PS) + i);
-    if (ms == -CUDART_INF_F) continue;
-    const float ws = exp2f(ms - mm);
+    const float ws = wsm[s];
+    if (ws == 0.f) continue;
     float row[E];
     ldcg_vec<E>(part_acc<D>(parts + s * PS, i) + E * lane, row);
 #pragma unroll
@@ -1885,7 +1903,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeMinBlocks) decode_kernel(cons
   __syncthreads();
   if (*sm.flag) {
     __threadfence();
-    combine_global<D>(p, b, h, parts);
+    combine_global<D>(p, sm, b, h, parts);
     if (tid == 0) p.counters[b * p.Hkv + h] = 0u;
   }
 }
@@ -1898,8 +1916,10 @@ size_t smem_bytes(const DecodeParams& p) {
   const size_t win = p.lq_w ? static_cast<size_t>(kMaxGroup + 1) * 3 * p.lq_w * 4
                             : (p.R > 0 ? win_bytes(p.R, D) : 0);
   const size_t merge = static_cast<size_t>(merge_floats<D>()) * 4;   // shares the area
+  const size_t weights = static_cast<size_t>(kMaxGroup) * kMaxNS * 4;  // ticket combine
   size_t area = stages > win ? stages : win;
   if (merge > area) area = merge;
+  if (weights > area) area = weights;
   return header_bytes(D, rbuf_ctas(p.cluster, p.NS)) + area;
 }
 
