@@ -1955,7 +1955,7 @@ cudaError_t launch_d(const DecodeParams& p, cudaStream_t s) {
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   unsigned n = 0;
-  if (p.cluster) {
+  if (p.cluster && p.NS > 1) {   // a lone CTA is a cluster of one without the attribute
     attr[n].id = cudaLaunchAttributeClusterDimension;
     attr[n].val.clusterDim.x = p.NS;
     attr[n].val.clusterDim.y = 1;
