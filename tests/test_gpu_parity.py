@@ -150,6 +150,17 @@ def test_decode_tiny_fp32_query():
     pr.decode_check(0, q, pt, np.array([256], np.int32), q_fp32=True)
 
 
+@pytest.mark.parametrize("window", [0, 128])
+def test_decode_split_limit_ticket_merge(window):
+    # one sequence, one KV head (4 query heads), 65536 tokens: the wave leaves
+    # this unit all 592 slots, so it takes the split limit, 256 splits of 16
+    # pages (257 CTAs with the window), merged through global memory by the
+    # last CTA -- the combine's largest partial count
+    pr, pt, k, v = _filled_pair(1, 128, 128, (4, 2), [65536], window=window)
+    q = queries(1003, 0, 1, 4, 128, False)
+    pr.decode_check(0, q, pt, np.array([65536], np.int32))
+
+
 @pytest.mark.parametrize("lens", [[1, 300, 77], [4096, 4000], [16, 17, 15, 0]])
 def test_decode_gqa4_ragged(lens):
     pr, pt, k, v = _filled_pair(8, 128, 128, (4, 4), lens)
