@@ -136,3 +136,22 @@ def test_reserve_rows_hold_the_members():
         for h in range(hkv):
             assert np.array_equal(res[h, 0, row], k[0, p, h]), (p, h)
             assert np.array_equal(res[h, 1, row], v[0, p, h]), (p, h)
+
+
+def test_decode_split_limit_with_reserve():
+    # one sequence, one KV head (4 query heads), 65536 tokens, W = 128, K2V2: the
+    # wave leaves the unit all 592 slots, so it takes 256 splits of 16 pages and
+    # four reserve CTAs -- 260 partials, the ticket combine's largest count
+    w, d, hkv, g, n = 128, 128, 1, 4, 65536
+    mp = n // 16
+    pt = page_table(93, 1, mp)
+    btab = np.array([[[2, 2]]])
+    c = kvq.Cache(1, hkv, d, 128, btab, mp, max_batch=1, logquant_w=w)
+    k = kv_tokens(93, 0, 1, n, hkv, d, 4, 10.0, 50.0)
+    v = kv_tokens(93, 1, 1, n, hkv, d, 4, 10.0, 50.0)
+    c.append(0, _dev(k), _dev(v), _dev(pt, None), _dev(np.zeros(1, np.int32), None),
+             window_row=0)
+    torch.cuda.synchronize()
+    assert c.get_status() == 0
+    q = queries(93, 0, 1, g * hkv, d, False)
+    _check(c, btab, q, pt, np.array([n], np.int32), k, v, w)
