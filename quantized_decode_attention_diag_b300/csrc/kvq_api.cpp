@@ -160,17 +160,19 @@ struct Plan {
 };
 
 // Resident decode CTAs per SM with `smem` bytes of shared memory (the
-// occupancy calculator's answer, cached per size, head_dim and mode); <= 0 when
-// none fits.
+// occupancy calculator's answer, cached per size, head_dim and mode: a plan
+// asks for one or two sizes, and a model's layers may differ in stage size);
+// <= 0 when none fits.
+constexpr int kOccupancyCache = 16;
 int resident_ctas(const kvq_cache* c, size_t smem) {
-  static thread_local int cache_key[4] = {0, 0, 0, 0}, cache_val[4] = {0, 0, 0, 0};
+  static thread_local int cache_key[kOccupancyCache] = {}, cache_val[kOccupancyCache] = {};
   const int mode = decode_mode(c);
   const int key = (static_cast<int>(smem) * 2 + (c->head_dim == 128)) * 4 + mode + 1;
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < kOccupancyCache; ++i)
     if (cache_key[i] == key) return cache_val[i];
   const int bps = kvq::decode_blocks_per_sm(c->head_dim, smem, mode);
   if (bps > 0) {
-    for (int i = 3; i > 0; --i) {
+    for (int i = kOccupancyCache - 1; i > 0; --i) {
       cache_key[i] = cache_key[i - 1];
       cache_val[i] = cache_val[i - 1];
     }
