@@ -81,8 +81,9 @@ struct DecodeParams {
   int NS;                        // S + the window or LogQuant reserve CTAs (0 to 4)
   int pages_per_split;       // host plan (page-table width / S); the kernel uses the lengths
   int overlap;               // launched with programmatic stream serialization
-  int cluster;                   // 1: the NS CTAs of a unit form a cluster and merge
-                                 // through distributed shared memory (NS <= 8)
+  int cluster;                   // 1: the NS (<= 4) CTAs of a unit merge in CTA 0's
+                                 // shared memory -- a cluster when NS > 1, a lone CTA
+                                 // combining its own partial when NS = 1; 0: tickets
   int step;                      // 1: decode step -- the new token (k_new, v_new) is
                                  // appended by this launch (seq_lens include it)
   const uint16_t* k_new;         // step: bf16 [B][Hkv][D]
