@@ -2,6 +2,7 @@
 // split planning, kernel dispatch, and the RateQuant greedy allocator.
 #include <cuda_runtime_api.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -376,6 +377,10 @@ kvq_status append_impl(const kvq_cache* cache, int layer, const void* K, const v
   p.warps_per_group = static_cast<int>((static_cast<long long>(B) * T_new + 15) / 16);
   p.div_wpg = kvq::make_fastdiv(static_cast<uint32_t>(p.warps_per_group));
   p.div_T = kvq::make_fastdiv(static_cast<uint32_t>(T_new));
+  {
+    const long long cap = static_cast<long long>(max_pages) * kvq::kPage;
+    p.cap_tokens = cap > INT_MAX ? INT_MAX : static_cast<int>(cap);
+  }
   p.lq_w = cache->logquant_w;
   p.lq_a = cache->logquant_w ? kvq::lq_log2(cache->logquant_w) : 0;
   p.lq_rows = cache->logquant_w ? kvq::lq_rows(cache->logquant_w, p.lq_a) : 0;

@@ -56,9 +56,7 @@ __device__ __forceinline__ int row_len0(const AppendParams& p, const RowRef& rr)
 
 // Position the row quantizes (-1: none; see append_chunk).
 __device__ __forceinline__ int row_dst(const AppendParams& p, const RowRef& rr, int l0) {
-  if (l0 == INT_MIN || l0 < 0 ||
-      static_cast<long long>(l0) + p.T > static_cast<long long>(p.max_pages) * kPage)
-    return -1;
+  if (l0 < 0 || l0 > p.cap_tokens - p.T) return -1;   // (INT_MIN: past the batch)
   const int pos = l0 + rr.t, len = l0 + p.T;
   const int qlim = p.R ? max(0, len - p.R) : len;
   if (pos < qlim) return pos;
@@ -155,7 +153,7 @@ __device__ __forceinline__ void append_chunk(const AppendParams& p, const RowRef
   const int b = rr.b < 0 ? 0 : rr.b, t = rr.t;
   bool active = rr.b >= 0;
   if (active &&
-      (l0 < 0 || static_cast<long long>(l0) + p.T > static_cast<long long>(p.max_pages) * kPage)) {
+      (l0 < 0 || l0 > p.cap_tokens - p.T)) {
     if (u == 0) flag_status(p.status, KVQ_DEV_BAD_LENGTH);
     active = false;
   }
@@ -199,7 +197,9 @@ __device__ __forceinline__ void append_chunk(const AppendParams& p, const RowRef
       from_ring = nullptr;
       dst = -1;
     } else {
-      seg = p.pool + static_cast<size_t>(pid) * p.geom.page_bytes + p.geom.head_off[h];
+      // a page is under 1 MB: one 32 x 32 -> 64-bit multiply-add
+      seg = p.pool + static_cast<uint32_t>(pid) * static_cast<size_t>(
+                         static_cast<uint32_t>(p.geom.page_bytes)) + p.geom.head_off[h];
     }
   }
 

@@ -59,6 +59,8 @@ struct AppendParams {
   int max_pages, B, T, Hkv, R, num_pages;
   int warps_per_group;           // ceil(B * T / 16)
   FastDiv div_wpg, div_T;        // division by warps_per_group and by T
+  int cap_tokens;                // max_pages * 16, at most INT_MAX: a sequence fits
+                                 // the page table while l0 <= cap_tokens - T
   int lq_w, lq_a, lq_rows;       // LogQuant base window W (0: off), log2 W, reserve rows
                                  // per plane; `window` is then the reserve
   int kpc;                       // key-per-channel mode: R is then the ring's R + 16 rows
