@@ -20,6 +20,8 @@ the kernel's precision, see ``quantizer``):
                     recent-token window (and the key-per-channel mode's
                     page-at-a-time rule).
 * ``attention``  -- decode attention over the dequantized cache.
+* ``logquant``   -- LogQuant's log-spaced full-precision set B (token-by-token
+                    halving) and decode attention with B's positions in bf16.
 * ``allocator``  -- RateQuant greedy marginal-gain bit allocation, the
                     closed-form reverse-waterfilling optimum, brute force.
 * ``distortion`` -- fitting D(b) = alpha * beta^-b to measured MSE.
@@ -31,6 +33,7 @@ Hadamard rows and the window flush rule are conventions of this library; the
 pages do not fix them, so they are checked for self-consistency only.
 """
 from . import allocator, attention, cache, distortion, fp16, hadamard, layout, quantizer
+from . import logquant
 
 __all__ = ["allocator", "attention", "cache", "distortion", "fp16", "hadamard", "layout",
-           "quantizer"]
+           "logquant", "quantizer"]
